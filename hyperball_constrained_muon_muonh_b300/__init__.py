@@ -1,0 +1,168 @@
+"""MuonH optimizer step (momentum -> Newton-Schulz -> hyperball projection)
+on B300 (sm_103a), behind the C ABI in include/muonh.h.
+
+MuonH, as the Puro-2B digest (jacksunwei.me) describes it in "The load-bearing
+tricks aren't in the abstract": Muon's orthogonalised-momentum update, with
+every weight matrix held at the Frobenius norm it had at initialisation.
+
+PyTorch supplies device memory and the current stream; every step of the
+computation runs in libmuonh's CUDA kernels.
+
+    opt = MuonH(weights, lr=0.02)        # fp32 2-D CUDA tensors; captures r0
+    ...backward...
+    opt.step()                           # uses w.grad, or opt.step(grads)
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (FLAG_FP32_CHECK, FLAG_SYNC_DEBUG, STATUS_DEGENERATE_NORM,  # noqa: F401
+                   STATUS_KERNEL_TIMEOUT, STATUS_NONFINITE_INPUT, MuonHError, check, lib)
+
+NS_COEFFS = (3.4445, -4.7750, 2.0315)
+
+__all__ = ["MuonH", "capture_norms", "workspace_size", "step", "orthogonalize",
+           "orthogonalize_workspace_size", "get_status", "MuonHError", "NS_COEFFS"]
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check_tensor(t, name, dtype=torch.float32):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def matrix_array(weights, grads=None, moms=None, bf16=None):
+    """Build the muonh_matrix_t array for a list of 2-D tensors."""
+    n = len(weights)
+    arr = (_lib.MatrixT * n)()
+    for i, w in enumerate(weights):
+        if w.dim() != 2:
+            raise ValueError(f"matrix {i} is not 2-D")
+        _check_tensor(w, f"weights[{i}]")
+        arr[i].w = w.data_ptr()
+        arr[i].rows, arr[i].cols = w.shape
+        if grads is not None:
+            _check_tensor(grads[i], f"grads[{i}]")
+            arr[i].grad = grads[i].data_ptr()
+        if moms is not None:
+            _check_tensor(moms[i], f"moms[{i}]")
+            arr[i].mom = moms[i].data_ptr()
+        if bf16 is not None and bf16[i] is not None:
+            _check_tensor(bf16[i], f"bf16[{i}]", torch.bfloat16)
+            arr[i].w_bf16 = bf16[i].data_ptr()
+    return arr
+
+
+def capture_norms(weights, out=None, stream=None) -> torch.Tensor:
+    """r0[i] = ||weights[i]||_F (fp32 CUDA tensor), via muonh_capture_norms."""
+    arr = matrix_array(weights)
+    if out is None:
+        out = torch.empty(len(weights), dtype=torch.float32, device=weights[0].device)
+    check(lib.muonh_capture_norms(arr, len(weights), ctypes.c_void_p(out.data_ptr()), _stream(stream)),
+          "muonh_capture_norms")
+    return out
+
+
+def workspace_size(shapes_or_arr, flags: int = 0) -> int:
+    if isinstance(shapes_or_arr, ctypes.Array):
+        arr = shapes_or_arr
+    else:
+        arr = (_lib.MatrixT * len(shapes_or_arr))()
+        for i, (r, c) in enumerate(shapes_or_arr):
+            arr[i].rows, arr[i].cols = r, c
+            arr[i].w = 256  # any aligned non-null value: only shapes are read
+    out = ctypes.c_size_t()
+    check(lib.muonh_workspace_size(arr, len(arr), flags, ctypes.byref(out)), "muonh_workspace_size")
+    return out.value
+
+
+def step(arr, r0, lr, beta, ns_steps, coeffs, eps, flags, workspace, stream=None) -> None:
+    """One muonh_step call on a prebuilt matrix array."""
+    c = (ctypes.c_float * 3)(*coeffs)
+    check(lib.muonh_step(arr, len(arr), ctypes.c_void_p(r0.data_ptr()), lr, beta, ns_steps, c, eps, flags,
+                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream)),
+          "muonh_step")
+
+
+def orthogonalize_workspace_size(rows: int, cols: int, flags: int = 0) -> int:
+    out = ctypes.c_size_t()
+    check(lib.muonh_orthogonalize_workspace_size(rows, cols, flags, ctypes.byref(out)),
+          "muonh_orthogonalize_workspace_size")
+    return out.value
+
+
+def orthogonalize(x: torch.Tensor, ns_steps: int = 5, coeffs=NS_COEFFS, eps: float = 1e-7,
+                  flags: int = 0, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """Newton-Schulz of a fp32 CUDA matrix (muonh_orthogonalize)."""
+    _check_tensor(x, "x")
+    if out is None:
+        out = torch.empty_like(x)
+    r, c_ = x.shape
+    need = orthogonalize_workspace_size(r, c_, flags)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    cf = (ctypes.c_float * 3)(*coeffs)
+    check(lib.muonh_orthogonalize(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()), r, c_,
+                                  ns_steps, cf, eps, flags, ctypes.c_void_p(workspace.data_ptr()),
+                                  workspace.numel(), _stream(stream)), "muonh_orthogonalize")
+    return out
+
+
+def get_status(stream=None) -> int:
+    """Synchronise, read and clear the device status word."""
+    v = ctypes.c_uint32()
+    check(lib.muonh_get_status(ctypes.byref(v), _stream(stream)), "muonh_get_status")
+    return v.value
+
+
+class MuonH:
+    """MuonH over a fixed list of fp32 2-D CUDA weight matrices.
+
+    r0 (the radius each matrix is held at) is captured from the weights at
+    construction; momenta start at zero.  ``bf16_copies=True`` keeps a bf16
+    copy of every weight, refreshed by each step.
+    """
+
+    def __init__(self, weights, lr=0.02, beta=0.95, ns_steps=5, ns_coeffs=NS_COEFFS, eps=1e-7,
+                 bf16_copies=False, fp32_check=False):
+        self.weights = list(weights)
+        self.lr, self.beta, self.ns_steps, self.eps = float(lr), float(beta), int(ns_steps), float(eps)
+        self.ns_coeffs = tuple(float(v) for v in ns_coeffs)
+        self.flags = FLAG_FP32_CHECK if fp32_check else 0
+        self.moms = [torch.zeros_like(w) for w in self.weights]
+        self.bf16 = [torch.empty_like(w, dtype=torch.bfloat16) for w in self.weights] if bf16_copies else None
+        self.r0 = capture_norms(self.weights)
+        self._grads_ptrs = None
+        self._arr = None
+        self.workspace = torch.empty(workspace_size([tuple(w.shape) for w in self.weights], self.flags),
+                                     dtype=torch.uint8, device=self.weights[0].device)
+
+    def step(self, grads=None, stream=None) -> None:
+        if grads is None:
+            grads = [w.grad for w in self.weights]
+        ptrs = tuple(g.data_ptr() for g in grads)
+        if ptrs != self._grads_ptrs:
+            self._arr = matrix_array(self.weights, grads, self.moms, self.bf16)
+            self._grads_ptrs = ptrs
+        step(self._arr, self.r0, self.lr, self.beta, self.ns_steps, self.ns_coeffs, self.eps, self.flags,
+             self.workspace, stream)
+
+    def state_dict(self):
+        return {"moms": [m.clone() for m in self.moms], "r0": self.r0.clone()}
+
+    def load_state_dict(self, sd):
+        for m, src in zip(self.moms, sd["moms"]):
+            m.copy_(src)
+        self.r0.copy_(sd["r0"])

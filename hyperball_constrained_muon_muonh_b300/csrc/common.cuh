@@ -1,0 +1,100 @@
+// Internal definitions shared by the CUDA translation units of libmuonh.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/muonh.h"
+
+namespace muonh {
+
+// ---- per-matrix record handed to the elementwise kernels by value ----------
+// W-orientation pointers plus where the matrix's Newton-Schulz state lives in
+// the workspace (X orientation: s x l, row stride ld).
+struct MatDesc {
+    float* w;             // fp32 master weight, rows x cols
+    uint16_t* wb;         // bf16 copy or nullptr
+    const float* g;       // gradient
+    float* m;             // momentum
+    float* xs;            // fp32 NS state X (s x ld)
+    __nv_bfloat16* xo;    // bf16 NS operand X (s x ld)
+    int rows, cols;
+    int ld;               // row stride of xs / xo, elements
+    int chunk0;           // first chunk index of this matrix
+    int user_index;       // position in the caller's list (indexes r0)
+    int pad_;
+};
+static_assert(sizeof(MatDesc) == 72, "MatDesc layout");
+
+// Largest descriptor batch one launch carries in its parameter space
+// (sm_90+ kernels take up to 32764 bytes of parameters).
+constexpr int kMaxDescPerLaunch = 440;
+
+struct DescBatch {
+    int n;                // matrices in this batch
+    int first;            // global (bucket-order) index of d[0]
+    int chunk_begin;      // first chunk of this batch
+    int chunk_end;        // one past the last chunk of this batch
+    MatDesc d[kMaxDescPerLaunch];
+};
+static_assert(sizeof(DescBatch) <= 32000, "descriptor batch exceeds kernel parameter space");
+
+// Rows per chunk: a chunk is rows [r, r + chunk_rows) of one matrix (W
+// orientation).  Transposed matrices (rows > cols) use 64-row tiles.
+constexpr int kChunkElems = 65536;
+constexpr int kTile = 64;
+
+__host__ __device__ inline bool is_transposed(int rows, int cols) { return rows > cols; }
+
+__host__ __device__ inline int chunk_rows_for(int rows, int cols) {
+    if (is_transposed(rows, cols)) return kTile;
+    int cr = kChunkElems / (cols > 0 ? cols : 1);
+    return cr < 1 ? 1 : cr;
+}
+
+__host__ __device__ inline int chunks_for(int rows, int cols) {
+    int cr = chunk_rows_for(rows, cols);
+    return (rows + cr - 1) / cr;
+}
+
+// Per-matrix scalars in the workspace, indexed by bucket-order position.
+struct Scalars {
+    double* nu2;          // ||M||_F^2
+    double* rho2;         // ||W - lr*O||_F^2
+    float* inv_nu;        // 1 / (||M||_F + eps)
+    float* inv_nu2;       // inv_nu^2
+    float* factor;        // r0 / ||W - lr*O||_F
+    uint32_t* flags;      // per-matrix status bits
+};
+
+__device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Deterministic block sum (fixed tree); result valid in thread 0.
+template <int THREADS>
+__device__ __forceinline__ double block_sum(double v, double* smem) {
+    v = warp_sum(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) smem[warp] = v;
+    __syncthreads();
+    double r = 0.0;
+    if (warp == 0) {
+        r = lane < THREADS / 32 ? smem[lane] : 0.0;
+        r = warp_sum(r);
+    }
+    __syncthreads();
+    return r;
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+}  // namespace muonh

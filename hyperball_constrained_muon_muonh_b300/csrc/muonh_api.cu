@@ -1,0 +1,541 @@
+// C ABI of libmuonh: argument checks, the shape planner, workspace layout and
+// the launch sequence of one MuonH step.
+//
+// Step (Puro-2B digest, section "The load-bearing tricks aren't in the
+// abstract"; model card, section "Training"): momentum, Newton-Schulz
+// orthogonalisation of the momentum, then retraction of W - lr*O onto the
+// sphere of radius r0 = ||W0||_F.
+//
+// Planner: matrices are grouped into buckets of equal (s, l) = (short side,
+// long side); a tall matrix (rows > cols) is handled through its transpose,
+// so one bucket holds both orientations.  Each bucket's Newton-Schulz state
+// lives contiguously in the workspace ([G][s][ld] tensors), so one GEMM
+// launch covers the whole bucket through 3-D TMA descriptors.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "ns_gemm.h"
+
+namespace muonh {
+
+cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, cudaStream_t st);
+cudaError_t launch_momentum_finalize(const DescBatch& b, const double* partials, const Scalars& sc, float eps,
+                                     cudaStream_t st);
+cudaError_t launch_hyperball_norm(const DescBatch& b, float lr, double* partials, const float* o_scale,
+                                  cudaStream_t st);
+cudaError_t launch_hyperball_finalize(const DescBatch& b, const double* partials, const Scalars& sc,
+                                      const float* r0, cudaStream_t st);
+cudaError_t launch_hyperball_apply(const DescBatch& b, float lr, const Scalars& sc, const float* o_scale,
+                                   cudaStream_t st);
+cudaError_t launch_emit(const DescBatch& b, const float* o_scale, cudaStream_t st);
+cudaError_t launch_capture_norms(const DescBatch& b, float* r0, cudaStream_t st);
+cudaError_t status_word(uint32_t** ptr);
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+    g_last_error = msg;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+    g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
+    return MUONH_ERR_CUDA;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Bucket {
+    int s, l, G;
+    int first;            // bucket-order index of its first matrix
+    int ld_x, ld_s;
+    size_t off_xs, off_xo, off_af, off_aop;   // byte offsets in the workspace
+    size_t x_elems() const { return (size_t)G * s * ld_x; }
+    size_t s_elems() const { return (size_t)G * s * ld_s; }
+};
+
+struct Plan {
+    int n = 0;
+    std::vector<Bucket> buckets;
+    std::vector<int> order;       // bucket-order position -> caller index
+    std::vector<int> slot;        // bucket-order position -> slot in its bucket
+    std::vector<int> bucket_of;   // bucket-order position -> bucket index
+    std::vector<int> chunk0;      // bucket-order position -> first chunk
+    int total_chunks = 0;
+    size_t off_nu2, off_rho2, off_inv, off_inv2, off_fac, off_flags, off_partials;
+    size_t bytes = 0;
+};
+
+std::mutex g_plan_mu;
+std::map<std::string, Plan> g_plans;
+
+std::string plan_key(const int64_t* rc, int n, uint32_t flags) {
+    std::string k;
+    k.reserve(16 * n + 8);
+    k.append(reinterpret_cast<const char*>(&flags), sizeof flags);
+    k.append(reinterpret_cast<const char*>(rc), sizeof(int64_t) * 2 * n);
+    return k;
+}
+
+Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
+    (void)flags;
+    Plan P;
+    P.n = n;
+    std::map<std::pair<int, int>, std::vector<int>> groups;  // (s, l) -> caller indices
+    for (int i = 0; i < n; ++i) {
+        const int r = (int)rc[2 * i], c = (int)rc[2 * i + 1];
+        groups[{std::min(r, c), std::max(r, c)}].push_back(i);
+    }
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        off = align_up(off, 256);
+        const size_t o = off;
+        off += bytes;
+        return o;
+    };
+    P.off_nu2 = take(sizeof(double) * n);
+    P.off_rho2 = take(sizeof(double) * n);
+    P.off_inv = take(sizeof(float) * n);
+    P.off_inv2 = take(sizeof(float) * n);
+    P.off_fac = take(sizeof(float) * n);
+    P.off_flags = take(sizeof(uint32_t) * n);
+    // largest buckets first: their GEMMs are the longest launches
+    std::vector<std::pair<std::pair<int, int>, std::vector<int>>> gl(groups.begin(), groups.end());
+    std::stable_sort(gl.begin(), gl.end(), [](const auto& a, const auto& b) {
+        return (double)a.first.first * a.first.second * a.second.size() >
+               (double)b.first.first * b.first.second * b.second.size();
+    });
+    int chunk = 0;
+    for (auto& kv : gl) {
+        Bucket B;
+        B.s = kv.first.first;
+        B.l = kv.first.second;
+        B.G = (int)kv.second.size();
+        B.first = (int)P.order.size();
+        B.ld_x = (int)align_up(B.l, 8);
+        B.ld_s = (int)align_up(B.s, 8);
+        B.off_xs = take(sizeof(float) * B.x_elems());
+        B.off_xo = take(2 * sizeof(__nv_bfloat16) * B.x_elems());    // two bf16 buffers (ping-pong)
+        B.off_af = take(sizeof(float) * B.s_elems());
+        B.off_aop = take(2 * sizeof(__nv_bfloat16) * B.s_elems());   // A_op then B_op
+        int sl = 0;
+        for (int i : kv.second) {
+            P.order.push_back(i);
+            P.slot.push_back(sl++);
+            P.bucket_of.push_back((int)P.buckets.size());
+            P.chunk0.push_back(chunk);
+            chunk += chunks_for((int)rc[2 * i], (int)rc[2 * i + 1]);
+        }
+        P.buckets.push_back(B);
+    }
+    P.total_chunks = chunk;
+    P.off_partials = take(sizeof(double) * std::max(chunk, 1));
+    P.bytes = align_up(off, 256);
+    return P;
+}
+
+const Plan& get_plan(const int64_t* rc, int n, uint32_t flags) {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    const std::string key = plan_key(rc, n, flags & MUONH_FLAG_FP32_CHECK);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) return it->second;
+    if (g_plans.size() > 64) g_plans.clear();
+    return g_plans.emplace(key, build_plan(rc, n, flags)).first->second;
+}
+
+int check_shapes(const muonh_matrix_t* mats, int n, std::vector<int64_t>& rc, bool need_state) {
+    if (!mats) return fail(MUONH_ERR_INVALID_ARG, "mats is NULL");
+    if (n <= 0 || n > (1 << 22)) return fail(MUONH_ERR_INVALID_ARG, "n must be in [1, 4194304]");
+    rc.resize(2 * (size_t)n);
+    for (int i = 0; i < n; ++i) {
+        const muonh_matrix_t& m = mats[i];
+        char buf[160];
+        if (m.rows < 1 || m.cols < 1 || m.rows > MUONH_MAX_SIDE || m.cols > MUONH_MAX_SIDE) {
+            snprintf(buf, sizeof buf, "matrix %d: rows/cols must be in [1, %d]", i, MUONH_MAX_SIDE);
+            return fail(MUONH_ERR_INVALID_ARG, buf);
+        }
+        if (!m.w || !aligned16(m.w)) {
+            snprintf(buf, sizeof buf, "matrix %d: w is NULL or not 16-byte aligned", i);
+            return fail(MUONH_ERR_INVALID_ARG, buf);
+        }
+        if (need_state) {
+            if (!m.grad || !aligned16(m.grad) || !m.mom || !aligned16(m.mom)) {
+                snprintf(buf, sizeof buf, "matrix %d: grad/mom NULL or not 16-byte aligned", i);
+                return fail(MUONH_ERR_INVALID_ARG, buf);
+            }
+            if (m.w_bf16 && !aligned16(m.w_bf16)) {
+                snprintf(buf, sizeof buf, "matrix %d: w_bf16 not 16-byte aligned", i);
+                return fail(MUONH_ERR_INVALID_ARG, buf);
+            }
+        }
+        rc[2 * i] = m.rows;
+        rc[2 * i + 1] = m.cols;
+    }
+    return MUONH_OK;
+}
+
+Scalars scalars_of(const Plan& P, uint8_t* ws) {
+    Scalars sc;
+    sc.nu2 = reinterpret_cast<double*>(ws + P.off_nu2);
+    sc.rho2 = reinterpret_cast<double*>(ws + P.off_rho2);
+    sc.inv_nu = reinterpret_cast<float*>(ws + P.off_inv);
+    sc.inv_nu2 = reinterpret_cast<float*>(ws + P.off_inv2);
+    sc.factor = reinterpret_cast<float*>(ws + P.off_fac);
+    sc.flags = reinterpret_cast<uint32_t*>(ws + P.off_flags);
+    return sc;
+}
+
+// Descriptor batches in bucket order.  `x_in_alt` points the hyperball /
+// emit view of X at the second fp32 buffer (fp32 check mode, odd step count).
+std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, uint8_t* ws, bool x_in_alt,
+                                    bool with_momentum) {
+    std::vector<DescBatch> out;
+    const int n = P.n;
+    for (int b0 = 0; b0 < n; b0 += kMaxDescPerLaunch) {
+        out.emplace_back();
+        DescBatch& B = out.back();
+        B.n = std::min(kMaxDescPerLaunch, n - b0);
+        B.first = b0;
+        for (int k = 0; k < B.n; ++k) {
+            const int p = b0 + k;
+            const int u = P.order[p];
+            const Bucket& bk = P.buckets[P.bucket_of[p]];
+            const muonh_matrix_t& m = mats[u];
+            MatDesc& D = B.d[k];
+            D.w = m.w;
+            D.wb = with_momentum ? m.w_bf16 : nullptr;
+            D.g = with_momentum ? m.grad : m.w;
+            D.m = with_momentum ? m.mom : nullptr;
+            const size_t xoff = (size_t)P.slot[p] * bk.s * bk.ld_x;
+            float* xs = reinterpret_cast<float*>(ws + bk.off_xs);
+            float* x2 = reinterpret_cast<float*>(ws + bk.off_xo);
+            D.xs = (x_in_alt ? x2 : xs) + xoff;
+            D.xo = reinterpret_cast<__nv_bfloat16*>(ws + bk.off_xo) + xoff;
+            D.rows = (int)m.rows;
+            D.cols = (int)m.cols;
+            D.ld = bk.ld_x;
+            D.chunk0 = P.chunk0[p];
+            D.user_index = u;
+            D.pad_ = 0;
+        }
+        B.chunk_begin = P.chunk0[b0];
+        B.chunk_end = (b0 + B.n < n) ? P.chunk0[b0 + B.n] : P.total_chunks;
+    }
+    return out;
+}
+
+struct Sync {
+    bool on;
+    cudaStream_t st;
+    int check(cudaError_t e, const char* where) {
+        if (e != cudaSuccess) return cuda_fail(e, where);
+        if (on) {
+            e = cudaStreamSynchronize(st);
+            if (e != cudaSuccess) return cuda_fail(e, where);
+        }
+        return MUONH_OK;
+    }
+};
+
+// Newton-Schulz over every bucket.  Returns MUONH_OK or an error code;
+// *x_in_alt tells where the fp32 result sits (check mode).
+int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_steps, const float* coeffs,
+                      uint32_t flags, uint32_t* status, Sync& sy, bool* x_in_alt) {
+    const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
+    *x_in_alt = false;
+    for (int it = 0; it < ns_steps; ++it) {
+        for (const Bucket& B : P.buckets) {
+            float* xs = reinterpret_cast<float*>(ws + B.off_xs);
+            float* af = reinterpret_cast<float*>(ws + B.off_af);
+            const float* inv = sc.inv_nu + B.first;
+            const float* inv2 = sc.inv_nu2 + B.first;
+            if (check) {
+                float* x2 = reinterpret_cast<float*>(ws + B.off_xo);
+                float* bf = reinterpret_cast<float*>(ws + B.off_aop);
+                float* xc = (it & 1) ? x2 : xs;
+                float* xn = (it & 1) ? xs : x2;
+                const long long xstr = (long long)B.s * B.ld_x, sstr = (long long)B.s * B.ld_s;
+                SimtParams g{};
+                g.mode = NS_GRAM; g.G = B.G; g.M = B.s; g.N = B.s; g.K = B.l;
+                g.a = xc; g.lda = B.ld_x; g.a_bstride = xstr;
+                g.b = xc; g.ldb = B.ld_x; g.b_bstride = xstr;
+                g.out = af; g.ldo = B.ld_s; g.out_bstride = sstr;
+                g.scale = it == 0 ? inv2 : nullptr;
+                int r = sy.check(launch_simt_gemm(g, sy.st), "fp32 Gram launch");
+                if (r) return r;
+                SimtParams q{};
+                q.mode = NS_POLY; q.G = B.G; q.M = B.s; q.N = B.s; q.K = B.s;
+                q.a = af; q.lda = B.ld_s; q.a_bstride = sstr;
+                q.b = af; q.ldb = B.ld_s; q.b_bstride = sstr;
+                q.addend = af; q.ld_add = B.ld_s; q.add_bstride = sstr;
+                q.out = bf; q.ldo = B.ld_s; q.out_bstride = sstr;
+                q.cb = coeffs[1]; q.cc = coeffs[2];
+                r = sy.check(launch_simt_gemm(q, sy.st), "fp32 polynomial launch");
+                if (r) return r;
+                SimtParams a{};
+                a.mode = NS_APPLY; a.G = B.G; a.M = B.s; a.N = B.l; a.K = B.s;
+                a.a = bf; a.lda = B.ld_s; a.a_bstride = sstr;
+                a.b = xc; a.ldb = B.ld_x; a.b_bstride = xstr;
+                a.addend = xc; a.ld_add = B.ld_x; a.add_bstride = xstr;
+                a.out = xn; a.ldo = B.ld_x; a.out_bstride = xstr;
+                a.scale = it == 0 ? inv : nullptr;
+                a.ca = coeffs[0];
+                r = sy.check(launch_simt_gemm(a, sy.st), "fp32 apply launch");
+                if (r) return r;
+            } else {
+                __nv_bfloat16* xo0 = reinterpret_cast<__nv_bfloat16*>(ws + B.off_xo);
+                __nv_bfloat16* xo1 = xo0 + B.x_elems();
+                __nv_bfloat16* aop = reinterpret_cast<__nv_bfloat16*>(ws + B.off_aop);
+                __nv_bfloat16* bop = aop + B.s_elems();
+                __nv_bfloat16* xc = (it & 1) ? xo1 : xo0;
+                __nv_bfloat16* xn = (it & 1) ? xo0 : xo1;
+                const char* why = "";
+                GemmParams g{};
+                g.mode = NS_GRAM; g.G = B.G; g.M = B.s; g.N = B.s; g.K = B.l;
+                g.ld_x = B.ld_x; g.ld_s = B.ld_s;
+                g.a_f32 = af; g.sym_bf16 = aop;
+                g.scale = it == 0 ? inv2 : nullptr;
+                g.status = status;
+                cudaError_t e = tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, sy.st, &why);
+                int r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 Gram launch");
+                if (r) return r;
+                GemmParams q{};
+                q.mode = NS_POLY; q.G = B.G; q.M = B.s; q.N = B.s; q.K = B.s;
+                q.ld_x = B.ld_x; q.ld_s = B.ld_s;
+                q.a_f32 = af; q.sym_bf16 = bop;
+                q.cb = coeffs[1]; q.cc = coeffs[2];
+                q.status = status;
+                e = tc::launch_ns_gemm(q, aop, B.ld_s, aop, B.ld_s, sy.st, &why);
+                r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 polynomial launch");
+                if (r) return r;
+                GemmParams a{};
+                a.mode = NS_APPLY; a.G = B.G; a.M = B.s; a.N = B.l; a.K = B.s;
+                a.ld_x = B.ld_x; a.ld_s = B.ld_s;
+                a.x_state = xs;
+                a.x_op_out = (it + 1 < ns_steps) ? xn : nullptr;
+                a.scale = it == 0 ? inv : nullptr;
+                a.ca = coeffs[0];
+                a.status = status;
+                e = tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, sy.st, &why);
+                r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 apply launch");
+                if (r) return r;
+            }
+        }
+    }
+    if (check) *x_in_alt = (ns_steps & 1) != 0;
+    return MUONH_OK;
+}
+
+int check_scalars(int ns_steps, const float* coeffs, float eps, uint32_t flags) {
+    if (ns_steps < 0 || ns_steps > 64) return fail(MUONH_ERR_INVALID_ARG, "ns_steps must be in [0, 64]");
+    if (!coeffs) return fail(MUONH_ERR_INVALID_ARG, "ns_coeffs is NULL");
+    for (int i = 0; i < 3; ++i)
+        if (!std::isfinite(coeffs[i])) return fail(MUONH_ERR_INVALID_ARG, "ns_coeffs must be finite");
+    if (!std::isfinite(eps) || eps < 0.f) return fail(MUONH_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (flags & ~(uint32_t)(MUONH_FLAG_FP32_CHECK | MUONH_FLAG_SYNC_DEBUG))
+        return fail(MUONH_ERR_UNSUPPORTED, "unknown flag bits");
+    return MUONH_OK;
+}
+
+int check_workspace(void* ws, size_t ws_bytes, size_t need) {
+    if (!ws) return fail(MUONH_ERR_WORKSPACE, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(MUONH_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    if (ws_bytes < need) {
+        char buf[128];
+        snprintf(buf, sizeof buf, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+        return fail(MUONH_ERR_WORKSPACE, buf);
+    }
+    return MUONH_OK;
+}
+
+int get_status_ptr(uint32_t** p) {
+    cudaError_t e = status_word(p);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    return MUONH_OK;
+}
+
+}  // namespace
+}  // namespace muonh
+
+using namespace muonh;
+
+extern "C" {
+
+int muonh_version(void) { return 100; }
+
+const char* muonh_last_error(void) { return g_last_error.c_str(); }
+
+const char* muonh_status_string(int code) {
+    switch (code) {
+        case MUONH_OK: return "ok";
+        case MUONH_ERR_INVALID_ARG: return "invalid argument";
+        case MUONH_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MUONH_ERR_UNSUPPORTED: return "unsupported flag or shape";
+        case MUONH_ERR_CUDA: return "CUDA error";
+        default: return "unknown code";
+    }
+}
+
+int muonh_capture_norms(const muonh_matrix_t* mats, int n, float* r0_dev, void* stream) {
+    g_last_error.clear();
+    std::vector<int64_t> rc;
+    int r = check_shapes(mats, n, rc, false);
+    if (r) return r;
+    if (!r0_dev || (reinterpret_cast<uintptr_t>(r0_dev) & 3u))
+        return fail(MUONH_ERR_INVALID_ARG, "r0_dev is NULL or not 4-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int b0 = 0; b0 < n; b0 += kMaxDescPerLaunch) {
+        DescBatch B;
+        memset(&B, 0, sizeof B);
+        B.n = std::min(kMaxDescPerLaunch, n - b0);
+        B.first = b0;
+        for (int k = 0; k < B.n; ++k) {
+            B.d[k].w = mats[b0 + k].w;
+            B.d[k].rows = (int)mats[b0 + k].rows;
+            B.d[k].cols = (int)mats[b0 + k].cols;
+            B.d[k].user_index = b0 + k;
+        }
+        cudaError_t e = launch_capture_norms(B, r0_dev, st);
+        if (e != cudaSuccess) return cuda_fail(e, "capture_norms launch");
+    }
+    return MUONH_OK;
+}
+
+int muonh_workspace_size(const muonh_matrix_t* mats, int n, uint32_t flags, size_t* bytes) {
+    g_last_error.clear();
+    if (!bytes) return fail(MUONH_ERR_INVALID_ARG, "bytes is NULL");
+    std::vector<int64_t> rc;
+    int r = check_shapes(mats, n, rc, false);
+    if (r) return r;
+    *bytes = get_plan(rc.data(), n, flags).bytes;
+    return MUONH_OK;
+}
+
+int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr, float beta, int ns_steps,
+               const float ns_coeffs[3], float eps, uint32_t flags, void* workspace, size_t ws_bytes,
+               void* stream) {
+    g_last_error.clear();
+    std::vector<int64_t> rc;
+    int r = check_shapes(mats, n, rc, true);
+    if (r) return r;
+    if (!r0_dev || (reinterpret_cast<uintptr_t>(r0_dev) & 3u))
+        return fail(MUONH_ERR_INVALID_ARG, "r0_dev is NULL or not 4-byte aligned");
+    if (!std::isfinite(lr) || !std::isfinite(beta)) return fail(MUONH_ERR_INVALID_ARG, "lr and beta must be finite");
+    r = check_scalars(ns_steps, ns_coeffs, eps, flags);
+    if (r) return r;
+    const Plan& P = get_plan(rc.data(), n, flags);
+    r = check_workspace(workspace, ws_bytes, P.bytes);
+    if (r) return r;
+    uint32_t* status = nullptr;
+    r = get_status_ptr(&status);
+    if (r) return r;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Sync sy{(flags & MUONH_FLAG_SYNC_DEBUG) != 0, st};
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const Scalars sc = scalars_of(P, ws);
+    double* partials = reinterpret_cast<double*>(ws + P.off_partials);
+
+    std::vector<DescBatch> batches = make_batches(P, mats, ws, false, true);
+    for (const DescBatch& B : batches) {
+        r = sy.check(launch_momentum(B, beta, partials, st), "momentum launch");
+        if (r) return r;
+        r = sy.check(launch_momentum_finalize(B, partials, sc, eps, st), "momentum finalize launch");
+        if (r) return r;
+    }
+    bool x_alt = false;
+    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt);
+    if (r) return r;
+    if (x_alt) batches = make_batches(P, mats, ws, true, true);
+    const float* o_scale = ns_steps == 0 ? sc.inv_nu : nullptr;
+    for (const DescBatch& B : batches) {
+        r = sy.check(launch_hyperball_norm(B, lr, partials, o_scale, st), "hyperball norm launch");
+        if (r) return r;
+        r = sy.check(launch_hyperball_finalize(B, partials, sc, r0_dev, st), "hyperball finalize launch");
+        if (r) return r;
+        r = sy.check(launch_hyperball_apply(B, lr, sc, o_scale, st), "hyperball apply launch");
+        if (r) return r;
+    }
+    return MUONH_OK;
+}
+
+int muonh_orthogonalize_workspace_size(int64_t rows, int64_t cols, uint32_t flags, size_t* bytes) {
+    g_last_error.clear();
+    if (!bytes) return fail(MUONH_ERR_INVALID_ARG, "bytes is NULL");
+    if (rows < 1 || cols < 1 || rows > MUONH_MAX_SIDE || cols > MUONH_MAX_SIDE)
+        return fail(MUONH_ERR_INVALID_ARG, "rows/cols out of range");
+    const int64_t rc[2] = {rows, cols};
+    *bytes = get_plan(rc, 1, flags).bytes;
+    return MUONH_OK;
+}
+
+int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols, int ns_steps,
+                        const float ns_coeffs[3], float eps, uint32_t flags, void* workspace, size_t ws_bytes,
+                        void* stream) {
+    g_last_error.clear();
+    if (!in || !out || !aligned16(in) || !aligned16(out))
+        return fail(MUONH_ERR_INVALID_ARG, "in/out NULL or not 16-byte aligned");
+    if (rows < 1 || cols < 1 || rows > MUONH_MAX_SIDE || cols > MUONH_MAX_SIDE)
+        return fail(MUONH_ERR_INVALID_ARG, "rows/cols out of range");
+    int r = check_scalars(ns_steps, ns_coeffs, eps, flags);
+    if (r) return r;
+    const int64_t rc[2] = {rows, cols};
+    const Plan& P = get_plan(rc, 1, flags);
+    r = check_workspace(workspace, ws_bytes, P.bytes);
+    if (r) return r;
+    uint32_t* status = nullptr;
+    r = get_status_ptr(&status);
+    if (r) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Sync sy{(flags & MUONH_FLAG_SYNC_DEBUG) != 0, st};
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const Scalars sc = scalars_of(P, ws);
+    double* partials = reinterpret_cast<double*>(ws + P.off_partials);
+    muonh_matrix_t m{};
+    m.w = const_cast<float*>(in);
+    m.rows = rows;
+    m.cols = cols;
+    std::vector<DescBatch> batches = make_batches(P, &m, ws, false, false);
+    r = sy.check(launch_momentum(batches[0], 0.f, partials, st), "momentum launch");
+    if (r) return r;
+    r = sy.check(launch_momentum_finalize(batches[0], partials, sc, eps, st), "momentum finalize launch");
+    if (r) return r;
+    bool x_alt = false;
+    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt);
+    if (r) return r;
+    m.w = out;
+    batches = make_batches(P, &m, ws, x_alt, false);
+    r = sy.check(launch_emit(batches[0], ns_steps == 0 ? sc.inv_nu : nullptr, st), "emit launch");
+    return r;
+}
+
+int muonh_get_status(uint32_t* status_out, void* stream) {
+    g_last_error.clear();
+    if (!status_out) return fail(MUONH_ERR_INVALID_ARG, "status_out is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t* dev = nullptr;
+    int r = get_status_ptr(&dev);
+    if (r) return r;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaMemcpy(status_out, dev, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read status word");
+    e = cudaMemset(dev, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    return MUONH_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,509 @@
+// Newton-Schulz GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// operands staged by TMA.  One iteration of the orthogonalisation (Puro-2B
+// digest, section "The load-bearing tricks aren't in the abstract": Muon's
+// Newton-Schulz iterations) on a bucket of G same-shape s x l matrices X:
+//
+//   GRAM   A = X X^T           (s x s, K = l)  symmetric: upper tiles only,
+//                                               epilogue writes A fp32, A bf16
+//                                               and their mirror images
+//   POLY   B = b*A + c*A A     (s x s, K = s)  symmetric (A A = A A^T):
+//                                               upper tiles, B bf16 + mirror
+//   APPLY  X <- a*X + B X      (s x l, K = s)  X fp32 state read/written in the
+//                                               epilogue, bf16 operand copy out
+//
+// Persistent, warp-specialised kernel, one CTA per SM:
+//   warp 0      TMA producer (one thread) and TMEM allocator
+//   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, bf16 in,
+//               fp32 accumulate in TMEM, 128 x 256 tile, K step 16
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)..+31), fused arithmetic, global stores
+// Shared memory: 4-stage ring of (A 128x64, B 256x64) bf16 tiles, 128-byte
+// swizzle.  TMEM: two 256-column fp32 accumulators so the epilogue of one
+// tile overlaps the main loop of the next.  Every mbarrier wait gives up
+// after a time limit, sets MUONH_STATUS_KERNEL_TIMEOUT and unwinds.
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "ns_gemm.h"
+
+namespace muonh {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int TMEM_COLS = 2 * BN;               // 512
+constexpr int NUM_THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s per wait
+
+// ---- PTX wrappers ------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: false if the CTA has aborted or the time limit passed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kTimeoutNs) {
+                *abort_flag = 1;
+                raise_status(status, MUONH_STATUS_KERNEL_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                            int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format:
+// start>>4 at [0,14), LBO>>4 at [16,30), SBO>>4 at [32,46), fixed 0b001 at
+// [46,49), swizzle mode 2 = 128B at [61,64)).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+    d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D f32, A/B bf16, A K-major, B K- or
+// MN-major, N = 256, M = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) |
+           ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- tile scheduling ---------------------------------------------------------
+// Symmetric modes keep tile (mi, nj) iff it holds an element with col >= row:
+// (nj+1)*BN > mi*BM, i.e. nj >= mi/2 (BN = 2*BM).
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int local, int& mi, int& nj) {
+    if (p.mode == NS_APPLY) {
+        // column panels outermost: consecutive CTAs share the X_op panel
+        nj = local / p.tiles_m;
+        mi = local - nj * p.tiles_m;
+        return;
+    }
+    int m = 0;
+    for (;;) {
+        const int cnt = p.tiles_n - (m >> 1);
+        if (local < cnt) break;
+        local -= cnt;
+        ++m;
+    }
+    mi = m;
+    nj = (m >> 1) + local;
+}
+
+// ---- epilogues -----------------------------------------------------------------
+__device__ __forceinline__ void store_row32_f32(float* dst, const float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+
+__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        uint4 u;
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(v[i], v[i + 1]);
+        __nv_bfloat162 h1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(v[i + 4], v[i + 5]);
+        __nv_bfloat162 h3 = __floats2bfloat162_rn(v[i + 6], v[i + 7]);
+        u.x = *reinterpret_cast<uint32_t*>(&h0);
+        u.y = *reinterpret_cast<uint32_t*>(&h1);
+        u.z = *reinterpret_cast<uint32_t*>(&h2);
+        u.w = *reinterpret_cast<uint32_t*>(&h3);
+        *reinterpret_cast<uint4*>(dst + i) = u;
+    }
+}
+
+// One 32-column slice of one accumulator row: row i, columns j0..j0+31.
+__device__ __forceinline__ void epilogue_slice(const GemmParams& p, int g, int i, int j0, float (&v)[32]) {
+    if (i >= p.M) return;
+    const int ncols = p.N;
+    if (p.mode == NS_APPLY) {
+        const size_t base = (size_t)g * p.ld_x * p.M + (size_t)i * p.ld_x;
+        float* xs = p.x_state + base;
+        const float sc = p.scale ? p.scale[g] : 1.f;
+        if (j0 + 32 <= ncols) {
+#pragma unroll
+            for (int t = 0; t < 32; t += 4) {
+                float4 x = *reinterpret_cast<const float4*>(xs + j0 + t);
+                v[t] = sc * fmaf(p.ca, x.x, v[t]);
+                v[t + 1] = sc * fmaf(p.ca, x.y, v[t + 1]);
+                v[t + 2] = sc * fmaf(p.ca, x.z, v[t + 2]);
+                v[t + 3] = sc * fmaf(p.ca, x.w, v[t + 3]);
+            }
+            store_row32_f32(xs + j0, v);
+            if (p.x_op_out) store_row32_bf16(p.x_op_out + base + j0, v);
+        } else {
+            for (int t = 0; t < 32 && j0 + t < ncols; ++t) {
+                const float r = sc * fmaf(p.ca, xs[j0 + t], v[t]);
+                xs[j0 + t] = r;
+                if (p.x_op_out) p.x_op_out[base + j0 + t] = __float2bfloat16_rn(r);
+            }
+        }
+        return;
+    }
+    // symmetric GRAM / POLY: keep j >= i, write (i, j) and the mirror (j, i)
+    const size_t mbase = (size_t)g * p.ld_s * p.M;
+    if (p.mode == NS_GRAM) {
+        const float sc = p.scale ? p.scale[g] : 1.f;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) v[t] *= sc;
+    } else {
+        const float* a = p.a_f32 + mbase + (size_t)i * p.ld_s;
+        if (j0 + 32 <= ncols) {
+#pragma unroll
+            for (int t = 0; t < 32; t += 4) {
+                float4 x = *reinterpret_cast<const float4*>(a + j0 + t);
+                v[t] = fmaf(p.cb, x.x, p.cc * v[t]);
+                v[t + 1] = fmaf(p.cb, x.y, p.cc * v[t + 1]);
+                v[t + 2] = fmaf(p.cb, x.z, p.cc * v[t + 2]);
+                v[t + 3] = fmaf(p.cb, x.w, p.cc * v[t + 3]);
+            }
+        } else {
+            for (int t = 0; t < 32 && j0 + t < ncols; ++t) v[t] = fmaf(p.cb, a[j0 + t], p.cc * v[t]);
+        }
+    }
+    float* af = (p.mode == NS_GRAM) ? p.a_f32 + mbase : nullptr;
+    __nv_bfloat16* ob = p.sym_bf16 + mbase;
+    const bool full = (j0 >= i) && (j0 + 32 <= ncols);
+    if (full) {
+        if (af) store_row32_f32(af + (size_t)i * p.ld_s + j0, v);
+        store_row32_bf16(ob + (size_t)i * p.ld_s + j0, v);
+    } else {
+        for (int t = 0; t < 32; ++t) {
+            const int j = j0 + t;
+            if (j >= i && j < ncols) {
+                if (af) af[(size_t)i * p.ld_s + j] = v[t];
+                ob[(size_t)i * p.ld_s + j] = __float2bfloat16_rn(v[t]);
+            }
+        }
+    }
+    // mirror: for fixed t the warp's 32 lanes (consecutive i) write one
+    // contiguous run of row j.
+#pragma unroll 4
+    for (int t = 0; t < 32; ++t) {
+        const int j = j0 + t;
+        if (j > i && j < ncols) {
+            if (af) af[(size_t)j * p.ld_s + i] = v[t];
+            ob[(size_t)j * p.ld_s + i] = __float2bfloat16_rn(v[t]);
+        }
+    }
+}
+
+// ---- the kernel ----------------------------------------------------------------
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+               const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* smem_a = smem;
+    uint8_t* smem_b = smem + STAGES * A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(tfull0 + 8 * s, 1);
+            mbar_init(tempty0 + 8 * s, 128);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tm_a);
+        prefetch_tmap(&tm_b);
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total = p.G * p.tiles_per_mat;
+    const int num_kb = (p.K + BK - 1) / BK;
+    const bool b_mn = (p.mode == NS_APPLY);
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const int g = t / p.tiles_per_mat;
+            int mi, nj;
+            tile_coords(p, t - g * p.tiles_per_mat, mi, nj);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+                const uint32_t fb = full0 + 8 * stage;
+                mbar_expect_tx(fb, STAGE_BYTES);
+                const uint32_t sa = smem_u32(smem_a + stage * A_BYTES);
+                const uint32_t sb = smem_u32(smem_b + stage * B_BYTES);
+                tma_load_3d(sa, &tm_a, fb, kb * BK, mi * BM, g);
+                if (!b_mn) {
+                    tma_load_3d(sb, &tm_b, fb, kb * BK, nj * BN, g);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + c * (64 * BK * 2), &tm_b, fb, nj * BN + c * 64, kb * BK, g);
+                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok) {
+            // let copies already in flight land before the CTA exits
+            for (int s = 0; s < STAGES; ++s) {
+                const unsigned long long t0 = global_ns();
+                while (global_ns() - t0 < 20000000ull) {
+                    if (mbar_try_wait(full0 + 8 * s, 0) || mbar_try_wait(full0 + 8 * s, 1)) break;
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer ----------------
+        const uint32_t idesc = idesc_bf16(b_mn);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem_a + stage * A_BYTES);
+                const uint32_t sb = smem_u32(smem_b + stage * B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t ad = sdesc(sa + kk * 32, 16, 1024);
+                    const uint64_t bd = b_mn ? sdesc(sb + kk * 2048, 64 * BK * 2, 1024) : sdesc(sb + kk * 32, 16, 1024);
+                    mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                }
+                mma_commit(empty0 + 8 * stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            mma_commit(tfull0 + 8 * acc);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    } else if (warp >= 2) {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.status)) break;
+            tc_fence_after();
+            const int g = t / p.tiles_per_mat;
+            int mi, nj;
+            tile_coords(p, t - g * p.tiles_per_mat, mi, nj);
+            const int i = mi * BM + q * 32 + lane;
+            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            for (int c = 0; c < BN / 32; ++c) {
+                const int j0 = nj * BN + c * 32;
+                if (j0 >= p.N) break;  // warp-uniform
+                float v[32];
+                tmem_ld32(trow + c * 32, v);
+                if (c == BN / 32 - 1 || j0 + 32 >= p.N) {
+                    // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    mbar_arrive(tempty0 + 8 * acc);
+                }
+                epilogue_slice(p, g, i, j0, v);
+            }
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---- host side -------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// bf16 tensor [G][rows][ld] (cols valid), box {64, box_rows, 1}, 128B swizzle.
+static bool encode_bf16_3d(CUtensorMap* map, const void* base, int cols, int rows, int G, int ld, int box_rows) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)G};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)ld * 2 * (cuuint64_t)rows};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+static int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
+int tiles_per_matrix(int mode, int M, int N) {
+    const int tm = (M + BM - 1) / BM, tn = (N + BN - 1) / BN;
+    if (mode == NS_APPLY) return tm * tn;
+    int cnt = 0;
+    for (int m = 0; m < tm; ++m) cnt += tn - (m >> 1) > 0 ? tn - (m >> 1) : 0;
+    return cnt;
+}
+
+// Operand tensors: GRAM A = B = X_op [G][s][ld_x] (K = l);
+// POLY A = B = A_op [G][s][ld_s] (K = s);  APPLY A = B_op [G][s][ld_s],
+// B = X_op (MN-major: rows = k).
+cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld,
+                           cudaStream_t st, const char** why) {
+    CUtensorMap ta, tb;
+    // A operand: rows = M, cols = K
+    if (!encode_bf16_3d(&ta, a_op, p.K, p.M, p.G, a_ld, BM)) { *why = "cuTensorMapEncodeTiled (A) failed"; return cudaErrorInvalidValue; }
+    bool okb;
+    if (p.mode == NS_APPLY)  // B operand X_op: rows = K (= s), cols = N (= l), box 64 x 64
+        okb = encode_bf16_3d(&tb, b_op, p.N, p.K, p.G, b_ld, 64);
+    else                     // B operand: rows = N, cols = K
+        okb = encode_bf16_3d(&tb, b_op, p.K, p.N, p.G, b_ld, BN);
+    if (!okb) { *why = "cuTensorMapEncodeTiled (B) failed"; return cudaErrorInvalidValue; }
+    p.tiles_m = (p.M + BM - 1) / BM;
+    p.tiles_n = (p.N + BN - 1) / BN;
+    p.tiles_per_mat = tiles_per_matrix(p.mode, p.M, p.N);
+    const long long total = (long long)p.G * p.tiles_per_mat;
+    if (total <= 0) return cudaSuccess;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) { *why = "cudaFuncSetAttribute failed"; return e; }
+        attr_set = true;
+    }
+    const int grid = (int)(total < sm_count() ? total : sm_count());
+    ns_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace muonh

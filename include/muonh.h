@@ -1,0 +1,155 @@
+/*
+ * muonh.h -- C ABI of the B300 (sm_103a) MuonH optimizer-step library.
+ *
+ * MuonH (Puro-2B digest, jacksunwei.me, section "The load-bearing tricks
+ * aren't in the abstract", with its footnote 3 on the Hyperball / MuonH
+ * paper): Muon's Newton-Schulz-orthogonalised momentum update, followed by a
+ * projection that holds every weight matrix at the Frobenius norm it had at
+ * initialisation.  The Puro-2B model card (axforge.ai), section "Training",
+ * applies it with zero weight decay to the selected matrix weights and keeps
+ * master weights and optimizer state in FP32.
+ *
+ * One step over a list of matrices W (fp32, rows x cols, row-major), each
+ * with gradient G and momentum M (fp32, same shape) and radius r0:
+ *
+ *   M  <- beta*M + G                               (heavy-ball momentum)
+ *   X  <- M / (||M||_F + eps), transposed when rows > cols (so X is s x l,
+ *         s = min(rows, cols) <= l = max(rows, cols))
+ *   ns_steps times:  A = X X^T;  B = b*A + c*A A;  X <- a*X + B X
+ *         with (a, b, c) = ns_coeffs
+ *   O  <- X, transposed back
+ *   U  <- W - lr*O;   W <- r0 * U / ||U||_F;   W_bf16 <- bf16(W)  (RNE)
+ *
+ * The pages leave open the momentum form, the Newton-Schulz coefficients and
+ * step count, eps, the transpose rule and any update scaling; here they are
+ * explicit arguments (momentum form and transpose rule as above, update
+ * scale 1, no weight decay).
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are CUDA device (or managed) addresses on the current
+ *    device, 16-byte aligned.  Host pointers are plain host memory, read
+ *    before the call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call is stream-ordered and asynchronous unless stated.
+ *  - The caller owns every buffer, including the workspace.  The library
+ *    allocates no device memory; it keeps a host-side cache of plans (shape
+ *    lists and TMA descriptors) and one status word per device.
+ *  - Return codes are MUONH_* below.  On a non-zero return nothing was
+ *    launched, except MUONH_ERR_CUDA, which means a launch or a CUDA call
+ *    failed; muonh_last_error() then describes it (per host thread).
+ *  - Non-finite data is not a return code: kernels record it in the device
+ *    status word (MUONH_STATUS_*), read with muonh_get_status().
+ */
+#ifndef MUONH_H
+#define MUONH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---- */
+#define MUONH_OK                  0
+#define MUONH_ERR_INVALID_ARG     1  /* null/misaligned pointer, bad shape, bad scalar */
+#define MUONH_ERR_WORKSPACE       2  /* workspace missing, misaligned or too small */
+#define MUONH_ERR_UNSUPPORTED     3  /* flag or shape this build does not handle */
+#define MUONH_ERR_CUDA            4  /* a CUDA call or kernel launch failed */
+
+/* ---- device status bits (ORed over all matrices and calls until read) ---- */
+#define MUONH_STATUS_NONFINITE_INPUT  0x1u  /* ||M||_F non-finite: W left unchanged */
+#define MUONH_STATUS_DEGENERATE_NORM  0x2u  /* ||W - lr*O||_F zero or non-finite: W left unchanged */
+#define MUONH_STATUS_KERNEL_TIMEOUT   0x4u  /* a pipeline wait gave up; outputs of that call are invalid */
+
+/* ---- flags ---- */
+#define MUONH_FLAG_FP32_CHECK  0x1u  /* Newton-Schulz in fp32 CUDA-core GEMMs (accuracy check mode) */
+#define MUONH_FLAG_SYNC_DEBUG  0x4u  /* synchronise and check errors after every kernel */
+
+/* One weight matrix and its optimizer state.  All device pointers, fp32
+ * row-major rows x cols (row stride = cols elements), 16-byte aligned.
+ * w_bf16 may be NULL (no bf16 copy written); it holds bfloat16 bit patterns. */
+typedef struct muonh_matrix {
+    float*       w;       /* in/out: fp32 master weight                     */
+    uint16_t*    w_bf16;  /* out (optional): bf16 copy of the new weight    */
+    const float* grad;    /* in: gradient                                   */
+    float*       mom;     /* in/out: momentum (caller zeroes it at start)   */
+    int64_t      rows;    /* >= 1 */
+    int64_t      cols;    /* >= 1 */
+} muonh_matrix_t;
+
+/* Largest matrix side handled (rows and cols each <= this). */
+#define MUONH_MAX_SIDE 65536
+
+/*
+ * r0_dev[i] = ||W_i||_F (fp32; accumulated in fp64) for i < n, read from
+ * mats[i].w only.  Call once, at initialisation: the digest's MuonH
+ * paragraph fixes each matrix's norm at its initial value.  mats is a host
+ * array of n >= 1 entries (grad/mom/w_bf16 are ignored and may be NULL);
+ * r0_dev is a device array of n floats.  Needs no workspace.
+ */
+int muonh_capture_norms(const muonh_matrix_t* mats, int n, float* r0_dev, void* stream);
+
+/*
+ * Bytes of device workspace muonh_step needs for this list of shapes and
+ * flags, written to *bytes.  Depends only on the shapes, n and flags.
+ */
+int muonh_workspace_size(const muonh_matrix_t* mats, int n, uint32_t flags, size_t* bytes);
+
+/*
+ * One MuonH step over mats[0..n) (host array): momentum, Newton-Schulz,
+ * hyperball projection, as in the header comment.
+ *   r0_dev     device array of n radii (from muonh_capture_norms)
+ *   lr         step size eta (the effective, already-multiplied rate)
+ *   beta       momentum coefficient
+ *   ns_steps   Newton-Schulz iterations, 0..64
+ *   ns_coeffs  host array {a, b, c}
+ *   eps        added to ||M||_F before dividing, >= 0
+ *   flags      MUONH_FLAG_*
+ *   workspace  device buffer of >= muonh_workspace_size() bytes, 256-byte
+ *              aligned, owned by the caller, not read or written by anything
+ *              else while the step runs.  Its contents need no initialising.
+ * Matrices must not overlap one another.  A matrix whose momentum turns
+ * non-finite, or whose ||W - lr*O||_F is zero or non-finite, keeps its W
+ * (its momentum is still updated) and sets a status bit.
+ */
+int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev,
+               float lr, float beta, int ns_steps, const float ns_coeffs[3], float eps,
+               uint32_t flags, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Workspace bytes for muonh_orthogonalize of one rows x cols matrix.
+ */
+int muonh_orthogonalize_workspace_size(int64_t rows, int64_t cols, uint32_t flags, size_t* bytes);
+
+/*
+ * Newton-Schulz alone (the "X <- ... ; O <- X" lines of the header comment)
+ * on one fp32 rows x cols device matrix `in`, written to fp32 `out` (same
+ * shape; may equal `in`).  Same meaning of ns_steps, ns_coeffs, eps, flags
+ * and workspace as muonh_step.  A non-finite ||in||_F sets
+ * MUONH_STATUS_NONFINITE_INPUT and `out` is then unspecified.
+ */
+int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
+                        int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then copies the current device's status word to
+ * *status_out (host) and clears it.  Blocking.
+ */
+int muonh_get_status(uint32_t* status_out, void* stream);
+
+/* Static text for a return code. */
+const char* muonh_status_string(int code);
+
+/* Text of the last error on this host thread ("" if none). */
+const char* muonh_last_error(void);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int muonh_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUONH_H */

@@ -1,0 +1,111 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol
+include/muonh.h declares, rejects bad arguments before any launch, and sizes
+workspaces from shapes alone."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from hyperball_constrained_muon_muonh_b300 import _lib
+import hyperball_constrained_muon_muonh_b300 as mh
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(muonh_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_header_declarations_are_exported():
+    declared = _declared()
+    assert declared >= set(_lib.EXPORTS)
+    for name in declared:
+        assert hasattr(_lib.lib, name), name
+
+
+def test_version_and_strings():
+    assert _lib.lib.muonh_version() >= 100
+    assert _lib.lib.muonh_status_string(0) == b"ok"
+    assert _lib.lib.muonh_status_string(2).startswith(b"workspace")
+
+
+def _arr(shapes, ptr=256):
+    arr = (_lib.MatrixT * len(shapes))()
+    for i, (r, c) in enumerate(shapes):
+        arr[i].rows, arr[i].cols = r, c
+        arr[i].w = arr[i].grad = arr[i].mom = ptr
+    return arr
+
+
+COEFFS = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+
+
+def _step(arr, n=None, r0=256, lr=0.02, beta=0.95, steps=5, coeffs=COEFFS, eps=1e-7, flags=0, ws=256,
+          ws_bytes=1 << 40):
+    return _lib.lib.muonh_step(arr, len(arr) if n is None else n, ctypes.c_void_p(r0), lr, beta, steps, coeffs,
+                               eps, flags, ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_step_rejects_bad_arguments_before_launch():
+    good = _arr([(4, 4)])
+    assert _lib.lib.muonh_step(None, 1, None, 0.02, 0.95, 5, COEFFS, 1e-7, 0, None, 0, None) == _lib.ERR_INVALID_ARG
+    assert _step(good, n=0) == _lib.ERR_INVALID_ARG
+    assert _step(_arr([(0, 4)])) == _lib.ERR_INVALID_ARG
+    assert _step(_arr([(4, 70000)])) == _lib.ERR_INVALID_ARG
+    assert _step(_arr([(4, 4)], ptr=260)) == _lib.ERR_INVALID_ARG          # misaligned
+    assert _step(good, r0=0) == _lib.ERR_INVALID_ARG
+    assert _step(good, lr=float("nan")) == _lib.ERR_INVALID_ARG
+    assert _step(good, steps=-1) == _lib.ERR_INVALID_ARG
+    assert _step(good, steps=65) == _lib.ERR_INVALID_ARG
+    assert _step(good, coeffs=(ctypes.c_float * 3)(1.0, float("inf"), 0.0)) == _lib.ERR_INVALID_ARG
+    assert _step(good, eps=-1.0) == _lib.ERR_INVALID_ARG
+    assert _step(good, flags=0x80) == _lib.ERR_UNSUPPORTED
+    assert _step(good, ws=0) == _lib.ERR_WORKSPACE
+    assert _step(good, ws=512 + 16) == _lib.ERR_WORKSPACE
+    assert _step(good, ws_bytes=16) == _lib.ERR_WORKSPACE
+    assert b"workspace too small" in _lib.lib.muonh_last_error()
+    nullgrad = _arr([(4, 4)])
+    nullgrad[0].grad = None
+    assert _step(nullgrad) == _lib.ERR_INVALID_ARG
+
+
+def test_capture_and_orthogonalize_reject_bad_arguments():
+    assert _lib.lib.muonh_capture_norms(None, 1, None, None) == _lib.ERR_INVALID_ARG
+    assert _lib.lib.muonh_capture_norms(_arr([(4, 4)]), 1, None, None) == _lib.ERR_INVALID_ARG
+    o = _lib.lib.muonh_orthogonalize
+    assert o(None, None, 4, 4, 5, COEFFS, 1e-7, 0, None, 0, None) == _lib.ERR_INVALID_ARG
+    assert o(ctypes.c_void_p(256), ctypes.c_void_p(256), 0, 4, 5, COEFFS, 1e-7, 0, None, 0, None) \
+        == _lib.ERR_INVALID_ARG
+    assert o(ctypes.c_void_p(256), ctypes.c_void_p(256), 4, 4, 5, COEFFS, 1e-7, 0, None, 0, None) \
+        == _lib.ERR_WORKSPACE
+
+
+def test_workspace_size_layout():
+    sz = mh.workspace_size([(256, 128)])
+    # X fp32 + 2 X bf16 (128 x 256) + A fp32 + A/B bf16 (128 x 128), plus scalars
+    assert sz >= 128 * 256 * (4 + 4) + 128 * 128 * (4 + 4)
+    assert sz % 256 == 0
+    # a tall and a wide matrix of the same sides share one bucket
+    assert mh.workspace_size([(256, 128), (128, 256)]) < 2 * sz + 4096
+    # padding: l rounded up to 8 elements
+    assert mh.workspace_size([(3, 5)]) >= 3 * 8 * 8
+    # grows with the number of matrices, deterministic
+    assert mh.workspace_size([(64, 64)] * 10) == mh.workspace_size([(64, 64)] * 10)
+    with pytest.raises(mh.MuonHError):
+        mh.workspace_size([(0, 3)])
+
+
+def test_qwen3_2b_workspace_fits():
+    import muonh_workloads as wl
+    w = wl.qwen3_2b()
+    sz = mh.workspace_size(w.shapes)
+    assert 10e9 < sz < 20e9
+    assert w.n_params == 1_409_286_144
