@@ -1,0 +1,335 @@
+"""MuonH optimizer-step benchmark (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one full MuonH step (momentum, Newton-Schulz, hyperball projection)
+over every matrix of the workload, through the library's C ABI.  Default
+workload: the 2B-class set (28 Qwen3-style decoder layers, 196 matrices,
+1.409 G parameters).  value = steps/s over all ranks (each rank steps its own
+replica: weak scaling, no collective on the data path).
+
+Reported beside it:
+  roofline      the Newton-Schulz GEMM kernel (the dominant one): symmetric-
+                aware algorithmic TFLOP/s from CUDA events recorded by the
+                library around each launch, against the measured sustained
+                bf16 peak
+  cpu_baseline  the float64 oracle on this host, on one decoder layer's
+                matrices (1/28 of a step), scaled to steps/s of the full set
+  e2e           steps/s with gradients copied in from pinned host memory and
+                the status word read back every step
+  clocks        nvidia-smi samples taken during the timed region
+--impl reference times the oracle alone (the reference arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MuonH steps/s on a 2B param set (1 B300); NS GEMM % of bf16 tensor peak"
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16": 1800.0, "bf16_sustained": 1400.0, "source": "fallback"}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples in the background (every 200 ms)."""
+
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        mhz, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                mhz.append(float(parts[0]))
+                maxes.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        mhz.sort()
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def _ns_traffic_from_profiles():
+    """Per-launch DRAM bytes of the NS GEMM kernel from the committed ncu summary, if current."""
+    p = os.path.join(PROFILE_DIR, "ns_gemm_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d
+    except (OSError, ValueError):
+        return None
+
+
+def oracle_sample(work, repeats=1):
+    """Time the oracle on one decoder layer's matrices (or a bounded subset)."""
+    import numpy as np
+    from oracle import muonh as om
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
+    except Exception:  # threadpoolctl missing: report the host's logical cores
+        cores = os.cpu_count()
+    n_all = len(work.shapes)
+    if work.name.startswith("qwen3_2b"):
+        idx = list(range(7))            # one decoder layer: 1/28 of the step
+    elif work.name.startswith("batched"):
+        idx = list(range(64))
+    elif work.name.startswith("aspect"):
+        idx = [0, 4]
+    else:
+        idx = list(range(n_all))
+    ws = [w.numpy() for w in work.weights("cpu", idx)]
+    gs = [g.numpy() for g in work.grads(0, "cpu", idx)]
+    ms = [np.zeros_like(w) for w in ws]
+    r0 = om.capture_norms(ws)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        om.muonh_step(ws, gs, ms, r0, work.lr, work.beta, work.ns_steps, work.coeffs, work.eps)
+    dt = (time.perf_counter() - t0) / repeats
+    # scale by the workload's Newton-Schulz flops
+    def flops(shapes):
+        return sum(3 * min(r, c) ** 2 * max(r, c) + min(r, c) ** 3 for r, c in shapes)
+    frac = flops([work.shapes[i] for i in idx]) / flops(work.shapes)
+    steps_per_s = frac / dt
+    sample = f"oracle (NumPy float64) on {len(idx)} of {n_all} matrices, {repeats} step(s), {dt:.2f} s; " \
+             f"scaled by their share ({frac:.4f}) of the step's Newton-Schulz flops"
+    return steps_per_s, cores, sample
+
+
+def run_reference(args, work, world, rank):
+    if rank != 0:
+        return
+    v, cores, sample = oracle_sample(work)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": work.name, "matrices": len(work.shapes), "params": work.n_params},
+        "cpu_baseline": {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="qwen3_2b_28layers")
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    import muonh_workloads as wl
+    work = wl.ALL[args.workload]()
+    world, rank, local = _dist()
+
+    if args.impl == "reference":
+        run_reference(args, work, world, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    # the oracle's BLAS pool is started before any CUDA work
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(work)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    import hyperball_constrained_muon_muonh_b300 as mh
+
+    ws = work.weights(dev)
+    grads = [work.grads(t, dev) for t in range(2)]   # two gradient sets, alternated
+    opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps, ns_coeffs=work.coeffs,
+                   eps=work.eps, bf16_copies=True)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    for t in range(args.warmup):
+        opt.step(grads[t % 2])
+    torch.cuda.synchronize()
+    st = mh.get_status()
+    if st:
+        raise SystemExit(f"device status {st:#x} after warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    n_launch0 = mh.lib.muonh_launch_count()
+    mh.lib.muonh_profile_enable(1)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local) as clk:
+        barrier()
+        ev0.record(stream)
+        for t in range(args.steps):
+            opt.step(grads[t % 2])
+        ev1.record(stream)
+        barrier()
+    gpu_launches = mh.lib.muonh_launch_count() - n_launch0
+    ms_total = ev0.elapsed_time(ev1)
+    prof = mh.profile_read()
+    mh.lib.muonh_profile_enable(0)
+    if world > 1:
+        t_ = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t_, op=dist.ReduceOp.MAX)
+        ms_total = t_.item()
+    ms_step = ms_total / args.steps
+    value = world * args.steps / (ms_total / 1000.0)
+
+    # ---- end to end: host gradients in, status word out, every step ----
+    e2e = None
+    if not args.no_e2e:
+        host = [g.to("cpu").pin_memory() for g in grads[0]]
+        dev_g = grads[1]
+        h2d = sum(h.numel() * h.element_size() for h in host)
+        for _ in range(2):
+            for d, h in zip(dev_g, host):
+                d.copy_(h, non_blocking=True)
+            opt.step(dev_g)
+            mh.get_status()
+        e_steps = max(2, min(args.steps, 5))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            for d, h in zip(dev_g, host):
+                d.copy_(h, non_blocking=True)
+            opt.step(dev_g)
+            st = mh.get_status()          # synchronises; 4-byte device->host read
+        dt = time.perf_counter() - t0
+        if world > 1:
+            t_ = torch.tensor([dt], device=dev)
+            dist.all_reduce(t_, op=dist.ReduceOp.MAX)
+            dt = t_.item()
+        e2e = {"value": world * e_steps / dt, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": 4}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks = _peaks()
+    ns_kinds = ("ns_gram", "ns_poly", "ns_apply")
+    ns_ms = sum(prof[k]["ms"] for k in ns_kinds if k in prof)
+    ns_flops = sum(prof[k]["flops"] for k in ns_kinds if k in prof)
+    ns_launches = sum(prof[k]["launches"] for k in ns_kinds if k in prof)
+    achieved = ns_flops / (ns_ms / 1000.0) / 1e12 if ns_ms > 0 else 0.0
+    tr = _ns_traffic_from_profiles()
+    roofline = {
+        "bound": "tensor", "kernel": "ns_gemm_kernel (Gram, polynomial, apply launches)",
+        "achieved": achieved, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+        "frac": achieved / peaks["bf16_sustained"],
+        "peak_kind": f"bf16 dense sustained, {peaks['source']}",
+        "frac_of_burst": achieved / peaks["bf16"],
+        "traffic": tr["bytes_per_launch"] if tr and tr.get("current") else None,
+        "launches": ns_launches, "flops_per_launch": ns_flops / max(ns_launches, 1),
+        "ms_per_launch": ns_ms / max(ns_launches, 1),
+        "ns_share_of_step": ns_ms / max(ms_total, 1e-9),
+    }
+    hbm = {}
+    for k in ("momentum", "hyperball_norm", "hyperball_apply"):
+        if k in prof and prof[k]["ms"] > 0:
+            gbs = prof[k]["bytes"] / (prof[k]["ms"] / 1000.0) / 1e9
+            hbm[k] = {"GB/s": gbs, "frac": gbs / peaks["hbm_gbs"], "ms_per_step": prof[k]["ms"] / args.steps}
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": work.name, "matrices": len(work.shapes), "params": work.n_params,
+                   "ns_steps": work.ns_steps, "ns_coeffs": list(work.coeffs), "beta": work.beta, "lr": work.lr,
+                   "eps": work.eps, "state": "fp32 W/M/G + bf16 W copy; NS bf16 operands, fp32 state",
+                   "l2": "inputs larger than L2 (about 20 GB of optimizer state touched per step)",
+                   "parallelism": f"replica x{world}"},
+        "ns_tflops": achieved,
+        "roofline": roofline,
+        "hbm_kernels": hbm,
+        "gpu_launches": gpu_launches,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "kernels": {k: {"launches": v["launches"], "ms_per_step": v["ms"] / args.steps} for k, v in prof.items()},
+    }
+    if cpu is not None:
+        v, cores, sample = cpu
+        line["cpu_baseline"] = {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

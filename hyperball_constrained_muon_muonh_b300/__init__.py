@@ -26,7 +26,7 @@ from ._lib import (FLAG_FP32_CHECK, FLAG_SYNC_DEBUG, STATUS_DEGENERATE_NORM,  # 
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
 
 __all__ = ["MuonH", "capture_norms", "workspace_size", "step", "orthogonalize",
-           "orthogonalize_workspace_size", "get_status", "MuonHError", "NS_COEFFS"]
+           "orthogonalize_workspace_size", "get_status", "profile_read", "MuonHError", "NS_COEFFS"]
 
 
 def _stream(stream=None) -> ctypes.c_void_p:
@@ -125,6 +125,15 @@ def get_status(stream=None) -> int:
     v = ctypes.c_uint32()
     check(lib.muonh_get_status(ctypes.byref(v), _stream(stream)), "muonh_get_status")
     return v.value
+
+
+def profile_read() -> dict:
+    """Per-kernel totals recorded since muonh_profile_enable(1) (blocking)."""
+    buf = (_lib.ProfileEntry * 32)()
+    n = ctypes.c_int()
+    check(lib.muonh_profile_read(buf, 32, ctypes.byref(n)), "muonh_profile_read")
+    return {buf[i].name.decode(): {"launches": buf[i].launches, "ms": buf[i].ms, "flops": buf[i].flops,
+                                   "bytes": buf[i].bytes} for i in range(n.value)}
 
 
 class MuonH:

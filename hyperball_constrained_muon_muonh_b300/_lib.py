@@ -34,6 +34,7 @@ EXPORTS = (
     "muonh_capture_norms", "muonh_workspace_size", "muonh_step",
     "muonh_orthogonalize_workspace_size", "muonh_orthogonalize", "muonh_get_status",
     "muonh_status_string", "muonh_last_error", "muonh_version",
+    "muonh_profile_enable", "muonh_profile_read", "muonh_launch_count",
 )
 
 
@@ -46,6 +47,17 @@ class MatrixT(ctypes.Structure):
         ("mom", ctypes.c_void_p),
         ("rows", ctypes.c_int64),
         ("cols", ctypes.c_int64),
+    ]
+
+
+class ProfileEntry(ctypes.Structure):
+    """muonh_profile_entry_t"""
+    _fields_ = [
+        ("name", ctypes.c_char_p),
+        ("launches", ctypes.c_int64),
+        ("ms", ctypes.c_double),
+        ("flops", ctypes.c_double),
+        ("bytes", ctypes.c_double),
     ]
 
 
@@ -76,9 +88,13 @@ def _load():
     lib.muonh_last_error.argtypes = []
     lib.muonh_last_error.restype = ctypes.c_char_p
     lib.muonh_version.argtypes = []
+    lib.muonh_profile_enable.argtypes = [I]
+    lib.muonh_profile_read.argtypes = [ctypes.POINTER(ProfileEntry), I, ctypes.POINTER(I)]
+    lib.muonh_launch_count.argtypes = []
     for name in EXPORTS:
         if name not in ("muonh_status_string", "muonh_last_error"):
             getattr(lib, name).restype = ctypes.c_int
+    lib.muonh_launch_count.restype = ctypes.c_int64
     return lib
 
 

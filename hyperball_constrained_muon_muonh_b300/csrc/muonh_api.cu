@@ -16,6 +16,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <string>
@@ -54,6 +55,65 @@ int cuda_fail(cudaError_t e, const char* where) {
 }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---- tracing: per-kernel CUDA-event timing ---------------------------------
+enum Kind { K_MOMENTUM, K_MOM_FIN, K_GRAM, K_POLY, K_APPLY, K_HB_NORM, K_HB_FIN, K_HB_APPLY, K_EMIT, K_CAPTURE,
+            K_SIMT_GRAM, K_SIMT_POLY, K_SIMT_APPLY, K_COUNT };
+const char* const kKindName[K_COUNT] = {"momentum", "momentum_finalize", "ns_gram", "ns_poly", "ns_apply",
+                                        "hyperball_norm", "hyperball_finalize", "hyperball_apply", "emit",
+                                        "capture_norms", "fp32_gram", "fp32_poly", "fp32_apply"};
+
+std::atomic<long long> g_launches{0};
+
+struct Pending {
+    int kind;
+    cudaEvent_t a, b;
+    double flops, bytes;
+};
+
+struct Profiler {
+    std::mutex mu;
+    bool on = false;
+    std::vector<Pending> pending;
+    std::vector<cudaEvent_t> pool;
+    long long launches[K_COUNT] = {};
+    double ms[K_COUNT] = {}, flops[K_COUNT] = {}, bytes[K_COUNT] = {};
+    cudaEvent_t get() {
+        if (!pool.empty()) {
+            cudaEvent_t e = pool.back();
+            pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        cudaEventCreate(&e);
+        return e;
+    }
+};
+Profiler g_prof;
+
+// Brackets one launch: records the start event (when tracing) on construction
+// and the end event plus the work on done().
+struct Trace {
+    int kind;
+    cudaStream_t st;
+    cudaEvent_t a = nullptr;
+    Trace(int k, cudaStream_t s) : kind(k), st(s) {
+        ++g_launches;
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        if (g_prof.on) {
+            a = g_prof.get();
+            cudaEventRecord(a, st);
+        }
+    }
+    cudaError_t done(cudaError_t e, double flops, double bytes) {
+        if (!a) return e;
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        cudaEvent_t b = g_prof.get();
+        cudaEventRecord(b, st);
+        g_prof.pending.push_back({kind, a, b, flops, bytes});
+        return e;
+    }
+};
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Bucket {
@@ -235,6 +295,12 @@ std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, u
     return out;
 }
 
+double batch_elems(const DescBatch& b) {
+    double e = 0;
+    for (int k = 0; k < b.n; ++k) e += (double)b.d[k].rows * b.d[k].cols;
+    return e;
+}
+
 struct Sync {
     bool on;
     cudaStream_t st;
@@ -272,7 +338,13 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 g.b = xc; g.ldb = B.ld_x; g.b_bstride = xstr;
                 g.out = af; g.ldo = B.ld_s; g.out_bstride = sstr;
                 g.scale = it == 0 ? inv2 : nullptr;
-                int r = sy.check(launch_simt_gemm(g, sy.st), "fp32 Gram launch");
+                const double G = B.G, S = B.s, L = B.l;
+                int r;
+                {
+                    Trace tr(K_SIMT_GRAM, sy.st);
+                    r = sy.check(tr.done(launch_simt_gemm(g, sy.st), G * S * S * L, G * S * L * 4 + G * S * S * 4),
+                                 "fp32 Gram launch");
+                }
                 if (r) return r;
                 SimtParams q{};
                 q.mode = NS_POLY; q.G = B.G; q.M = B.s; q.N = B.s; q.K = B.s;
@@ -281,7 +353,11 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 q.addend = af; q.ld_add = B.ld_s; q.add_bstride = sstr;
                 q.out = bf; q.ldo = B.ld_s; q.out_bstride = sstr;
                 q.cb = coeffs[1]; q.cc = coeffs[2];
-                r = sy.check(launch_simt_gemm(q, sy.st), "fp32 polynomial launch");
+                {
+                    Trace tr(K_SIMT_POLY, sy.st);
+                    r = sy.check(tr.done(launch_simt_gemm(q, sy.st), G * S * S * S, G * S * S * 12),
+                                 "fp32 polynomial launch");
+                }
                 if (r) return r;
                 SimtParams a{};
                 a.mode = NS_APPLY; a.G = B.G; a.M = B.s; a.N = B.l; a.K = B.s;
@@ -291,7 +367,11 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 a.out = xn; a.ldo = B.ld_x; a.out_bstride = xstr;
                 a.scale = it == 0 ? inv : nullptr;
                 a.ca = coeffs[0];
-                r = sy.check(launch_simt_gemm(a, sy.st), "fp32 apply launch");
+                {
+                    Trace tr(K_SIMT_APPLY, sy.st);
+                    r = sy.check(tr.done(launch_simt_gemm(a, sy.st), 2 * G * S * S * L, G * S * S * 4 + G * S * L * 12),
+                                 "fp32 apply launch");
+                }
                 if (r) return r;
             } else {
                 __nv_bfloat16* xo0 = reinterpret_cast<__nv_bfloat16*>(ws + B.off_xo);
@@ -307,7 +387,13 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 g.a_f32 = af; g.sym_bf16 = aop;
                 g.scale = it == 0 ? inv2 : nullptr;
                 g.status = status;
-                cudaError_t e = tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, sy.st, &why);
+                const double G = B.G, S = B.s, L = B.l;
+                cudaError_t e;
+                {
+                    Trace tr(K_GRAM, sy.st);
+                    e = tr.done(tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, sy.st, &why), G * S * S * L,
+                                G * S * L * 2 + G * S * S * 6);
+                }
                 int r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 Gram launch");
                 if (r) return r;
                 GemmParams q{};
@@ -316,7 +402,11 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 q.a_f32 = af; q.sym_bf16 = bop;
                 q.cb = coeffs[1]; q.cc = coeffs[2];
                 q.status = status;
-                e = tc::launch_ns_gemm(q, aop, B.ld_s, aop, B.ld_s, sy.st, &why);
+                {
+                    Trace tr(K_POLY, sy.st);
+                    e = tr.done(tc::launch_ns_gemm(q, aop, B.ld_s, aop, B.ld_s, sy.st, &why), G * S * S * S,
+                                G * S * S * 8);
+                }
                 r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 polynomial launch");
                 if (r) return r;
                 GemmParams a{};
@@ -327,7 +417,11 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 a.scale = it == 0 ? inv : nullptr;
                 a.ca = coeffs[0];
                 a.status = status;
-                e = tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, sy.st, &why);
+                {
+                    Trace tr(K_APPLY, sy.st);
+                    e = tr.done(tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, sy.st, &why), 2 * G * S * S * L,
+                                G * S * S * 2 + G * S * L * (a.x_op_out ? 12 : 10));
+                }
                 r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 apply launch");
                 if (r) return r;
             }
@@ -406,7 +500,8 @@ int muonh_capture_norms(const muonh_matrix_t* mats, int n, float* r0_dev, void* 
             B.d[k].cols = (int)mats[b0 + k].cols;
             B.d[k].user_index = b0 + k;
         }
-        cudaError_t e = launch_capture_norms(B, r0_dev, st);
+        Trace tr(K_CAPTURE, st);
+        cudaError_t e = tr.done(launch_capture_norms(B, r0_dev, st), 0, batch_elems(B) * 4);
         if (e != cudaSuccess) return cuda_fail(e, "capture_norms launch");
     }
     return MUONH_OK;
@@ -449,9 +544,16 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
 
     std::vector<DescBatch> batches = make_batches(P, mats, ws, false, true);
     for (const DescBatch& B : batches) {
-        r = sy.check(launch_momentum(B, beta, partials, st), "momentum launch");
+        const double e = batch_elems(B);
+        {
+            Trace tr(K_MOMENTUM, st);
+            r = sy.check(tr.done(launch_momentum(B, beta, partials, st), 0, e * 18), "momentum launch");
+        }
         if (r) return r;
-        r = sy.check(launch_momentum_finalize(B, partials, sc, eps, st), "momentum finalize launch");
+        {
+            Trace tr(K_MOM_FIN, st);
+            r = sy.check(tr.done(launch_momentum_finalize(B, partials, sc, eps, st), 0, 0), "momentum finalize launch");
+        }
         if (r) return r;
     }
     bool x_alt = false;
@@ -460,11 +562,22 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     if (x_alt) batches = make_batches(P, mats, ws, true, true);
     const float* o_scale = ns_steps == 0 ? sc.inv_nu : nullptr;
     for (const DescBatch& B : batches) {
-        r = sy.check(launch_hyperball_norm(B, lr, partials, o_scale, st), "hyperball norm launch");
+        const double e = batch_elems(B);
+        {
+            Trace tr(K_HB_NORM, st);
+            r = sy.check(tr.done(launch_hyperball_norm(B, lr, partials, o_scale, st), 0, e * 8), "hyperball norm launch");
+        }
         if (r) return r;
-        r = sy.check(launch_hyperball_finalize(B, partials, sc, r0_dev, st), "hyperball finalize launch");
+        {
+            Trace tr(K_HB_FIN, st);
+            r = sy.check(tr.done(launch_hyperball_finalize(B, partials, sc, r0_dev, st), 0, 0),
+                         "hyperball finalize launch");
+        }
         if (r) return r;
-        r = sy.check(launch_hyperball_apply(B, lr, sc, o_scale, st), "hyperball apply launch");
+        {
+            Trace tr(K_HB_APPLY, st);
+            r = sy.check(tr.done(launch_hyperball_apply(B, lr, sc, o_scale, st), 0, e * 14), "hyperball apply launch");
+        }
         if (r) return r;
     }
     return MUONH_OK;
@@ -507,16 +620,28 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     m.rows = rows;
     m.cols = cols;
     std::vector<DescBatch> batches = make_batches(P, &m, ws, false, false);
-    r = sy.check(launch_momentum(batches[0], 0.f, partials, st), "momentum launch");
+    const double el = (double)rows * cols;
+    {
+        Trace tr(K_MOMENTUM, st);
+        r = sy.check(tr.done(launch_momentum(batches[0], 0.f, partials, st), 0, el * 10), "momentum launch");
+    }
     if (r) return r;
-    r = sy.check(launch_momentum_finalize(batches[0], partials, sc, eps, st), "momentum finalize launch");
+    {
+        Trace tr(K_MOM_FIN, st);
+        r = sy.check(tr.done(launch_momentum_finalize(batches[0], partials, sc, eps, st), 0, 0),
+                     "momentum finalize launch");
+    }
     if (r) return r;
     bool x_alt = false;
     r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt);
     if (r) return r;
     m.w = out;
     batches = make_batches(P, &m, ws, x_alt, false);
-    r = sy.check(launch_emit(batches[0], ns_steps == 0 ? sc.inv_nu : nullptr, st), "emit launch");
+    {
+        Trace tr(K_EMIT, st);
+        r = sy.check(tr.done(launch_emit(batches[0], ns_steps == 0 ? sc.inv_nu : nullptr, st), 0, el * 8),
+                     "emit launch");
+    }
     return r;
 }
 
@@ -537,5 +662,62 @@ int muonh_get_status(uint32_t* status_out, void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
     return MUONH_OK;
 }
+
+int muonh_profile_enable(int on) {
+    g_last_error.clear();
+    std::vector<Pending> drop;
+    {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        g_prof.on = on != 0;
+        if (on) {
+            drop.swap(g_prof.pending);
+            for (int k = 0; k < K_COUNT; ++k) {
+                g_prof.launches[k] = 0;
+                g_prof.ms[k] = g_prof.flops[k] = g_prof.bytes[k] = 0;
+            }
+        }
+    }
+    for (Pending& q : drop) {
+        cudaEventSynchronize(q.b);
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        g_prof.pool.push_back(q.a);
+        g_prof.pool.push_back(q.b);
+    }
+    return MUONH_OK;
+}
+
+int muonh_profile_read(muonh_profile_entry_t* out, int max_entries, int* n_out) {
+    g_last_error.clear();
+    if (!out || !n_out || max_entries < 0) return fail(MUONH_ERR_INVALID_ARG, "out/n_out NULL");
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    for (Pending& q : g_prof.pending) {
+        cudaError_t e = cudaEventSynchronize(q.b);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, q.a, q.b);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+        g_prof.launches[q.kind] += 1;
+        g_prof.ms[q.kind] += ms;
+        g_prof.flops[q.kind] += q.flops;
+        g_prof.bytes[q.kind] += q.bytes;
+        g_prof.pool.push_back(q.a);
+        g_prof.pool.push_back(q.b);
+    }
+    g_prof.pending.clear();
+    int n = 0;
+    for (int k = 0; k < K_COUNT && n < max_entries; ++k) {
+        if (g_prof.launches[k] == 0) continue;
+        out[n].name = kKindName[k];
+        out[n].launches = g_prof.launches[k];
+        out[n].ms = g_prof.ms[k];
+        out[n].flops = g_prof.flops[k];
+        out[n].bytes = g_prof.bytes[k];
+        ++n;
+    }
+    *n_out = n;
+    return MUONH_OK;
+}
+
+int64_t muonh_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"

@@ -148,6 +148,30 @@ const char* muonh_last_error(void);
 /* Library ABI version (major*10000 + minor*100 + patch). */
 int muonh_version(void);
 
+/* ---- tracing: per-kernel timing (no counterpart on the pages) ----
+ * While enabled, every kernel this library launches is bracketed by two CUDA
+ * events on the launching stream, and its algorithmic work (floating-point
+ * operations of the symmetric-aware Newton-Schulz count, or HBM bytes) is
+ * recorded.  Disabled by default; enabling resets the accumulators. */
+typedef struct muonh_profile_entry {
+    const char* name;   /* kernel kind: "momentum", "ns_gram", ...  (static string) */
+    int64_t launches;   /* launches recorded */
+    double  ms;         /* summed event-measured duration, milliseconds */
+    double  flops;      /* summed algorithmic floating-point operations */
+    double  bytes;      /* summed algorithmic HBM bytes */
+} muonh_profile_entry_t;
+
+/* Turn recording on (on != 0, accumulators cleared) or off. */
+int muonh_profile_enable(int on);
+
+/* Waits for the recorded events, adds their durations into the per-kind
+ * totals, and writes up to max_entries kinds with launches > 0 to out (host
+ * array); *n_out = number written.  Blocking. */
+int muonh_profile_read(muonh_profile_entry_t* out, int max_entries, int* n_out);
+
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t muonh_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

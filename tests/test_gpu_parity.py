@@ -70,15 +70,22 @@ def _run_steps(work, steps=1, fp32_check=False, device="cuda", indices=None, bf1
     return w0, r0[idx], hist, status
 
 
+def _f32(x):
+    """The value the library receives for a float argument."""
+    return float(np.float32(x))
+
+
 def _check_step(work, w0, r0_gpu, hist, fp32_check, idx=None):
     idx = list(range(len(work.shapes))) if idx is None else idx
+    lr, beta, eps = _f32(work.lr), _f32(work.beta), _f32(work.eps)
+    coeffs = tuple(_f32(c) for c in work.coeffs)
     # r0 against the oracle's norm of the initial weights
     r0_or = om.capture_norms(w0)
     assert np.max(np.abs(r0_gpu / r0_or - 1)) < 1e-6
     tol = TOL_O[int(fp32_check)]
     for h in hist:
-        out = om.muonh_step(h["w_prev"], h["g"], h["m_prev"], r0_gpu.astype(np.float64), work.lr,
-                            work.beta, work.ns_steps, work.coeffs, work.eps)
+        out = om.muonh_step(h["w_prev"], h["g"], h["m_prev"], r0_gpu.astype(np.float64), lr,
+                            beta, work.ns_steps, coeffs, eps)
         for k in range(len(idx)):
             m_or = out["m"][k]
             ulp = np.spacing(np.abs(m_or).astype(np.float32))
@@ -86,8 +93,8 @@ def _check_step(work, w0, r0_gpu, hist, fp32_check, idx=None):
             w = h["w"][k].astype(np.float64)
             assert abs(np.linalg.norm(w) / r0_gpu[k] - 1) <= 1e-5, f"norm of matrix {idx[k]}"
             o = out["o"][k]
-            u = h["w_prev"][k].astype(np.float64) - work.lr * o
-            bound = 2 * work.lr * tol * np.linalg.norm(o) / np.linalg.norm(u) + 1e-6
+            u = h["w_prev"][k].astype(np.float64) - lr * o
+            bound = 2 * lr * tol * np.linalg.norm(o) / np.linalg.norm(u) + 1e-6
             err = _rel(w, out["w"][k])
             assert err <= bound, f"W of matrix {idx[k]}: {err:.3e} > {bound:.3e}"
             if h["wb"] is not None:
@@ -107,7 +114,7 @@ NS_SHAPES = [(256, 128), (128, 256), (300, 200), (200, 300), (129, 520), (520, 1
 @pytest.mark.parametrize("shape", NS_SHAPES)
 def test_orthogonalize_matches_oracle(shape, fp32_check):
     work = wl.ragged([shape])
-    g = work.grad(0, "cuda")
+    g = work.grad(0, 0, "cuda")
     o = mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7, flags=mh.FLAG_FP32_CHECK if fp32_check else 0)
     torch.cuda.synchronize()
     want = om.newton_schulz(g.cpu().numpy(), 5, wl.NS_COEFFS, 1e-7)
@@ -118,7 +125,7 @@ def test_orthogonalize_matches_oracle(shape, fp32_check):
 
 @pytest.mark.parametrize("steps", [0, 1, 2])
 def test_orthogonalize_step_counts(steps):
-    g = wl.ragged([(384, 640)]).grad(0, "cuda")
+    g = wl.ragged([(384, 640)]).grad(0, 0, "cuda")
     for fp32 in (0, 1):
         o = mh.orthogonalize(g, steps, wl.NS_COEFFS, 1e-7, flags=mh.FLAG_FP32_CHECK if fp32 else 0)
         want = om.newton_schulz(g.cpu().numpy(), steps, wl.NS_COEFFS, 1e-7)
@@ -224,7 +231,7 @@ def test_nonfinite_gradient_keeps_weight_and_sets_status():
 def test_degenerate_norm_sets_status():
     # W = lr*O exactly: W is the orthogonalised gradient scaled by lr, taken
     # from the library's own orthogonalisation of the same momentum.
-    g = wl.ragged([(16, 16)]).grad(0, "cuda")
+    g = wl.ragged([(16, 16)]).grad(0, 0, "cuda")
     o = mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7)
     w = (0.5 * o).contiguous()
     keep = w.clone()
