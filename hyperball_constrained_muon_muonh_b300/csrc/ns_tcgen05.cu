@@ -35,8 +35,11 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int TMEM_COLS = 2 * BN;               // 512
-constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int EPI_WARPS = 8;                    // two per TMEM lane quarter
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int ST_FLOATS = 32 * 32;              // 4 KB staging tile per epilogue warp
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ +
+                           EPI_WARPS * ST_FLOATS * 4;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s per wait
 
 // ---- PTX wrappers ------------------------------------------------------------
@@ -181,104 +184,141 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int local, int&
 }
 
 // ---- epilogues -----------------------------------------------------------------
-__device__ __forceinline__ void store_row32_f32(float* dst, const float (&v)[32]) {
+// tcgen05.ld gives each lane one accumulator row (32 consecutive columns).
+// Row-wise global access from that layout touches 32 rows per instruction,
+// so each warp stages its 32 x 32 slice in shared memory and reads it back
+// so that 8 lanes cover one 128-byte row segment.  The staging tile is
+// XOR-swizzled in 16-byte chunks (chunk c of row r sits at c ^ (r & 7)),
+// which keeps both the row-per-lane writes and the row-segment reads free of
+// bank conflicts.  Mirror writes of the symmetric products go straight from
+// registers: for a fixed column the 32 lanes write one contiguous run.
+// Operands the epilogue reads (X for APPLY, A for POLY) are loaded one slice
+// ahead so that their latency overlaps the previous slice's stores.
+
+__device__ __forceinline__ void stage_rows(float* st, int lane, const float (&v)[32]) {
+    __syncwarp();
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(st + lane * 32 + ((c ^ (lane & 7)) << 2)) =
+            make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    __syncwarp();
 }
 
-__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const float (&v)[32]) {
+// row r (0..31), chunk c (0..7) of the staged slice
+__device__ __forceinline__ float4 staged(const float* st, int r, int c) {
+    return *reinterpret_cast<const float4*>(st + r * 32 + ((c ^ (r & 7)) << 2));
+}
+
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = u;
+}
+
+// Prefetch for APPLY: X[i0 + 4k + lane/8][j0 + 4*(lane%8) .. +3], k = 0..7.
+// Row strides are multiples of 8 elements, so a 4-wide access at a column
+// < N stays inside the padded row (padding columns are never read back).
+__device__ __forceinline__ void prefetch_x(const GemmParams& p, int g, int i0, int lane, int j0, float4 (&xp)[8]) {
+    const int col = j0 + (lane & 7) * 4;
+    const float* xs = p.x_state + (size_t)g * p.ld_x * p.M;
 #pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-        uint4 u;
-        __nv_bfloat162 h0 = __floats2bfloat162_rn(v[i], v[i + 1]);
-        __nv_bfloat162 h1 = __floats2bfloat162_rn(v[i + 2], v[i + 3]);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(v[i + 4], v[i + 5]);
-        __nv_bfloat162 h3 = __floats2bfloat162_rn(v[i + 6], v[i + 7]);
-        u.x = *reinterpret_cast<uint32_t*>(&h0);
-        u.y = *reinterpret_cast<uint32_t*>(&h1);
-        u.z = *reinterpret_cast<uint32_t*>(&h2);
-        u.w = *reinterpret_cast<uint32_t*>(&h3);
-        *reinterpret_cast<uint4*>(dst + i) = u;
+    for (int k = 0; k < 8; ++k) {
+        const int row = i0 + k * 4 + (lane >> 3);
+        xp[k] = (row < p.M && col < p.N) ? __ldcs(reinterpret_cast<const float4*>(xs + (size_t)row * p.ld_x + col))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
-// One 32-column slice of one accumulator row: row i, columns j0..j0+31.
-__device__ __forceinline__ void epilogue_slice(const GemmParams& p, int g, int i, int j0, float (&v)[32]) {
-    if (i >= p.M) return;
-    const int ncols = p.N;
-    if (p.mode == NS_APPLY) {
-        const size_t base = (size_t)g * p.ld_x * p.M + (size_t)i * p.ld_x;
-        float* xs = p.x_state + base;
-        const float sc = p.scale ? p.scale[g] : 1.f;
-        if (j0 + 32 <= ncols) {
+// Prefetch for POLY: A[i][j] for this lane's row i and columns j0..j0+31,
+// read as A[j][i] (A is exactly symmetric), which is coalesced over lanes.
+__device__ __forceinline__ void prefetch_a(const GemmParams& p, int g, int i0, int lane, int j0, float (&ap)[32]) {
+    const int i = i0 + lane;
+    const float* a = p.a_f32 + (size_t)g * p.ld_s * p.M + i;
 #pragma unroll
-            for (int t = 0; t < 32; t += 4) {
-                float4 x = *reinterpret_cast<const float4*>(xs + j0 + t);
-                v[t] = sc * fmaf(p.ca, x.x, v[t]);
-                v[t + 1] = sc * fmaf(p.ca, x.y, v[t + 1]);
-                v[t + 2] = sc * fmaf(p.ca, x.z, v[t + 2]);
-                v[t + 3] = sc * fmaf(p.ca, x.w, v[t + 3]);
-            }
-            store_row32_f32(xs + j0, v);
-            if (p.x_op_out) store_row32_bf16(p.x_op_out + base + j0, v);
-        } else {
-            for (int t = 0; t < 32 && j0 + t < ncols; ++t) {
-                const float r = sc * fmaf(p.ca, xs[j0 + t], v[t]);
-                xs[j0 + t] = r;
-                if (p.x_op_out) p.x_op_out[base + j0 + t] = __float2bfloat16_rn(r);
-            }
+    for (int t = 0; t < 32; ++t) {
+        const int j = j0 + t;
+        ap[t] = (i < p.M && j < p.N && j >= i) ? a[(size_t)j * p.ld_s] : 0.f;
+    }
+}
+
+__device__ __forceinline__ void apply_slice(const GemmParams& p, int g, int i0, int lane, int j0,
+                                            const float (&v)[32], float* st, const float4 (&xp)[8], float sc) {
+    stage_rows(st, lane, v);
+    const int col = j0 + (lane & 7) * 4;
+    float* xs = p.x_state + (size_t)g * p.ld_x * p.M;
+    __nv_bfloat16* xo = p.x_op_out ? p.x_op_out + (size_t)g * p.ld_x * p.M : nullptr;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int r = k * 4 + (lane >> 3), row = i0 + r;
+        const float4 a = staged(st, r, lane & 7);
+        if (row < p.M && col < p.N) {
+            float4 y;
+            y.x = sc * fmaf(p.ca, xp[k].x, a.x);
+            y.y = sc * fmaf(p.ca, xp[k].y, a.y);
+            y.z = sc * fmaf(p.ca, xp[k].z, a.z);
+            y.w = sc * fmaf(p.ca, xp[k].w, a.w);
+            const size_t off = (size_t)row * p.ld_x + col;
+            *reinterpret_cast<float4*>(xs + off) = y;
+            if (xo) store_bf16x4(xo + off, y);
         }
-        return;
     }
-    // symmetric GRAM / POLY: keep j >= i, write (i, j) and the mirror (j, i)
-    const size_t mbase = (size_t)g * p.ld_s * p.M;
-    if (p.mode == NS_GRAM) {
-        const float sc = p.scale ? p.scale[g] : 1.f;
+}
+
+// GRAM / POLY: element (i, j) is written when j >= i, its mirror (j, i) when
+// j > i; tiles entirely below the diagonal are never scheduled.
+template <int MODE>
+__device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, int lane, int j0, float (&v)[32],
+                                          float* st, const float (&ap)[32], float sc) {
+    const int M = p.M, N = p.N;
+    const int i = i0 + lane;
+    const bool row_ok = i < M;
+    const size_t mbase = (size_t)g * p.ld_s * M;
+    if (MODE == NS_GRAM) {
 #pragma unroll
         for (int t = 0; t < 32; ++t) v[t] *= sc;
     } else {
-        const float* a = p.a_f32 + mbase + (size_t)i * p.ld_s;
-        if (j0 + 32 <= ncols) {
 #pragma unroll
-            for (int t = 0; t < 32; t += 4) {
-                float4 x = *reinterpret_cast<const float4*>(a + j0 + t);
-                v[t] = fmaf(p.cb, x.x, p.cc * v[t]);
-                v[t + 1] = fmaf(p.cb, x.y, p.cc * v[t + 1]);
-                v[t + 2] = fmaf(p.cb, x.z, p.cc * v[t + 2]);
-                v[t + 3] = fmaf(p.cb, x.w, p.cc * v[t + 3]);
-            }
-        } else {
-            for (int t = 0; t < 32 && j0 + t < ncols; ++t) v[t] = fmaf(p.cb, a[j0 + t], p.cc * v[t]);
-        }
+        for (int t = 0; t < 32; ++t) v[t] = fmaf(p.cb, ap[t], p.cc * v[t]);
     }
-    float* af = (p.mode == NS_GRAM) ? p.a_f32 + mbase : nullptr;
+    float* af = (MODE == NS_GRAM) ? p.a_f32 + mbase : nullptr;
     __nv_bfloat16* ob = p.sym_bf16 + mbase;
-    const bool full = (j0 >= i) && (j0 + 32 <= ncols);
-    if (full) {
-        if (af) store_row32_f32(af + (size_t)i * p.ld_s + j0, v);
-        store_row32_bf16(ob + (size_t)i * p.ld_s + j0, v);
-    } else {
-        for (int t = 0; t < 32; ++t) {
-            const int j = j0 + t;
-            if (j >= i && j < ncols) {
-                if (af) af[(size_t)i * p.ld_s + j] = v[t];
-                ob[(size_t)i * p.ld_s + j] = __float2bfloat16_rn(v[t]);
-            }
-        }
-    }
-    // mirror: for fixed t the warp's 32 lanes (consecutive i) write one
-    // contiguous run of row j.
-#pragma unroll 4
+#pragma unroll
     for (int t = 0; t < 32; ++t) {
         const int j = j0 + t;
-        if (j > i && j < ncols) {
-            if (af) af[(size_t)j * p.ld_s + i] = v[t];
+        if (row_ok && j > i && j < N) {
+            if (MODE == NS_GRAM) af[(size_t)j * p.ld_s + i] = v[t];
             ob[(size_t)j * p.ld_s + i] = __float2bfloat16_rn(v[t]);
+        }
+    }
+    stage_rows(st, lane, v);
+    const int col = j0 + (lane & 7) * 4;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int r = k * 4 + (lane >> 3), row = i0 + r;
+        if (row >= M || col >= N || col + 3 < row) continue;
+        const float4 y = staged(st, r, lane & 7);
+        const size_t off = (size_t)row * p.ld_s + col;
+        if (col >= row) {
+            if (MODE == NS_GRAM) *reinterpret_cast<float4*>(af + off) = y;
+            store_bf16x4(ob + off, y);
+        } else {
+            const float ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (col + e >= row && col + e < N) {
+                    if (MODE == NS_GRAM) af[off + e] = ys[e];
+                    ob[off + e] = __float2bfloat16_rn(ys[e]);
+                }
+            }
         }
     }
 }
 
 // ---- the kernel ----------------------------------------------------------------
+template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ GemmParams p) {
@@ -290,6 +330,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* stage_base = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
@@ -302,7 +343,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(tfull0 + 8 * s, 1);
-            mbar_init(tempty0 + 8 * s, 128);
+            mbar_init(tempty0 + 8 * s, 32 * EPI_WARPS);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -322,7 +363,7 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 
     const int total = p.G * p.tiles_per_mat;
     const int num_kb = (p.K + BK - 1) / BK;
-    const bool b_mn = (p.mode == NS_APPLY);
+    constexpr bool b_mn = (MODE == NS_APPLY);
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
@@ -390,28 +431,60 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         }
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // warp w reads TMEM lane quarter w%4; warps 2..5 take accumulator
+        // columns 0..127, warps 6..9 columns 128..255 (four 32-column slices)
+        const int e = warp - 2;
+        const int q = warp & 3;
+        const int h = e >> 2;
+        float* st = stage_base + e * ST_FLOATS;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.status)) break;
-            tc_fence_after();
             const int g = t / p.tiles_per_mat;
             int mi, nj;
             tile_coords(p, t - g * p.tiles_per_mat, mi, nj);
-            const int i = mi * BM + q * 32 + lane;
-            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            for (int c = 0; c < BN / 32; ++c) {
-                const int j0 = nj * BN + c * 32;
-                if (j0 >= p.N) break;  // warp-uniform
-                float v[32];
-                tmem_ld32(trow + c * 32, v);
-                if (c == BN / 32 - 1 || j0 + 32 >= p.N) {
-                    // accumulator fully read: hand it back to the MMA warp
-                    tc_fence_before();
-                    mbar_arrive(tempty0 + 8 * acc);
+            const int i0 = mi * BM + q * 32;
+            const int jb = nj * BN + h * (BN / 2);
+            const int nsl = max(0, min(BN / 64, (p.N - jb + 31) / 32));
+            float sc = 1.f;
+            if (MODE != NS_POLY && p.scale) sc = p.scale[g];
+            float4 xc[8], xn[8];
+            float ac[32], an[32];
+            if (nsl > 0) {
+                if (MODE == NS_APPLY) prefetch_x(p, g, i0, lane, jb, xc);
+                if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, jb, ac);
+            }
+            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + h * (BN / 2));
+            if (nsl == 0) mbar_arrive(tempty0 + 8 * acc);
+#pragma unroll
+            for (int k = 0; k < BN / 64; ++k) {
+                if (k < nsl) {
+                    const int j0 = jb + 32 * k;
+                    float v[32];
+                    tmem_ld32(trow + 32 * k, v);
+                    if (k == nsl - 1) {
+                        // last read of this accumulator by this warp
+                        tc_fence_before();
+                        mbar_arrive(tempty0 + 8 * acc);
+                    }
+                    if (k + 1 < nsl) {
+                        if (MODE == NS_APPLY) prefetch_x(p, g, i0, lane, j0 + 32, xn);
+                        if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, j0 + 32, an);
+                    }
+                    if (MODE == NS_APPLY) {
+                        apply_slice(p, g, i0, lane, j0, v, st, xc, sc);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) xc[u] = xn[u];
+                    } else {
+                        sym_slice<MODE>(p, g, i0, lane, j0, v, st, ac, sc);
+                        if (MODE == NS_POLY) {
+#pragma unroll
+                            for (int u = 0; u < 32; ++u) ac[u] = an[u];
+                        }
+                    }
                 }
-                epilogue_slice(p, g, i, j0, v);
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
@@ -496,12 +569,22 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
     if (total <= 0) return cudaSuccess;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<NS_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ns_gemm_kernel<NS_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ns_gemm_kernel<NS_APPLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) { *why = "cudaFuncSetAttribute failed"; return e; }
         attr_set = true;
     }
     const int grid = (int)(total < sm_count() ? total : sm_count());
-    ns_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+    if (p.mode == NS_GRAM)
+        ns_gemm_kernel<NS_GRAM><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+    else if (p.mode == NS_POLY)
+        ns_gemm_kernel<NS_POLY><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+    else
+        ns_gemm_kernel<NS_APPLY><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
     return cudaGetLastError();
 }
 
