@@ -1,6 +1,6 @@
 """Builds libmuonh.so (the CUDA kernels and the C ABI) in this directory.
 
-    python -m hyperball_constrained_muon_muonh_b300.build
+    python hyperball_constrained_muon_muonh_b300/build.py
 
 Compiles for sm_103a only (B300).  nvcc cross-compiles without a GPU.
 """
