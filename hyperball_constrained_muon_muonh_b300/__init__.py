@@ -120,6 +120,24 @@ def orthogonalize(x: torch.Tensor, ns_steps: int = 5, coeffs=NS_COEFFS, eps: flo
     return out
 
 
+def orthogonalize_static(x: torch.Tensor, ns_steps: int = 5, coeffs=NS_COEFFS, eps: float = 1e-7,
+                         flags: int = 0, out=None, stream=None) -> torch.Tensor:
+    """Newton-Schulz without a workspace (muonh_orthogonalize_static).
+
+    For code that cannot allocate device memory: scratch comes from the
+    library's fixed device array (see include/muonh.h).  ``out`` must be
+    given by such callers; calls that may overlap on the GPU race.
+    """
+    _check_tensor(x, "x")
+    if out is None:
+        out = torch.empty_like(x)
+    r, c_ = x.shape
+    cf = (ctypes.c_float * 3)(*coeffs)
+    check(lib.muonh_orthogonalize_static(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()), r, c_,
+                                         ns_steps, cf, eps, flags, _stream(stream)), "muonh_orthogonalize_static")
+    return out
+
+
 def get_status(stream=None) -> int:
     """Synchronise, read and clear the device status word."""
     v = ctypes.c_uint32()

@@ -35,7 +35,10 @@ EXPORTS = (
     "muonh_orthogonalize_workspace_size", "muonh_orthogonalize", "muonh_get_status",
     "muonh_status_string", "muonh_last_error", "muonh_version",
     "muonh_profile_enable", "muonh_profile_read", "muonh_launch_count",
+    "muonh_orthogonalize_static",
 )
+
+STATIC_SCRATCH_BYTES = 80 * 1024 * 1024
 
 
 class MatrixT(ctypes.Structure):
@@ -71,7 +74,7 @@ def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is missing: build it with "
-            "`python -m hyperball_constrained_muon_muonh_b300.build` (nvcc, sm_103a)")
+            "`python hyperball_constrained_muon_muonh_b300/build.py` (nvcc, sm_103a)")
     lib = ctypes.CDLL(LIB_PATH)
     P, I, U32, SZ, F, I64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_size_t,
                              ctypes.c_float, ctypes.c_int64)
@@ -82,6 +85,7 @@ def _load():
     lib.muonh_step.argtypes = [mp, I, P, F, F, I, fp, F, U32, P, SZ, P]
     lib.muonh_orthogonalize_workspace_size.argtypes = [I64, I64, U32, ctypes.POINTER(SZ)]
     lib.muonh_orthogonalize.argtypes = [P, P, I64, I64, I, fp, F, U32, P, SZ, P]
+    lib.muonh_orthogonalize_static.argtypes = [P, P, I64, I64, I, fp, F, U32, P]
     lib.muonh_get_status.argtypes = [ctypes.POINTER(U32), P]
     lib.muonh_status_string.argtypes = [I]
     lib.muonh_status_string.restype = ctypes.c_char_p

@@ -460,6 +460,10 @@ int get_status_ptr(uint32_t** p) {
 }
 
 }  // namespace
+
+// Lets other translation units of the library report an error text.
+int report_error(int code, const char* msg) { return fail(code, msg); }
+
 }  // namespace muonh
 
 using namespace muonh;

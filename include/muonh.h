@@ -134,6 +134,35 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
                         void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Newton-Schulz alone, like muonh_orthogonalize, for callers that cannot
+ * allocate device memory: code running where cudaMalloc is unavailable or
+ * forbidden (inside a custom allocator or memory-pool callback, under a
+ * fixed device-memory budget, or in a host process that must not grow its
+ * device footprint after start-up).  No counterpart on the pages: it is a
+ * packaging of the same computation.
+ *
+ * Scratch comes from one array of MUONH_STATIC_SCRATCH_BYTES that the
+ * library holds in device memory (a file-scope __device__ variable), on
+ * every device that loads the library, until the process exits.  Shapes
+ * whose muonh_orthogonalize_workspace_size() exceeds it are rejected with
+ * MUONH_ERR_WORKSPACE and a message (muonh_last_error); 2048 x 2048,
+ * 1024 x 8192 and anything smaller fit.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture.  The call allocates no device memory
+ * and calls no cudaMalloc/cudaFree.  All calls share the one array, so two
+ * calls that may overlap on the GPU (different streams, or different host
+ * threads on one device) race and corrupt each other's results: order them
+ * on one stream.  No scratch byte is read before the same call writes it, so
+ * stale contents from an earlier call do not matter.
+ */
+#define MUONH_STATIC_SCRATCH_BYTES (80u * 1024u * 1024u)
+int muonh_orthogonalize_static(const float* in, float* out, int64_t rows, int64_t cols,
+                               int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags,
+                               void* stream);
+
+/*
  * Synchronises `stream`, then copies the current device's status word to
  * *status_out (host) and clears it.  Blocking.
  */
