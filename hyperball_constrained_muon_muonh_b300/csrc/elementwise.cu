@@ -62,20 +62,45 @@ momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restr
 
     if (!is_transposed(rows, cols)) {
         if (ld == cols && (cols & 3) == 0) {
+            // flat float4 stream; four vectors per thread in flight
             const size_t e0 = (size_t)r_begin * cols, e1 = (size_t)r_end * cols;
-            for (size_t e = e0 + 4 * (size_t)threadIdx.x; e < e1; e += 4 * kThreads) {
-                float4 g = __ldcs(reinterpret_cast<const float4*>(D.g + e));
-                float4 m = g;
+            constexpr int U = 4;
+            size_t e = e0 + 4 * (size_t)threadIdx.x;
+            for (; e + 4 * kThreads * (U - 1) < e1; e += 4 * kThreads * U) {
+                float4 g[U], m[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) g[u] = __ldcs(reinterpret_cast<const float4*>(D.g + e + 4 * kThreads * u));
                 if (D.m) {
-                    m = *reinterpret_cast<const float4*>(D.m + e);
-                    m.x = fmaf(beta, m.x, g.x); m.y = fmaf(beta, m.y, g.y);
-                    m.z = fmaf(beta, m.z, g.z); m.w = fmaf(beta, m.w, g.w);
-                    *reinterpret_cast<float4*>(D.m + e) = m;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) m[u] = __ldcs(reinterpret_cast<const float4*>(D.m + e + 4 * kThreads * u));
                 }
-                *reinterpret_cast<float4*>(D.xs + e) = m;
-                store_bf16x4(D.xo + e, m);
-                acc = fmaf(m.x, m.x, acc); acc = fmaf(m.y, m.y, acc);
-                acc = fmaf(m.z, m.z, acc); acc = fmaf(m.w, m.w, acc);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const size_t f = e + 4 * kThreads * u;
+                    float4 v = g[u];
+                    if (D.m) {
+                        v.x = fmaf(beta, m[u].x, v.x); v.y = fmaf(beta, m[u].y, v.y);
+                        v.z = fmaf(beta, m[u].z, v.z); v.w = fmaf(beta, m[u].w, v.w);
+                        *reinterpret_cast<float4*>(D.m + f) = v;
+                    }
+                    *reinterpret_cast<float4*>(D.xs + f) = v;
+                    store_bf16x4(D.xo + f, v);
+                    acc = fmaf(v.x, v.x, acc); acc = fmaf(v.y, v.y, acc);
+                    acc = fmaf(v.z, v.z, acc); acc = fmaf(v.w, v.w, acc);
+                }
+            }
+            for (; e < e1; e += 4 * kThreads) {
+                float4 v = __ldcs(reinterpret_cast<const float4*>(D.g + e));
+                if (D.m) {
+                    const float4 m = *reinterpret_cast<const float4*>(D.m + e);
+                    v.x = fmaf(beta, m.x, v.x); v.y = fmaf(beta, m.y, v.y);
+                    v.z = fmaf(beta, m.z, v.z); v.w = fmaf(beta, m.w, v.w);
+                    *reinterpret_cast<float4*>(D.m + e) = v;
+                }
+                *reinterpret_cast<float4*>(D.xs + e) = v;
+                store_bf16x4(D.xo + e, v);
+                acc = fmaf(v.x, v.x, acc); acc = fmaf(v.y, v.y, acc);
+                acc = fmaf(v.z, v.z, acc); acc = fmaf(v.w, v.w, acc);
             }
         } else {
             for (int r = r_begin; r < r_end; ++r) {
@@ -91,8 +116,46 @@ momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restr
         }
     } else {
         // X = M^T: stage 64x64 tiles in shared memory, write them transposed.
-        const int tr = threadIdx.x & 63, tq = threadIdx.x >> 6;   // 64 x 4
+        const bool vec_ok = (cols & 3) == 0;
         for (int c0 = 0; c0 < cols; c0 += kTile) {
+            if (vec_ok && r_begin + kTile <= r_end && c0 + kTile <= cols) {
+                // full tile: float4 along W rows, then float4 along X rows
+                const int lr = threadIdx.x >> 4, lc = (threadIdx.x & 15) * 4;
+                float4 g[4], m[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    g[k] = __ldcs(reinterpret_cast<const float4*>(D.g + (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc));
+                if (D.m) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        m[k] = __ldcs(reinterpret_cast<const float4*>(D.m + (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc));
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float4 v = g[k];
+                    if (D.m) {
+                        v.x = fmaf(beta, m[k].x, v.x); v.y = fmaf(beta, m[k].y, v.y);
+                        v.z = fmaf(beta, m[k].z, v.z); v.w = fmaf(beta, m[k].w, v.w);
+                        *reinterpret_cast<float4*>(D.m + (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc) = v;
+                    }
+                    acc = fmaf(v.x, v.x, acc); acc = fmaf(v.y, v.y, acc);
+                    acc = fmaf(v.z, v.z, acc); acc = fmaf(v.w, v.w, acc);
+                    float* tr = &tile[lr + 16 * k][lc];
+                    tr[0] = v.x; tr[1] = v.y; tr[2] = v.z; tr[3] = v.w;
+                }
+                __syncthreads();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int cc = lr + 16 * k, rr = lc;   // X row c0+cc, X cols r_begin+rr..+3
+                    const float4 v = make_float4(tile[rr][cc], tile[rr + 1][cc], tile[rr + 2][cc], tile[rr + 3][cc]);
+                    const size_t o = (size_t)(c0 + cc) * ld + r_begin + rr;
+                    *reinterpret_cast<float4*>(D.xs + o) = v;
+                    store_bf16x4(D.xo + o, v);
+                }
+                __syncthreads();
+                continue;
+            }
+            const int tr = threadIdx.x & 63, tq = threadIdx.x >> 6;   // 64 x 4
             for (int i = 0; i < kTile; i += 4) {
                 const int r = r_begin + i + tq, c = c0 + tr;
                 if (r < r_end && c < cols) {
@@ -173,31 +236,45 @@ hyperball_kernel(const __grid_constant__ DescBatch b, float lr, double* __restri
     const float nlr = o_scale ? -lr * o_scale[p] : -lr;
     float acc = 0.f;
 
+    // U = W - lr*O for four values; APPLY: W <- f*U (+ bf16 copy), else ||U||^2
+    auto visit4 = [&](float4 w, float4 o, size_t widx) {
+        float4 u;
+        u.x = fmaf(nlr, o.x, w.x); u.y = fmaf(nlr, o.y, w.y);
+        u.z = fmaf(nlr, o.z, w.z); u.w = fmaf(nlr, o.w, w.w);
+        if (APPLY) {
+            u.x *= f; u.y *= f; u.z *= f; u.w *= f;
+            *reinterpret_cast<float4*>(D.w + widx) = u;
+            if (D.wb) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(u.x, u.y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(u.z, u.w);
+                uint2 v;
+                v.x = *reinterpret_cast<uint32_t*>(&lo);
+                v.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(D.wb + widx) = v;
+            }
+        } else {
+            acc = fmaf(u.x, u.x, acc); acc = fmaf(u.y, u.y, acc);
+            acc = fmaf(u.z, u.z, acc); acc = fmaf(u.w, u.w, acc);
+        }
+    };
+
     if (!is_transposed(rows, cols)) {
         if (ld == cols && (cols & 3) == 0) {
             const size_t e0 = (size_t)r_begin * cols, e1 = (size_t)r_end * cols;
-            for (size_t e = e0 + 4 * (size_t)threadIdx.x; e < e1; e += 4 * kThreads) {
-                float4 w = *reinterpret_cast<const float4*>(D.w + e);
-                float4 o = __ldcs(reinterpret_cast<const float4*>(D.xs + e));
-                float4 u;
-                u.x = fmaf(nlr, o.x, w.x); u.y = fmaf(nlr, o.y, w.y);
-                u.z = fmaf(nlr, o.z, w.z); u.w = fmaf(nlr, o.w, w.w);
-                if (APPLY) {
-                    u.x *= f; u.y *= f; u.z *= f; u.w *= f;
-                    *reinterpret_cast<float4*>(D.w + e) = u;
-                    if (D.wb) {
-                        __nv_bfloat162 lo = __floats2bfloat162_rn(u.x, u.y);
-                        __nv_bfloat162 hi = __floats2bfloat162_rn(u.z, u.w);
-                        uint2 v;
-                        v.x = *reinterpret_cast<uint32_t*>(&lo);
-                        v.y = *reinterpret_cast<uint32_t*>(&hi);
-                        *reinterpret_cast<uint2*>(D.wb + e) = v;
-                    }
-                } else {
-                    acc = fmaf(u.x, u.x, acc); acc = fmaf(u.y, u.y, acc);
-                    acc = fmaf(u.z, u.z, acc); acc = fmaf(u.w, u.w, acc);
+            constexpr int U = 4;
+            size_t e = e0 + 4 * (size_t)threadIdx.x;
+            for (; e + 4 * kThreads * (U - 1) < e1; e += 4 * kThreads * U) {
+                float4 w[U], o[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    w[u] = *reinterpret_cast<const float4*>(D.w + e + 4 * kThreads * u);
+                    o[u] = __ldcs(reinterpret_cast<const float4*>(D.xs + e + 4 * kThreads * u));
                 }
+#pragma unroll
+                for (int u = 0; u < U; ++u) visit4(w[u], o[u], e + 4 * kThreads * u);
             }
+            for (; e < e1; e += 4 * kThreads)
+                visit4(*reinterpret_cast<const float4*>(D.w + e), __ldcs(reinterpret_cast<const float4*>(D.xs + e)), e);
         } else {
             for (int r = r_begin; r < r_end; ++r) {
                 for (int c = threadIdx.x; c < cols; c += kThreads) {
@@ -214,8 +291,36 @@ hyperball_kernel(const __grid_constant__ DescBatch b, float lr, double* __restri
             }
         }
     } else {
-        const int tr = threadIdx.x & 63, tq = threadIdx.x >> 6;
+        const bool vec_ok = (cols & 3) == 0;
         for (int c0 = 0; c0 < cols; c0 += kTile) {
+            if (vec_ok && r_begin + kTile <= r_end && c0 + kTile <= cols) {
+                // full tile: X rows (W columns) loaded as float4 along W rows
+                const int lr = threadIdx.x >> 4, lc = (threadIdx.x & 15) * 4;
+                float4 x[4], w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    x[k] = __ldcs(reinterpret_cast<const float4*>(D.xs + (size_t)(c0 + lr + 16 * k) * ld + r_begin + lc));
+                    w[k] = *reinterpret_cast<const float4*>(D.w + (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    // tile[W row][W col]
+                    tile[lc][lr + 16 * k] = x[k].x;
+                    tile[lc + 1][lr + 16 * k] = x[k].y;
+                    tile[lc + 2][lr + 16 * k] = x[k].z;
+                    tile[lc + 3][lr + 16 * k] = x[k].w;
+                }
+                __syncthreads();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float* t = &tile[lr + 16 * k][lc];
+                    visit4(w[k], make_float4(t[0], t[1], t[2], t[3]),
+                           (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc);
+                }
+                __syncthreads();
+                continue;
+            }
+            const int tr = threadIdx.x & 63, tq = threadIdx.x >> 6;
             // X_state rows c (contiguous along r) -> tile[c - c0][r - r_begin]
             for (int i = 0; i < kTile; i += 4) {
                 const int c = c0 + i + tq, r = r_begin + tr;
