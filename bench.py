@@ -181,12 +181,13 @@ def run_reference(args, work, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="qwen3_2b_28layers")
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gemm-1sm", action="store_true", help="one-SM Newton-Schulz GEMM kernel")
     args = ap.parse_args()
 
     import muonh_workloads as wl
@@ -214,7 +215,7 @@ def main():
     ws = work.weights(dev)
     grads = [work.grads(t, dev) for t in range(2)]   # two gradient sets, alternated
     opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps, ns_coeffs=work.coeffs,
-                   eps=work.eps, bf16_copies=True)
+                   eps=work.eps, bf16_copies=True, flags=mh.FLAG_GEMM_1SM if args.gemm_1sm else 0)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -314,7 +315,8 @@ def main():
                    "ns_steps": work.ns_steps, "ns_coeffs": list(work.coeffs), "beta": work.beta, "lr": work.lr,
                    "eps": work.eps, "state": "fp32 W/M/G + bf16 W copy; NS bf16 operands, fp32 state",
                    "l2": "inputs larger than L2 (about 20 GB of optimizer state touched per step)",
-                   "parallelism": f"replica x{world}"},
+                   "parallelism": f"replica x{world}",
+                   "ns_gemm": "1-SM 128x256 tiles" if args.gemm_1sm else "2-SM pair 256x256 tiles"},
         "ns_tflops": achieved,
         "roofline": roofline,
         "hbm_kernels": hbm,

@@ -20,7 +20,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (FLAG_FP32_CHECK, FLAG_SYNC_DEBUG, STATUS_DEGENERATE_NORM,  # noqa: F401
+from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_SYNC_DEBUG, STATUS_DEGENERATE_NORM,  # noqa: F401
                    STATUS_KERNEL_TIMEOUT, STATUS_NONFINITE_INPUT, MuonHError, check, lib)
 
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
@@ -163,11 +163,11 @@ class MuonH:
     """
 
     def __init__(self, weights, lr=0.02, beta=0.95, ns_steps=5, ns_coeffs=NS_COEFFS, eps=1e-7,
-                 bf16_copies=False, fp32_check=False):
+                 bf16_copies=False, fp32_check=False, flags=0):
         self.weights = list(weights)
         self.lr, self.beta, self.ns_steps, self.eps = float(lr), float(beta), int(ns_steps), float(eps)
         self.ns_coeffs = tuple(float(v) for v in ns_coeffs)
-        self.flags = FLAG_FP32_CHECK if fp32_check else 0
+        self.flags = (FLAG_FP32_CHECK if fp32_check else 0) | int(flags)
         self.moms = [torch.zeros_like(w) for w in self.weights]
         self.bf16 = [torch.empty_like(w, dtype=torch.bfloat16) for w in self.weights] if bf16_copies else None
         self.r0 = capture_norms(self.weights)

@@ -26,6 +26,7 @@ STATUS_KERNEL_TIMEOUT = 0x4
 
 FLAG_FP32_CHECK = 0x1
 FLAG_SYNC_DEBUG = 0x4
+FLAG_GEMM_1SM = 0x8
 
 MAX_SIDE = 65536
 

@@ -319,6 +319,7 @@ struct Sync {
 int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_steps, const float* coeffs,
                       uint32_t flags, uint32_t* status, Sync& sy, bool* x_in_alt) {
     const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
+    const bool pair = (flags & MUONH_FLAG_GEMM_1SM) == 0;
     *x_in_alt = false;
     for (int it = 0; it < ns_steps; ++it) {
         for (const Bucket& B : P.buckets) {
@@ -391,7 +392,7 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 cudaError_t e;
                 {
                     Trace tr(K_GRAM, sy.st);
-                    e = tr.done(tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, sy.st, &why), G * S * S * L,
+                    e = tr.done(tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, pair, sy.st, &why), G * S * S * L,
                                 G * S * L * 2 + G * S * S * 6);
                 }
                 int r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 Gram launch");
@@ -404,7 +405,7 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 q.status = status;
                 {
                     Trace tr(K_POLY, sy.st);
-                    e = tr.done(tc::launch_ns_gemm(q, aop, B.ld_s, aop, B.ld_s, sy.st, &why), G * S * S * S,
+                    e = tr.done(tc::launch_ns_gemm(q, aop, B.ld_s, aop, B.ld_s, pair, sy.st, &why), G * S * S * S,
                                 G * S * S * 8);
                 }
                 r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 polynomial launch");
@@ -419,7 +420,7 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 a.status = status;
                 {
                     Trace tr(K_APPLY, sy.st);
-                    e = tr.done(tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, sy.st, &why), 2 * G * S * S * L,
+                    e = tr.done(tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, pair, sy.st, &why), 2 * G * S * S * L,
                                 G * S * S * 2 + G * S * L * (a.x_op_out ? 12 : 10));
                 }
                 r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 apply launch");
@@ -437,7 +438,7 @@ int check_scalars(int ns_steps, const float* coeffs, float eps, uint32_t flags) 
     for (int i = 0; i < 3; ++i)
         if (!std::isfinite(coeffs[i])) return fail(MUONH_ERR_INVALID_ARG, "ns_coeffs must be finite");
     if (!std::isfinite(eps) || eps < 0.f) return fail(MUONH_ERR_INVALID_ARG, "eps must be finite and >= 0");
-    if (flags & ~(uint32_t)(MUONH_FLAG_FP32_CHECK | MUONH_FLAG_SYNC_DEBUG))
+    if (flags & ~(uint32_t)(MUONH_FLAG_FP32_CHECK | MUONH_FLAG_SYNC_DEBUG | MUONH_FLAG_GEMM_1SM))
         return fail(MUONH_ERR_UNSUPPORTED, "unknown flag bits");
     return MUONH_OK;
 }

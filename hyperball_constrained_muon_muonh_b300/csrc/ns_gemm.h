@@ -30,7 +30,7 @@ struct GemmParams {
 };
 
 namespace tc {
-cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld,
+cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld, bool pair,
                            cudaStream_t st, const char** why);
 int tiles_per_matrix(int mode, int M, int N);
 }  // namespace tc

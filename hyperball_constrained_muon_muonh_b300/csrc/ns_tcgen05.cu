@@ -499,6 +499,295 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
 }
 
+// ---- 2-SM variant: one CTA pair (cluster of 2) per 256 x 256 tile -------------------
+// tcgen05.mma.cta_group::2 issued by the even CTA of the pair computes a
+// 256 x 256 tile: each CTA holds 128 rows of A and 128 rows (N) of B in its
+// own shared memory and receives its 128 accumulator rows in its own TMEM.
+// Per CTA and K step this moves 32 KB instead of 48 KB, so the ring is 6
+// stages deep.  Both CTAs' TMA loads complete on the even CTA's full barrier;
+// the MMA commits are multicast to both CTAs' empty / tmem-full barriers; the
+// epilogue warps of both CTAs release an accumulator on the even CTA's
+// tmem-empty barrier.
+namespace pair {
+
+constexpr int STAGES2 = 6;
+constexpr int A2_BYTES = BM * BK * 2;                 // 16 KB: this CTA's 128 rows of A
+constexpr int B2_BYTES = (BN / 2) * BK * 2;           // 16 KB: this CTA's 128 rows of B
+constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
+constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + 1024 + 256 + EPI_WARPS * ST_FLOATS * 4;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// shared::cluster address of the same variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// TMA load into this CTA's shared memory, completing on a barrier that may
+// belong to the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int x,
+                                                 int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// arrive once on the barrier at the same offset in both CTAs of the pair
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+__host__ __device__ constexpr uint32_t idesc_pair(bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) |
+           ((uint32_t)((2 * BM) >> 4) << 24);
+}
+
+// Pair tile (mp, nj): rows mp*256 .. +255, columns nj*256 .. +255.
+// Symmetric modes keep nj >= mp.
+__device__ __forceinline__ void pair_coords(const GemmParams& p, int local, int& mp, int& nj) {
+    if (p.mode == NS_APPLY) {
+        nj = local / p.tiles_m;
+        mp = local - nj * p.tiles_m;
+        return;
+    }
+    int m = 0;
+    for (;;) {
+        const int cnt = p.tiles_n - m;
+        if (local < cnt) break;
+        local -= cnt;
+        ++m;
+    }
+    mp = m;
+    nj = m + local;
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* smem_a = smem;
+    uint8_t* smem_b = smem + STAGES2 * A2_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES2 * STAGE2_BYTES);
+    // bars: full[STAGES2], empty[STAGES2], tfull[2], tempty[2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 4);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* stage_base = reinterpret_cast<float*>(smem + STAGES2 * STAGE2_BYTES + 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES2);
+    const uint32_t tfull0 = smem_u32(bars + 2 * STAGES2), tempty0 = smem_u32(bars + 2 * STAGES2 + 2);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES2; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(tfull0 + 8 * s, 1);
+            mbar_init(tempty0 + 8 * s, 2 * EPI_WARPS);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tm_a);
+        prefetch_tmap(&tm_b);
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers initialised before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total = p.G * p.tiles_per_mat;
+    const int num_kb = (p.K + BK - 1) / BK;
+    constexpr bool b_mn = (MODE == NS_APPLY);
+    const int cid = (int)cluster_id(), ncl = (int)cluster_count();
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer (both CTAs) ----------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = cid; t < total && ok; t += ncl) {
+            const int g = t / p.tiles_per_mat;
+            int mp, nj;
+            pair_coords(p, t - g * p.tiles_per_mat, mp, nj);
+            const int row_a = mp * 2 * BM + (int)rank * BM;       // this CTA's 128 rows of A
+            const int row_b = nj * BN + (int)rank * (BN / 2);     // this CTA's 128 rows (N) of B
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+                const uint32_t fb_local = full0 + 8 * stage;
+                const uint32_t fb = map_to_rank(fb_local, 0);
+                if (leader) mbar_expect_tx(fb_local, 2 * STAGE2_BYTES);
+                const uint32_t sa = smem_u32(smem_a + stage * A2_BYTES);
+                const uint32_t sb = smem_u32(smem_b + stage * B2_BYTES);
+                tma_load_3d_pair(sa, &tm_a, fb, kb * BK, row_a, g);
+                if (!b_mn) {
+                    tma_load_3d_pair(sb, &tm_b, fb, kb * BK, row_b, g);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BN / 128; ++c)
+                        tma_load_3d_pair(sb + c * (64 * BK * 2), &tm_b, fb, row_b + c * 64, kb * BK, g);
+                }
+                if (++stage == STAGES2) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok && leader) {
+            for (int s = 0; s < STAGES2; ++s) {
+                const unsigned long long t0 = global_ns();
+                while (global_ns() - t0 < 20000000ull) {
+                    if (mbar_try_wait(full0 + 8 * s, 0) || mbar_try_wait(full0 + 8 * s, 1)) break;
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ---------------- MMA issuer (even CTA only) ----------------
+        const uint32_t idesc = idesc_pair(b_mn);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int t = cid; t < total && ok; t += ncl) {
+            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem_a + stage * A2_BYTES);
+                const uint32_t sb = smem_u32(smem_b + stage * B2_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t ad = sdesc(sa + kk * 32, 16, 1024);
+                    const uint64_t bd = b_mn ? sdesc(sb + kk * 2048, 64 * BK * 2, 1024) : sdesc(sb + kk * 32, 16, 1024);
+                    mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+                }
+                mma_commit_pair(empty0 + 8 * stage);
+                if (++stage == STAGES2) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            mma_commit_pair(tfull0 + 8 * acc);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    } else if (warp >= 2) {
+        // ---------------- epilogue (both CTAs: 128 rows each) ----------------
+        const int e = warp - 2;
+        const int q = warp & 3;
+        const int h = e >> 2;
+        float* st = stage_base + e * ST_FLOATS;
+        const uint32_t tempty_leader = map_to_rank(tempty0, 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = cid; t < total; t += ncl) {
+            const int g = t / p.tiles_per_mat;
+            int mp, nj;
+            pair_coords(p, t - g * p.tiles_per_mat, mp, nj);
+            const int i0 = mp * 2 * BM + (int)rank * BM + q * 32;
+            const int jb = nj * BN + h * (BN / 2);
+            const int nsl = max(0, min(BN / 64, (p.N - jb + 31) / 32));
+            float sc = 1.f;
+            if (MODE != NS_POLY && p.scale) sc = p.scale[g];
+            float4 xc[8], xn[8];
+            float ac[32], an[32];
+            if (nsl > 0) {
+                if (MODE == NS_APPLY) prefetch_x(p, g, i0, lane, jb, xc);
+                if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, jb, ac);
+            }
+            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + h * (BN / 2));
+            if (nsl == 0) {
+                __syncwarp();
+                if (lane == 0) remote_arrive(tempty_leader + 8 * acc);
+            }
+#pragma unroll
+            for (int k = 0; k < BN / 64; ++k) {
+                if (k < nsl) {
+                    const int j0 = jb + 32 * k;
+                    float v[32];
+                    tmem_ld32(trow + 32 * k, v);
+                    if (k == nsl - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) remote_arrive(tempty_leader + 8 * acc);
+                    }
+                    if (k + 1 < nsl) {
+                        if (MODE == NS_APPLY) prefetch_x(p, g, i0, lane, j0 + 32, xn);
+                        if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, j0 + 32, an);
+                    }
+                    if (MODE == NS_APPLY) {
+                        apply_slice(p, g, i0, lane, j0, v, st, xc, sc);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) xc[u] = xn[u];
+                    } else {
+                        sym_slice<MODE>(p, g, i0, lane, j0, v, st, ac, sc);
+                        if (MODE == NS_POLY) {
+#pragma unroll
+                            for (int u = 0; u < 32; ++u) ac[u] = an[u];
+                        }
+                    }
+                }
+            }
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    cluster_sync();   // no CTA leaves while its peer may still signal or read it
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+}  // namespace pair
+
 // ---- host side -------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -548,11 +837,76 @@ int tiles_per_matrix(int mode, int M, int N) {
     return cnt;
 }
 
+int pair_tiles_per_matrix(int mode, int M, int N) {
+    const int tm = (M + 2 * BM - 1) / (2 * BM), tn = (N + BN - 1) / BN;
+    if (mode == NS_APPLY) return tm * tn;
+    int cnt = 0;
+    for (int m = 0; m < tm; ++m) cnt += tn - m > 0 ? tn - m : 0;
+    return cnt;
+}
+
+template <int MODE>
+static int max_pair_clusters() {
+    static int cached[3] = {0, 0, 0};
+    if (cached[MODE]) return cached[MODE];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 148, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::SMEM2_BYTES;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, pair::ns_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        n = sm_count() / 2;
+    }
+    cached[MODE] = n;
+    return n;
+}
+
+template <int MODE>
+static cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, long long total,
+                               cudaStream_t st) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(pair::ns_gemm_pair_kernel<MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM2_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const long long clusters = total < max_pair_clusters<MODE>() ? total : max_pair_clusters<MODE>();
+    pair::ns_gemm_pair_kernel<MODE><<<(int)(2 * clusters), NUM_THREADS, pair::SMEM2_BYTES, st>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
 // Operand tensors: GRAM A = B = X_op [G][s][ld_x] (K = l);
 // POLY A = B = A_op [G][s][ld_s] (K = s);  APPLY A = B_op [G][s][ld_s],
-// B = X_op (MN-major: rows = k).
-cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld,
+// B = X_op (MN-major: rows = k).  `pair` selects the 2-SM kernel.
+cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld, bool pair,
                            cudaStream_t st, const char** why) {
+    if (pair) {
+        CUtensorMap ta, tb;
+        if (!encode_bf16_3d(&ta, a_op, p.K, p.M, p.G, a_ld, BM)) { *why = "cuTensorMapEncodeTiled (A) failed"; return cudaErrorInvalidValue; }
+        const bool okb = (p.mode == NS_APPLY) ? encode_bf16_3d(&tb, b_op, p.N, p.K, p.G, b_ld, 64)
+                                              : encode_bf16_3d(&tb, b_op, p.K, p.N, p.G, b_ld, BN / 2);
+        if (!okb) { *why = "cuTensorMapEncodeTiled (B) failed"; return cudaErrorInvalidValue; }
+        p.tiles_m = (p.M + 2 * BM - 1) / (2 * BM);
+        p.tiles_n = (p.N + BN - 1) / BN;
+        p.tiles_per_mat = pair_tiles_per_matrix(p.mode, p.M, p.N);
+        const long long total = (long long)p.G * p.tiles_per_mat;
+        if (total <= 0) return cudaSuccess;
+        cudaError_t e;
+        if (p.mode == NS_GRAM) e = launch_pair<NS_GRAM>(ta, tb, p, total, st);
+        else if (p.mode == NS_POLY) e = launch_pair<NS_POLY>(ta, tb, p, total, st);
+        else e = launch_pair<NS_APPLY>(ta, tb, p, total, st);
+        if (e != cudaSuccess) *why = "2-SM GEMM launch failed";
+        return e;
+    }
     CUtensorMap ta, tb;
     // A operand: rows = M, cols = K
     if (!encode_bf16_3d(&ta, a_op, p.K, p.M, p.G, a_ld, BM)) { *why = "cuTensorMapEncodeTiled (A) failed"; return cudaErrorInvalidValue; }

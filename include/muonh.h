@@ -65,6 +65,9 @@ extern "C" {
 /* ---- flags ---- */
 #define MUONH_FLAG_FP32_CHECK  0x1u  /* Newton-Schulz in fp32 CUDA-core GEMMs (accuracy check mode) */
 #define MUONH_FLAG_SYNC_DEBUG  0x4u  /* synchronise and check errors after every kernel */
+#define MUONH_FLAG_GEMM_1SM    0x8u  /* Newton-Schulz GEMMs on one SM per 128x256 tile instead of the
+                                        default CTA pair per 256x256 tile (same results up to bf16
+                                        rounding order; for comparison and small problems) */
 
 /* One weight matrix and its optimizer state.  All device pointers, fp32
  * row-major rows x cols (row stride = cols elements), 16-byte aligned.

@@ -43,13 +43,13 @@ def _cuda():
     assert mh.get_status() & mh.STATUS_KERNEL_TIMEOUT == 0
 
 
-def _run_steps(work, steps=1, fp32_check=False, device="cuda", indices=None, bf16=True):
+def _run_steps(work, steps=1, fp32_check=False, device="cuda", indices=None, bf16=True, flags=0):
     """GPU MuonH over `work`; returns host copies of inputs and outputs per step."""
     idx = list(range(len(work.shapes))) if indices is None else indices
     ws = work.weights(device)
     w0 = [ws[i].cpu().numpy() for i in idx]
     opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps, ns_coeffs=work.coeffs,
-                   eps=work.eps, bf16_copies=bf16, fp32_check=fp32_check)
+                   eps=work.eps, bf16_copies=bf16, fp32_check=fp32_check, flags=flags)
     r0 = opt.r0.cpu().numpy()
     hist = []
     for t in range(steps):
@@ -110,12 +110,17 @@ NS_SHAPES = [(256, 128), (128, 256), (300, 200), (200, 300), (129, 520), (520, 1
              (77, 77), (640, 384), (2048, 2048), (1024, 2048), (6144, 2048), (2048, 6144)]
 
 
-@pytest.mark.parametrize("fp32_check", [0, 1])
+# flag sets: the default 2-SM pair GEMM, the 1-SM GEMM, the fp32 check mode
+MODES = {"pair": 0, "1sm": 1 << 3, "fp32": 1}
+
+
+@pytest.mark.parametrize("mode", list(MODES))
 @pytest.mark.parametrize("shape", NS_SHAPES)
-def test_orthogonalize_matches_oracle(shape, fp32_check):
+def test_orthogonalize_matches_oracle(shape, mode):
+    fp32_check = int(mode == "fp32")
     work = wl.ragged([shape])
     g = work.grad(0, 0, "cuda")
-    o = mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7, flags=mh.FLAG_FP32_CHECK if fp32_check else 0)
+    o = mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7, flags=MODES[mode])
     torch.cuda.synchronize()
     want = om.newton_schulz(g.cpu().numpy(), 5, wl.NS_COEFFS, 1e-7)
     err = _rel(o.cpu().numpy(), want)
@@ -137,9 +142,10 @@ def test_orthogonalize_low_rank_aspect():
     work = wl.aspect_16384x1024()
     for i in (0, 4):
         g = work.grad(i, 0, "cuda")
-        o = mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7)
         want = om.newton_schulz(g.cpu().numpy(), 5, wl.NS_COEFFS, 1e-7)
-        assert _rel(o.cpu().numpy(), want) <= TOL_O[0]
+        for flags in (0, MODES["1sm"]):
+            o = mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7, flags=flags)
+            assert _rel(o.cpu().numpy(), want) <= TOL_O[0]
 
 
 # ---------------------------------------------------------------------------
@@ -154,18 +160,20 @@ def test_step_single_256x128(fp32_check):
     _check_step(work, w0, r0, hist, fp32_check)
 
 
-@pytest.mark.parametrize("fp32_check", [False, True])
-def test_step_ragged_shapes_three_steps(fp32_check):
+@pytest.mark.parametrize("mode", list(MODES))
+def test_step_ragged_shapes_three_steps(mode):
+    fp32_check = mode == "fp32"
     work = wl.ragged([(300, 200), (200, 300), (129, 520), (1, 8), (8, 1), (77, 77), (5, 3), (640, 384)])
-    w0, r0, hist, status = _run_steps(work, 3, fp32_check)
+    w0, r0, hist, status = _run_steps(work, 3, fp32_check, flags=MODES[mode])
     assert status == 0
     _check_step(work, w0, r0, hist, fp32_check)
 
 
-@pytest.mark.parametrize("fp32_check", [False, True])
-def test_step_qwen3_layer(fp32_check):
+@pytest.mark.parametrize("mode", list(MODES))
+def test_step_qwen3_layer(mode):
+    fp32_check = mode == "fp32"
     work = wl.qwen3_layer()
-    w0, r0, hist, status = _run_steps(work, 2, fp32_check)
+    w0, r0, hist, status = _run_steps(work, 2, fp32_check, flags=MODES[mode])
     assert status == 0
     _check_step(work, w0, r0, hist, fp32_check)
 
