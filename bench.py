@@ -184,6 +184,8 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="qwen3_2b_28layers")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="first N decoder layers of the 2B set (a smaller case for profiling)")
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -191,7 +193,12 @@ def main():
     args = ap.parse_args()
 
     import muonh_workloads as wl
-    work = wl.ALL[args.workload]()
+    if args.layers is not None:
+        if args.workload != "qwen3_2b_28layers":
+            raise SystemExit("--layers applies to the qwen3_2b_28layers workload only")
+        work = wl.qwen3_2b(layers=args.layers)
+    else:
+        work = wl.ALL[args.workload]()
     world, rank, local = _dist()
 
     if args.impl == "reference":
@@ -285,7 +292,7 @@ def main():
         return
 
     peaks = _peaks()
-    ns_kinds = ("ns_gram", "ns_poly", "ns_apply")
+    ns_kinds = ("ns_gram", "ns_poly", "ns_apply", "ns_apply_in", "ns_apply_out", "ns_apply_in_out")
     ns_ms = sum(prof[k]["ms"] for k in ns_kinds if k in prof)
     ns_flops = sum(prof[k]["flops"] for k in ns_kinds if k in prof)
     ns_launches = sum(prof[k]["launches"] for k in ns_kinds if k in prof)

@@ -17,19 +17,42 @@ struct MatDesc {
     uint16_t* wb;         // bf16 copy or nullptr
     const float* g;       // gradient
     float* m;             // momentum
-    float* xs;            // fp32 NS state X (s x ld)
-    __nv_bfloat16* xo;    // bf16 NS operand X (s x ld)
+    float* xs;            // fp32 NS state X (rows x ld, the matrix's own orientation)
+    __nv_bfloat16* xo;    // bf16 NS operand X (rows x ld)
     int rows, cols;
     int ld;               // row stride of xs / xo, elements
     int chunk0;           // first chunk index of this matrix
     int user_index;       // position in the caller's list (indexes r0)
-    int pad_;
+    int part0;            // first ||U||^2 partial written by the last apply GEMM
+    int npart;            // number of those partials
+    int fused;            // kFused* bits: how this matrix meets the Newton-Schulz GEMMs
 };
-static_assert(sizeof(MatDesc) == 72, "MatDesc layout");
+
+// MatDesc::fused bits.
+//   kFusedIn   the first apply GEMM reads X from the momentum (or input)
+//              itself, so the momentum kernel writes no fp32 copy of X
+//   kFusedOut  the last apply GEMM writes U = W - lr*O and the partials of
+//              ||U||^2 (part0, npart), so the hyperball step only rescales
+constexpr int kFusedIn = 1, kFusedOut = 2;
+static_assert(sizeof(MatDesc) == 80, "MatDesc layout");
 
 // Largest descriptor batch one launch carries in its parameter space
 // (sm_90+ kernels take up to 32764 bytes of parameters).
-constexpr int kMaxDescPerLaunch = 440;
+constexpr int kMaxDescPerLaunch = 396;
+
+// Where the Newton-Schulz apply epilogue finds a matrix's own buffers (row-
+// major, row stride = cols; the state X has the matrix's own orientation).
+// Written by the momentum kernel into the workspace, one record per
+// bucket-order position.
+//   src: the unscaled Newton-Schulz input (the momentum M, or the input of a
+//        standalone orthogonalisation), read by the first apply in place of
+//        an fp32 copy of X
+//   w:   the master weight, read by the last apply of a MuonH step
+struct NsIO {
+    const float* src;
+    const float* w;
+};
+static_assert(sizeof(NsIO) == 16, "NsIO layout");
 
 struct DescBatch {
     int n;                // matrices in this batch
@@ -40,15 +63,14 @@ struct DescBatch {
 };
 static_assert(sizeof(DescBatch) <= 32000, "descriptor batch exceeds kernel parameter space");
 
-// Rows per chunk: a chunk is rows [r, r + chunk_rows) of one matrix (W
-// orientation).  Transposed matrices (rows > cols) use 64-row tiles.
+// Rows per chunk: a chunk is rows [r, r + chunk_rows) of one matrix, about
+// kChunkElems elements.  Every matrix keeps its own orientation throughout
+// (the Newton-Schulz state of a tall matrix is tall too), so the HBM-bound
+// kernels stream each matrix row-major.
 constexpr int kChunkElems = 65536;
-constexpr int kTile = 64;
-
-__host__ __device__ inline bool is_transposed(int rows, int cols) { return rows > cols; }
 
 __host__ __device__ inline int chunk_rows_for(int rows, int cols) {
-    if (is_transposed(rows, cols)) return kTile;
+    (void)rows;
     int cr = kChunkElems / (cols > 0 ? cols : 1);
     return cr < 1 ? 1 : cr;
 }

@@ -43,141 +43,94 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, float4 v) {
 }
 
 // ---------------------------------------------------------------------------
-// K1: M <- beta*M + G; X_state = M and X_op = bf16(M) in X orientation
-// (unscaled: the 1/(||M||+eps) factor is folded into the Newton-Schulz
-// epilogues); partial ||M||^2 per chunk.  With D.m null the input G itself
-// is the Newton-Schulz input (standalone orthogonalisation).
+// K1: M <- beta*M + G; X_op = bf16(M) and, unless D.fused has kFusedIn (the
+// first apply GEMM then reads M itself), X_state = M, in the matrix's own
+// orientation (unscaled: the 1/(||M||+eps) factor is folded into the
+// Newton-Schulz epilogues); partial ||M||^2 per chunk.  With D.m null the
+// input G itself is the Newton-Schulz input (standalone orthogonalisation).
+// With `io` set, the CTA of each matrix's first chunk records where the
+// matrix's input and weight are (NsIO, indexed by bucket-order position).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads)
-momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restrict__ partials) {
-    __shared__ float tile[kTile][kTile + 1];
-    __shared__ double red[kThreads / 32];
-    const int chunk = b.chunk_begin + blockIdx.x;
-    const MatDesc& D = b.d[find_matrix(b, chunk)];
-    const int rows = D.rows, cols = D.cols, ld = D.ld;
-    const int cr = chunk_rows_for(rows, cols);
-    const int r_begin = (chunk - D.chunk0) * cr;
-    const int r_end = min(rows, r_begin + cr);
-    float acc = 0.f;
-
-    if (!is_transposed(rows, cols)) {
-        if (ld == cols && (cols & 3) == 0) {
-            // flat float4 stream; four vectors per thread in flight
-            const size_t e0 = (size_t)r_begin * cols, e1 = (size_t)r_end * cols;
-            constexpr int U = 4;
-            size_t e = e0 + 4 * (size_t)threadIdx.x;
-            for (; e + 4 * kThreads * (U - 1) < e1; e += 4 * kThreads * U) {
-                float4 g[U], m[U];
+template <bool WRITE_XS>
+__device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, int r_end, float beta, float& acc) {
+    const int cols = D.cols, ld = D.ld;
+    if (ld == cols && (cols & 3) == 0) {
+        // flat float4 stream; four vectors per thread in flight
+        const size_t e0 = (size_t)r_begin * cols, e1 = (size_t)r_end * cols;
+        constexpr int U = 4;
+        size_t e = e0 + 4 * (size_t)threadIdx.x;
+        for (; e + 4 * kThreads * (U - 1) < e1; e += 4 * kThreads * U) {
+            float4 g[U], m[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) g[u] = __ldcs(reinterpret_cast<const float4*>(D.g + e + 4 * kThreads * u));
-                if (D.m) {
+            for (int u = 0; u < U; ++u) g[u] = __ldcs(reinterpret_cast<const float4*>(D.g + e + 4 * kThreads * u));
+            if (D.m) {
 #pragma unroll
-                    for (int u = 0; u < U; ++u) m[u] = __ldcs(reinterpret_cast<const float4*>(D.m + e + 4 * kThreads * u));
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const size_t f = e + 4 * kThreads * u;
-                    float4 v = g[u];
-                    if (D.m) {
-                        v.x = fmaf(beta, m[u].x, v.x); v.y = fmaf(beta, m[u].y, v.y);
-                        v.z = fmaf(beta, m[u].z, v.z); v.w = fmaf(beta, m[u].w, v.w);
-                        *reinterpret_cast<float4*>(D.m + f) = v;
-                    }
-                    *reinterpret_cast<float4*>(D.xs + f) = v;
-                    store_bf16x4(D.xo + f, v);
-                    acc = fmaf(v.x, v.x, acc); acc = fmaf(v.y, v.y, acc);
-                    acc = fmaf(v.z, v.z, acc); acc = fmaf(v.w, v.w, acc);
-                }
+                for (int u = 0; u < U; ++u) m[u] = __ldcs(reinterpret_cast<const float4*>(D.m + e + 4 * kThreads * u));
             }
-            for (; e < e1; e += 4 * kThreads) {
-                float4 v = __ldcs(reinterpret_cast<const float4*>(D.g + e));
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const size_t f = e + 4 * kThreads * u;
+                float4 v = g[u];
                 if (D.m) {
-                    const float4 m = *reinterpret_cast<const float4*>(D.m + e);
-                    v.x = fmaf(beta, m.x, v.x); v.y = fmaf(beta, m.y, v.y);
-                    v.z = fmaf(beta, m.z, v.z); v.w = fmaf(beta, m.w, v.w);
-                    *reinterpret_cast<float4*>(D.m + e) = v;
+                    v.x = fmaf(beta, m[u].x, v.x); v.y = fmaf(beta, m[u].y, v.y);
+                    v.z = fmaf(beta, m[u].z, v.z); v.w = fmaf(beta, m[u].w, v.w);
+                    *reinterpret_cast<float4*>(D.m + f) = v;
                 }
-                *reinterpret_cast<float4*>(D.xs + e) = v;
-                store_bf16x4(D.xo + e, v);
+                if (WRITE_XS) *reinterpret_cast<float4*>(D.xs + f) = v;
+                store_bf16x4(D.xo + f, v);
                 acc = fmaf(v.x, v.x, acc); acc = fmaf(v.y, v.y, acc);
                 acc = fmaf(v.z, v.z, acc); acc = fmaf(v.w, v.w, acc);
             }
-        } else {
-            for (int r = r_begin; r < r_end; ++r) {
-                for (int c = threadIdx.x; c < cols; c += kThreads) {
-                    const size_t e = (size_t)r * cols + c;
-                    float m = D.g[e];
-                    if (D.m) { m = fmaf(beta, D.m[e], m); D.m[e] = m; }
-                    D.xs[(size_t)r * ld + c] = m;
-                    D.xo[(size_t)r * ld + c] = __float2bfloat16_rn(m);
-                    acc = fmaf(m, m, acc);
-                }
+        }
+        for (; e < e1; e += 4 * kThreads) {
+            float4 v = __ldcs(reinterpret_cast<const float4*>(D.g + e));
+            if (D.m) {
+                const float4 m = *reinterpret_cast<const float4*>(D.m + e);
+                v.x = fmaf(beta, m.x, v.x); v.y = fmaf(beta, m.y, v.y);
+                v.z = fmaf(beta, m.z, v.z); v.w = fmaf(beta, m.w, v.w);
+                *reinterpret_cast<float4*>(D.m + e) = v;
             }
+            if (WRITE_XS) *reinterpret_cast<float4*>(D.xs + e) = v;
+            store_bf16x4(D.xo + e, v);
+            acc = fmaf(v.x, v.x, acc); acc = fmaf(v.y, v.y, acc);
+            acc = fmaf(v.z, v.z, acc); acc = fmaf(v.w, v.w, acc);
         }
     } else {
-        // X = M^T: stage 64x64 tiles in shared memory, write them transposed.
-        const bool vec_ok = (cols & 3) == 0;
-        for (int c0 = 0; c0 < cols; c0 += kTile) {
-            if (vec_ok && r_begin + kTile <= r_end && c0 + kTile <= cols) {
-                // full tile: float4 along W rows, then float4 along X rows
-                const int lr = threadIdx.x >> 4, lc = (threadIdx.x & 15) * 4;
-                float4 g[4], m[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    g[k] = __ldcs(reinterpret_cast<const float4*>(D.g + (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc));
-                if (D.m) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        m[k] = __ldcs(reinterpret_cast<const float4*>(D.m + (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc));
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float4 v = g[k];
-                    if (D.m) {
-                        v.x = fmaf(beta, m[k].x, v.x); v.y = fmaf(beta, m[k].y, v.y);
-                        v.z = fmaf(beta, m[k].z, v.z); v.w = fmaf(beta, m[k].w, v.w);
-                        *reinterpret_cast<float4*>(D.m + (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc) = v;
-                    }
-                    acc = fmaf(v.x, v.x, acc); acc = fmaf(v.y, v.y, acc);
-                    acc = fmaf(v.z, v.z, acc); acc = fmaf(v.w, v.w, acc);
-                    float* tr = &tile[lr + 16 * k][lc];
-                    tr[0] = v.x; tr[1] = v.y; tr[2] = v.z; tr[3] = v.w;
-                }
-                __syncthreads();
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int cc = lr + 16 * k, rr = lc;   // X row c0+cc, X cols r_begin+rr..+3
-                    const float4 v = make_float4(tile[rr][cc], tile[rr + 1][cc], tile[rr + 2][cc], tile[rr + 3][cc]);
-                    const size_t o = (size_t)(c0 + cc) * ld + r_begin + rr;
-                    *reinterpret_cast<float4*>(D.xs + o) = v;
-                    store_bf16x4(D.xo + o, v);
-                }
-                __syncthreads();
-                continue;
-            }
-            const int tr = threadIdx.x & 63, tq = threadIdx.x >> 6;   // 64 x 4
-            for (int i = 0; i < kTile; i += 4) {
-                const int r = r_begin + i + tq, c = c0 + tr;
-                if (r < r_end && c < cols) {
-                    const size_t e = (size_t)r * cols + c;
-                    float m = D.g[e];
-                    if (D.m) { m = fmaf(beta, D.m[e], m); D.m[e] = m; }
-                    acc = fmaf(m, m, acc);
-                    tile[i + tq][tr] = m;
-                }
-            }
-            __syncthreads();
-            for (int i = 0; i < kTile; i += 4) {
-                const int c = c0 + i + tq, r = r_begin + tr;
-                if (r < r_end && c < cols) {
-                    const float v = tile[tr][i + tq];
-                    D.xs[(size_t)c * ld + r] = v;
-                    D.xo[(size_t)c * ld + r] = __float2bfloat16_rn(v);
-                }
-            }
-            __syncthreads();
+        // any row length: the chunk's elements in row-major order
+        const size_t n = (size_t)(r_end - r_begin) * cols;
+        for (size_t e = threadIdx.x; e < n; e += kThreads) {
+            const size_t r = r_begin + e / cols, c = e % cols;
+            const size_t wi = r * cols + c, xi = r * ld + c;
+            float m = D.g[wi];
+            if (D.m) { m = fmaf(beta, D.m[wi], m); D.m[wi] = m; }
+            if (WRITE_XS) D.xs[xi] = m;
+            D.xo[xi] = __float2bfloat16_rn(m);
+            acc = fmaf(m, m, acc);
         }
     }
+}
+
+__global__ void __launch_bounds__(kThreads)
+momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restrict__ partials, NsIO* io) {
+    __shared__ double red[kThreads / 32];
+    const int chunk = b.chunk_begin + blockIdx.x;
+    const int mi = find_matrix(b, chunk);
+    const MatDesc& D = b.d[mi];
+    const int cols = D.cols;
+    if (io && chunk == D.chunk0 && threadIdx.x == 0) {
+        NsIO r;
+        r.src = D.m ? D.m : D.g;
+        r.w = D.w;
+        io[b.first + mi] = r;
+    }
+    const int cr = chunk_rows_for(D.rows, cols);
+    const int r_begin = (chunk - D.chunk0) * cr;
+    const int r_end = min(D.rows, r_begin + cr);
+    float acc = 0.f;
+    if (D.fused & kFusedIn)
+        momentum_chunk<false>(D, r_begin, r_end, beta, acc);
+    else
+        momentum_chunk<true>(D, r_begin, r_end, beta, acc);
     double s = block_sum<kThreads>((double)acc, red);
     if (threadIdx.x == 0) partials[chunk] = s;
 }
@@ -207,193 +160,158 @@ __global__ void momentum_finalize(const __grid_constant__ DescBatch b, const dou
 }
 
 // ---------------------------------------------------------------------------
-// K3a: partial ||W - lr*O||^2 per chunk (O = X_state, read transposed for
-// tall matrices).  K3b: W <- factor*(W - lr*O), W_bf16 = bf16(W).
-// Both evaluate U = fma(-lr, O, W) identically.
+// Hyperball retraction, W <- r0 * U / ||U||_F with U = W - lr*O.  One chunk
+// in one of three forms (O = X_state, same orientation as W, row stride D.ld):
+//   HB_NORM   partial ||U||^2 (U = fma(-lr, O, W))
+//   HB_APPLY  W <- factor*U, W_bf16 = bf16(W)   (U recomputed identically)
+//   HB_SCALE  W <- factor*U, W_bf16 = bf16(W), where X_state already holds U
+//             (written by the last apply GEMM, which also summed ||U||^2)
 // ---------------------------------------------------------------------------
-template <bool APPLY>
+enum { HB_NORM = 0, HB_APPLY = 1, HB_SCALE = 2 };
+
+template <int HB>
+__device__ __forceinline__ void hyperball_chunk(const MatDesc& D, int r_begin, int r_end, float nlr, float f,
+                                                float& acc) {
+    constexpr bool WRITE = HB != HB_NORM;
+    constexpr bool READ_W = HB != HB_SCALE;
+    const int cols = D.cols, ld = D.ld;
+    if (ld == cols && (cols & 3) == 0) {
+        const size_t e0 = (size_t)r_begin * cols, e1 = (size_t)r_end * cols;
+        constexpr int U = 4;
+        // U for four values (from W and O, or as read); write f*U or add ||U||^2
+        auto visit4 = [&](float4 w, float4 o, size_t widx) {
+            float4 u;
+            if (READ_W) {
+                u.x = fmaf(nlr, o.x, w.x); u.y = fmaf(nlr, o.y, w.y);
+                u.z = fmaf(nlr, o.z, w.z); u.w = fmaf(nlr, o.w, w.w);
+            } else {
+                u = o;
+            }
+            if (WRITE) {
+                u.x *= f; u.y *= f; u.z *= f; u.w *= f;
+                *reinterpret_cast<float4*>(D.w + widx) = u;
+                if (D.wb) store_bf16x4(reinterpret_cast<__nv_bfloat16*>(D.wb) + widx, u);
+            } else {
+                acc = fmaf(u.x, u.x, acc); acc = fmaf(u.y, u.y, acc);
+                acc = fmaf(u.z, u.z, acc); acc = fmaf(u.w, u.w, acc);
+            }
+        };
+        const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        size_t e = e0 + 4 * (size_t)threadIdx.x;
+        for (; e + 4 * kThreads * (U - 1) < e1; e += 4 * kThreads * U) {
+            float4 w[U], o[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                w[u] = READ_W ? *reinterpret_cast<const float4*>(D.w + e + 4 * kThreads * u) : zero4;
+                o[u] = __ldcs(reinterpret_cast<const float4*>(D.xs + e + 4 * kThreads * u));
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) visit4(w[u], o[u], e + 4 * kThreads * u);
+        }
+        for (; e < e1; e += 4 * kThreads)
+            visit4(READ_W ? *reinterpret_cast<const float4*>(D.w + e) : zero4,
+                   __ldcs(reinterpret_cast<const float4*>(D.xs + e)), e);
+    } else {
+        const size_t n = (size_t)(r_end - r_begin) * cols;
+        for (size_t e = threadIdx.x; e < n; e += kThreads) {
+            const size_t r = r_begin + e / cols, c = e % cols;
+            const size_t wi = r * cols + c;
+            const float o = D.xs[r * ld + c];
+            const float u = READ_W ? fmaf(nlr, o, D.w[wi]) : o;
+            if (WRITE) {
+                const float y = u * f;
+                D.w[wi] = y;
+                if (D.wb) D.wb[wi] = bf16_bits(y);
+            } else {
+                acc = fmaf(u, u, acc);
+            }
+        }
+    }
+}
+
+// Partial ||W - lr*O||^2 per chunk, for the matrices without kFusedOut
+// (their last apply GEMM left O in X_state).
 __global__ void __launch_bounds__(kThreads)
-hyperball_kernel(const __grid_constant__ DescBatch b, float lr, double* __restrict__ partials,
-                 const float* __restrict__ factor, const uint32_t* __restrict__ flags,
-                 const float* __restrict__ o_scale) {
-    __shared__ float tile[kTile][kTile + 1];
+hyperball_norm_kernel(const __grid_constant__ DescBatch b, float lr, double* __restrict__ partials,
+                      const float* __restrict__ o_scale) {
     __shared__ double red[kThreads / 32];
     const int chunk = b.chunk_begin + blockIdx.x;
     const int mi = find_matrix(b, chunk);
     const MatDesc& D = b.d[mi];
+    if (D.fused & kFusedOut) return;
     const int p = b.first + mi;
-    const int rows = D.rows, cols = D.cols, ld = D.ld;
-    const int cr = chunk_rows_for(rows, cols);
+    const int cr = chunk_rows_for(D.rows, D.cols);
     const int r_begin = (chunk - D.chunk0) * cr;
-    const int r_end = min(rows, r_begin + cr);
-    float f = 0.f;
-    if (APPLY) {
-        if (flags[p] != 0) return;  // W stays as it was
-        f = factor[p];
-    }
+    const int r_end = min(D.rows, r_begin + cr);
     // O = o_scale * X_state (o_scale is 1/(||M||+eps) when no Newton-Schulz
     // iteration ran, X_state then holding the unscaled momentum)
     const float nlr = o_scale ? -lr * o_scale[p] : -lr;
     float acc = 0.f;
-
-    // U = W - lr*O for four values; APPLY: W <- f*U (+ bf16 copy), else ||U||^2
-    auto visit4 = [&](float4 w, float4 o, size_t widx) {
-        float4 u;
-        u.x = fmaf(nlr, o.x, w.x); u.y = fmaf(nlr, o.y, w.y);
-        u.z = fmaf(nlr, o.z, w.z); u.w = fmaf(nlr, o.w, w.w);
-        if (APPLY) {
-            u.x *= f; u.y *= f; u.z *= f; u.w *= f;
-            *reinterpret_cast<float4*>(D.w + widx) = u;
-            if (D.wb) {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(u.x, u.y);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(u.z, u.w);
-                uint2 v;
-                v.x = *reinterpret_cast<uint32_t*>(&lo);
-                v.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(D.wb + widx) = v;
-            }
-        } else {
-            acc = fmaf(u.x, u.x, acc); acc = fmaf(u.y, u.y, acc);
-            acc = fmaf(u.z, u.z, acc); acc = fmaf(u.w, u.w, acc);
-        }
-    };
-
-    if (!is_transposed(rows, cols)) {
-        if (ld == cols && (cols & 3) == 0) {
-            const size_t e0 = (size_t)r_begin * cols, e1 = (size_t)r_end * cols;
-            constexpr int U = 4;
-            size_t e = e0 + 4 * (size_t)threadIdx.x;
-            for (; e + 4 * kThreads * (U - 1) < e1; e += 4 * kThreads * U) {
-                float4 w[U], o[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    w[u] = *reinterpret_cast<const float4*>(D.w + e + 4 * kThreads * u);
-                    o[u] = __ldcs(reinterpret_cast<const float4*>(D.xs + e + 4 * kThreads * u));
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) visit4(w[u], o[u], e + 4 * kThreads * u);
-            }
-            for (; e < e1; e += 4 * kThreads)
-                visit4(*reinterpret_cast<const float4*>(D.w + e), __ldcs(reinterpret_cast<const float4*>(D.xs + e)), e);
-        } else {
-            for (int r = r_begin; r < r_end; ++r) {
-                for (int c = threadIdx.x; c < cols; c += kThreads) {
-                    const size_t e = (size_t)r * cols + c;
-                    float u = fmaf(nlr, D.xs[(size_t)r * ld + c], D.w[e]);
-                    if (APPLY) {
-                        u *= f;
-                        D.w[e] = u;
-                        if (D.wb) D.wb[e] = bf16_bits(u);
-                    } else {
-                        acc = fmaf(u, u, acc);
-                    }
-                }
-            }
-        }
-    } else {
-        const bool vec_ok = (cols & 3) == 0;
-        for (int c0 = 0; c0 < cols; c0 += kTile) {
-            if (vec_ok && r_begin + kTile <= r_end && c0 + kTile <= cols) {
-                // full tile: X rows (W columns) loaded as float4 along W rows
-                const int lr = threadIdx.x >> 4, lc = (threadIdx.x & 15) * 4;
-                float4 x[4], w[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    x[k] = __ldcs(reinterpret_cast<const float4*>(D.xs + (size_t)(c0 + lr + 16 * k) * ld + r_begin + lc));
-                    w[k] = *reinterpret_cast<const float4*>(D.w + (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    // tile[W row][W col]
-                    tile[lc][lr + 16 * k] = x[k].x;
-                    tile[lc + 1][lr + 16 * k] = x[k].y;
-                    tile[lc + 2][lr + 16 * k] = x[k].z;
-                    tile[lc + 3][lr + 16 * k] = x[k].w;
-                }
-                __syncthreads();
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float* t = &tile[lr + 16 * k][lc];
-                    visit4(w[k], make_float4(t[0], t[1], t[2], t[3]),
-                           (size_t)(r_begin + lr + 16 * k) * cols + c0 + lc);
-                }
-                __syncthreads();
-                continue;
-            }
-            const int tr = threadIdx.x & 63, tq = threadIdx.x >> 6;
-            // X_state rows c (contiguous along r) -> tile[c - c0][r - r_begin]
-            for (int i = 0; i < kTile; i += 4) {
-                const int c = c0 + i + tq, r = r_begin + tr;
-                if (r < r_end && c < cols) tile[i + tq][tr] = D.xs[(size_t)c * ld + r];
-            }
-            __syncthreads();
-            for (int i = 0; i < kTile; i += 4) {
-                const int r = r_begin + i + tq, c = c0 + tr;
-                if (r < r_end && c < cols) {
-                    const size_t e = (size_t)r * cols + c;
-                    float u = fmaf(nlr, tile[tr][i + tq], D.w[e]);
-                    if (APPLY) {
-                        u *= f;
-                        D.w[e] = u;
-                        if (D.wb) D.wb[e] = bf16_bits(u);
-                    } else {
-                        acc = fmaf(u, u, acc);
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
-    if (!APPLY) {
-        double s = block_sum<kThreads>((double)acc, red);
-        if (threadIdx.x == 0) partials[chunk] = s;
-    }
+    hyperball_chunk<HB_NORM>(D, r_begin, r_end, nlr, 0.f, acc);
+    double s = block_sum<kThreads>((double)acc, red);
+    if (threadIdx.x == 0) partials[chunk] = s;
 }
 
-// Standalone orthogonalisation output: out (W orientation, D.w) = o_scale * X.
+// W <- factor * U, W_bf16 = bf16(W): U from W - lr*O, or read from X_state
+// for the matrices with kFusedOut.  Matrices with a status bit keep W.
 __global__ void __launch_bounds__(kThreads)
-emit_kernel(const __grid_constant__ DescBatch b, const float* __restrict__ o_scale) {
-    __shared__ float tile[kTile][kTile + 1];
+hyperball_finish_kernel(const __grid_constant__ DescBatch b, float lr, const float* __restrict__ factor,
+                        const uint32_t* __restrict__ flags, const float* __restrict__ o_scale) {
     const int chunk = b.chunk_begin + blockIdx.x;
     const int mi = find_matrix(b, chunk);
     const MatDesc& D = b.d[mi];
     const int p = b.first + mi;
-    const int rows = D.rows, cols = D.cols, ld = D.ld;
-    const int cr = chunk_rows_for(rows, cols);
+    if (flags[p] != 0) return;  // W stays as it was
+    const int cr = chunk_rows_for(D.rows, D.cols);
     const int r_begin = (chunk - D.chunk0) * cr;
-    const int r_end = min(rows, r_begin + cr);
-    const float os = o_scale ? o_scale[p] : 1.f;
-    if (!is_transposed(rows, cols)) {
-        for (int r = r_begin; r < r_end; ++r)
-            for (int c = threadIdx.x; c < cols; c += kThreads)
-                D.w[(size_t)r * cols + c] = os * D.xs[(size_t)r * ld + c];
+    const int r_end = min(D.rows, r_begin + cr);
+    float unused = 0.f;
+    if (D.fused & kFusedOut) {
+        hyperball_chunk<HB_SCALE>(D, r_begin, r_end, 0.f, factor[p], unused);
     } else {
-        const int tr = threadIdx.x & 63, tq = threadIdx.x >> 6;
-        for (int c0 = 0; c0 < cols; c0 += kTile) {
-            for (int i = 0; i < kTile; i += 4) {
-                const int c = c0 + i + tq, r = r_begin + tr;
-                if (r < r_end && c < cols) tile[i + tq][tr] = D.xs[(size_t)c * ld + r];
-            }
-            __syncthreads();
-            for (int i = 0; i < kTile; i += 4) {
-                const int r = r_begin + i + tq, c = c0 + tr;
-                if (r < r_end && c < cols) D.w[(size_t)r * cols + c] = os * tile[tr][i + tq];
-            }
-            __syncthreads();
-        }
+        const float nlr = o_scale ? -lr * o_scale[p] : -lr;
+        hyperball_chunk<HB_APPLY>(D, r_begin, r_end, nlr, factor[p], unused);
     }
 }
 
-// Per matrix: rho^2 = sum of partials; factor = r0 / rho, or a status bit.
+// Standalone orthogonalisation output: out (D.w) = o_scale * X_state.
+__global__ void __launch_bounds__(kThreads)
+emit_kernel(const __grid_constant__ DescBatch b, const float* __restrict__ o_scale) {
+    const int chunk = b.chunk_begin + blockIdx.x;
+    const int mi = find_matrix(b, chunk);
+    const MatDesc& D = b.d[mi];
+    const int p = b.first + mi;
+    const int cols = D.cols, ld = D.ld;
+    const int cr = chunk_rows_for(D.rows, cols);
+    const int r_begin = (chunk - D.chunk0) * cr;
+    const int r_end = min(D.rows, r_begin + cr);
+    const float os = o_scale ? o_scale[p] : 1.f;
+    const size_t n = (size_t)(r_end - r_begin) * cols;
+    for (size_t e = threadIdx.x; e < n; e += kThreads) {
+        const size_t r = r_begin + e / cols, c = e % cols;
+        D.w[r * cols + c] = os * D.xs[r * ld + c];
+    }
+}
+
+// Per matrix: rho^2 = sum of partials in index order (the hyperball norm
+// kernel's per-chunk partials, or, with kFusedOut, the last apply GEMM's
+// per-warp partials at upart[D.part0..]); factor = r0 / rho, or a status bit.
+// One warp per matrix: lane k adds partials k, k+32, ... in order, then a
+// fixed shuffle tree combines the lanes, so the sum is deterministic.
 __global__ void hyperball_finalize(const __grid_constant__ DescBatch b, const double* __restrict__ partials,
-                                   Scalars sc, const float* __restrict__ r0) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+                                   const double* __restrict__ upart, Scalars sc, const float* __restrict__ r0) {
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
     if (i >= b.n) return;
     const MatDesc& D = b.d[i];
     const int p = b.first + i;
-    const int nch = chunks_for(D.rows, D.cols);
+    const bool from_gemm = (D.fused & kFusedOut) != 0;
+    const double* src = from_gemm ? upart + (size_t)D.part0 : partials + D.chunk0;
+    const int cnt = from_gemm ? D.npart : chunks_for(D.rows, D.cols);
     double s = 0.0;
-    for (int k = 0; k < nch; ++k) s += partials[D.chunk0 + k];
+    for (int k = lane; k < cnt; k += 32) s += src[k];
+    s = warp_sum(s);
+    if (lane != 0) return;
     sc.rho2[p] = s;
     uint32_t f = sc.flags[p];
     float fac = 0.f;
@@ -450,10 +368,10 @@ capture_norms_kernel(const __grid_constant__ DescBatch b, float* __restrict__ r0
 // ---------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------
-cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, cudaStream_t st) {
+cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, NsIO* io, cudaStream_t st) {
     const int nblk = b.chunk_end - b.chunk_begin;
     if (nblk <= 0) return cudaSuccess;
-    momentum_kernel<<<nblk, kThreads, 0, st>>>(b, beta, partials);
+    momentum_kernel<<<nblk, kThreads, 0, st>>>(b, beta, partials, io);
     return cudaGetLastError();
 }
 
@@ -467,21 +385,21 @@ cudaError_t launch_hyperball_norm(const DescBatch& b, float lr, double* partials
                                   cudaStream_t st) {
     const int nblk = b.chunk_end - b.chunk_begin;
     if (nblk <= 0) return cudaSuccess;
-    hyperball_kernel<false><<<nblk, kThreads, 0, st>>>(b, lr, partials, nullptr, nullptr, o_scale);
+    hyperball_norm_kernel<<<nblk, kThreads, 0, st>>>(b, lr, partials, o_scale);
     return cudaGetLastError();
 }
 
-cudaError_t launch_hyperball_finalize(const DescBatch& b, const double* partials, const Scalars& sc,
-                                      const float* r0, cudaStream_t st) {
-    hyperball_finalize<<<(b.n + 127) / 128, 128, 0, st>>>(b, partials, sc, r0);
+cudaError_t launch_hyperball_finalize(const DescBatch& b, const double* partials, const double* upart,
+                                      const Scalars& sc, const float* r0, cudaStream_t st) {
+    hyperball_finalize<<<(b.n + 3) / 4, 128, 0, st>>>(b, partials, upart, sc, r0);
     return cudaGetLastError();
 }
 
-cudaError_t launch_hyperball_apply(const DescBatch& b, float lr, const Scalars& sc, const float* o_scale,
-                                   cudaStream_t st) {
+cudaError_t launch_hyperball_finish(const DescBatch& b, float lr, const Scalars& sc, const float* o_scale,
+                                    cudaStream_t st) {
     const int nblk = b.chunk_end - b.chunk_begin;
     if (nblk <= 0) return cudaSuccess;
-    hyperball_kernel<true><<<nblk, kThreads, 0, st>>>(b, lr, nullptr, sc.factor, sc.flags, o_scale);
+    hyperball_finish_kernel<<<nblk, kThreads, 0, st>>>(b, lr, sc.factor, sc.flags, o_scale);
     return cudaGetLastError();
 }
 

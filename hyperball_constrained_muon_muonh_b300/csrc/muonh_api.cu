@@ -6,11 +6,12 @@
 // orthogonalisation of the momentum, then retraction of W - lr*O onto the
 // sphere of radius r0 = ||W0||_F.
 //
-// Planner: matrices are grouped into buckets of equal (s, l) = (short side,
-// long side); a tall matrix (rows > cols) is handled through its transpose,
-// so one bucket holds both orientations.  Each bucket's Newton-Schulz state
-// lives contiguously in the workspace ([G][s][ld] tensors), so one GEMM
-// launch covers the whole bucket through 3-D TMA descriptors.
+// Planner: matrices are grouped into buckets of equal shape (R, C).  Each
+// matrix keeps its own orientation throughout: a tall matrix (R > C) is
+// orthogonalised through its Gram X^T X and X <- a X + X B rather than
+// through a transposed copy.  Each bucket's Newton-Schulz state lives
+// contiguously in the workspace ([G][R][ld_x] and [G][s][ld_s] tensors), so
+// one GEMM launch covers the whole bucket through 3-D TMA descriptors.
 
 #include <algorithm>
 #include <cmath>
@@ -27,15 +28,15 @@
 
 namespace muonh {
 
-cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, cudaStream_t st);
+cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, NsIO* io, cudaStream_t st);
 cudaError_t launch_momentum_finalize(const DescBatch& b, const double* partials, const Scalars& sc, float eps,
                                      cudaStream_t st);
 cudaError_t launch_hyperball_norm(const DescBatch& b, float lr, double* partials, const float* o_scale,
                                   cudaStream_t st);
-cudaError_t launch_hyperball_finalize(const DescBatch& b, const double* partials, const Scalars& sc,
-                                      const float* r0, cudaStream_t st);
-cudaError_t launch_hyperball_apply(const DescBatch& b, float lr, const Scalars& sc, const float* o_scale,
-                                   cudaStream_t st);
+cudaError_t launch_hyperball_finalize(const DescBatch& b, const double* partials, const double* upart,
+                                      const Scalars& sc, const float* r0, cudaStream_t st);
+cudaError_t launch_hyperball_finish(const DescBatch& b, float lr, const Scalars& sc, const float* o_scale,
+                                    cudaStream_t st);
 cudaError_t launch_emit(const DescBatch& b, const float* o_scale, cudaStream_t st);
 cudaError_t launch_capture_norms(const DescBatch& b, float* r0, cudaStream_t st);
 cudaError_t status_word(uint32_t** ptr);
@@ -57,10 +58,13 @@ int cuda_fail(cudaError_t e, const char* where) {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ---- tracing: per-kernel CUDA-event timing ---------------------------------
-enum Kind { K_MOMENTUM, K_MOM_FIN, K_GRAM, K_POLY, K_APPLY, K_HB_NORM, K_HB_FIN, K_HB_APPLY, K_EMIT, K_CAPTURE,
-            K_SIMT_GRAM, K_SIMT_POLY, K_SIMT_APPLY, K_COUNT };
+// ns_apply_in / _out / _in_out: the apply launches that read X from the
+// matrices' own input, write U = W - lr*O, or both (first / last iteration)
+enum Kind { K_MOMENTUM, K_MOM_FIN, K_GRAM, K_POLY, K_APPLY, K_APPLY_IN, K_APPLY_OUT, K_APPLY_IN_OUT, K_HB_NORM,
+            K_HB_FIN, K_HB_APPLY, K_HB_SCALE, K_EMIT, K_CAPTURE, K_SIMT_GRAM, K_SIMT_POLY, K_SIMT_APPLY, K_COUNT };
 const char* const kKindName[K_COUNT] = {"momentum", "momentum_finalize", "ns_gram", "ns_poly", "ns_apply",
-                                        "hyperball_norm", "hyperball_finalize", "hyperball_apply", "emit",
+                                        "ns_apply_in", "ns_apply_out", "ns_apply_in_out", "hyperball_norm",
+                                        "hyperball_finalize", "hyperball_apply", "hyperball_scale", "emit",
                                         "capture_norms", "fp32_gram", "fp32_poly", "fp32_apply"};
 
 std::atomic<long long> g_launches{0};
@@ -117,23 +121,42 @@ struct Trace {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct Bucket {
-    int s, l, G;
+    int R, C;             // matrix shape (rows, cols)
+    int s, l, G;          // short side, long side, matrices
+    bool tall;            // R > C
+    bool fusable;         // C % 4 == 0: the apply GEMM can read and write the matrices' own buffers
     int first;            // bucket-order index of its first matrix
     int ld_x, ld_s;
-    size_t off_xs, off_xo, off_af, off_aop;   // byte offsets in the workspace
-    size_t x_elems() const { return (size_t)G * s * ld_x; }
-    size_t s_elems() const { return (size_t)G * s * ld_s; }
+    size_t off_xs, off_xo;                    // byte offsets in the workspace
+    size_t off_af, off_aop, off_bop;          // this bucket's slice of its s-group's s x s buffers
+    size_t off_bf32;                          // fp32 check mode: its slice of the group's fp32 B
+    long long upart0;                         // first ||U||^2 partial of this bucket (index into the
+                                              // plan's partial region; written by the last apply GEMM)
+    int tiles1, tiles2;                       // apply tiles per matrix: 1-SM and pair kernel
+    size_t x_elems() const { return (size_t)G * R * ld_x; }
+};
+
+// Buckets with the same short side s share one set of s x s buffers (Gram
+// A fp32, A_op and B_op bf16, [G][s][ld_s] each), so one polynomial launch
+// covers all of them.
+struct SGroup {
+    int s, ld_s, G;
+    int b_begin, b_end;   // its buckets, contiguous in Plan::buckets
+    size_t off_af, off_aop, off_bop;
+    size_t elems() const { return (size_t)G * s * ld_s; }
 };
 
 struct Plan {
     int n = 0;
     std::vector<Bucket> buckets;
+    std::vector<SGroup> sgroups;
     std::vector<int> order;       // bucket-order position -> caller index
     std::vector<int> slot;        // bucket-order position -> slot in its bucket
     std::vector<int> bucket_of;   // bucket-order position -> bucket index
     std::vector<int> chunk0;      // bucket-order position -> first chunk
     int total_chunks = 0;
-    size_t off_nu2, off_rho2, off_inv, off_inv2, off_fac, off_flags, off_partials;
+    size_t off_nu2, off_rho2, off_inv, off_inv2, off_fac, off_flags, off_partials, off_io, off_upart;
+    long long n_upart = 0;        // ||U||^2 partials of the last apply GEMM, all buckets
     size_t bytes = 0;
 };
 
@@ -152,11 +175,8 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
     (void)flags;
     Plan P;
     P.n = n;
-    std::map<std::pair<int, int>, std::vector<int>> groups;  // (s, l) -> caller indices
-    for (int i = 0; i < n; ++i) {
-        const int r = (int)rc[2 * i], c = (int)rc[2 * i + 1];
-        groups[{std::min(r, c), std::max(r, c)}].push_back(i);
-    }
+    std::map<std::pair<int, int>, std::vector<int>> groups;  // (rows, cols) -> caller indices
+    for (int i = 0; i < n; ++i) groups[{(int)rc[2 * i], (int)rc[2 * i + 1]}].push_back(i);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         off = align_up(off, 256);
@@ -170,37 +190,82 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
     P.off_inv2 = take(sizeof(float) * n);
     P.off_fac = take(sizeof(float) * n);
     P.off_flags = take(sizeof(uint32_t) * n);
+    P.off_io = take(sizeof(NsIO) * n);
+    // s-groups with the most Newton-Schulz work first, and within one the
     // largest buckets first: their GEMMs are the longest launches
-    std::vector<std::pair<std::pair<int, int>, std::vector<int>>> gl(groups.begin(), groups.end());
-    std::stable_sort(gl.begin(), gl.end(), [](const auto& a, const auto& b) {
-        return (double)a.first.first * a.first.second * a.second.size() >
-               (double)b.first.first * b.first.second * b.second.size();
+    struct Shape { int R, C; std::vector<int> idx; double work; };
+    std::map<int, std::vector<Shape>> by_s;
+    for (auto& kv : groups) {
+        const int R = kv.first.first, C = kv.first.second, sd = std::min(R, C), ld = std::max(R, C);
+        by_s[sd].push_back({R, C, kv.second, (double)sd * sd * ld * kv.second.size()});
+    }
+    std::vector<std::vector<Shape>> sl_list;
+    for (auto& kv : by_s) {
+        std::stable_sort(kv.second.begin(), kv.second.end(), [](const Shape& a, const Shape& b) { return a.work > b.work; });
+        sl_list.push_back(kv.second);
+    }
+    std::stable_sort(sl_list.begin(), sl_list.end(), [](const std::vector<Shape>& a, const std::vector<Shape>& b) {
+        double wa = 0, wb = 0;
+        for (auto& x : a) wa += x.work;
+        for (auto& x : b) wb += x.work;
+        return wa > wb;
     });
     int chunk = 0;
-    for (auto& kv : gl) {
-        Bucket B;
-        B.s = kv.first.first;
-        B.l = kv.first.second;
-        B.G = (int)kv.second.size();
-        B.first = (int)P.order.size();
-        B.ld_x = (int)align_up(B.l, 8);
-        B.ld_s = (int)align_up(B.s, 8);
-        B.off_xs = take(sizeof(float) * B.x_elems());
-        B.off_xo = take(2 * sizeof(__nv_bfloat16) * B.x_elems());    // two bf16 buffers (ping-pong)
-        B.off_af = take(sizeof(float) * B.s_elems());
-        B.off_aop = take(2 * sizeof(__nv_bfloat16) * B.s_elems());   // A_op then B_op
-        int sl = 0;
-        for (int i : kv.second) {
-            P.order.push_back(i);
-            P.slot.push_back(sl++);
-            P.bucket_of.push_back((int)P.buckets.size());
-            P.chunk0.push_back(chunk);
-            chunk += chunks_for((int)rc[2 * i], (int)rc[2 * i + 1]);
+    long long n_upart = 0;
+    for (auto& shapes : sl_list) {
+        SGroup S;
+        S.s = std::min(shapes[0].R, shapes[0].C);
+        S.ld_s = (int)align_up(S.s, 8);
+        S.G = 0;
+        S.b_begin = (int)P.buckets.size();
+        for (auto& sh : shapes) S.G += (int)sh.idx.size();
+        S.off_af = take(sizeof(float) * S.elems());
+        S.off_aop = take(sizeof(__nv_bfloat16) * S.elems());
+        // fp32 check mode keeps an fp32 B at off_aop, spanning A_op and B_op
+        S.off_bop = take(sizeof(__nv_bfloat16) * S.elems());
+        int g_in_group = 0;
+        for (auto& sh : shapes) {
+            Bucket B;
+            B.R = sh.R;
+            B.C = sh.C;
+            B.s = S.s;
+            B.l = std::max(B.R, B.C);
+            B.tall = B.R > B.C;
+            B.fusable = (B.C & 3) == 0;
+            B.G = (int)sh.idx.size();
+            B.first = (int)P.order.size();
+            B.ld_x = (int)align_up(B.C, 8);
+            B.ld_s = S.ld_s;
+            B.off_xs = take(sizeof(float) * B.x_elems());
+            B.off_xo = take(2 * sizeof(__nv_bfloat16) * B.x_elems());    // two bf16 buffers (ping-pong)
+            const size_t so = (size_t)g_in_group * S.s * S.ld_s;
+            B.off_af = S.off_af + sizeof(float) * so;
+            B.off_aop = S.off_aop + sizeof(__nv_bfloat16) * so;
+            B.off_bop = S.off_bop + sizeof(__nv_bfloat16) * so;
+            B.off_bf32 = S.off_aop + sizeof(float) * so;
+            g_in_group += B.G;
+            B.tiles1 = tc::tiles_per_matrix(NS_APPLY, B.R, B.C);
+            B.tiles2 = tc::pair_tiles_per_matrix(NS_APPLY, B.R, B.C);
+            B.upart0 = n_upart;
+            n_upart += (long long)B.G * std::max((long long)B.tiles1 * tc::kUPartsPerTile1,
+                                                 (long long)B.tiles2 * tc::kUPartsPerTilePair);
+            int sl = 0;
+            for (int i : sh.idx) {
+                P.order.push_back(i);
+                P.slot.push_back(sl++);
+                P.bucket_of.push_back((int)P.buckets.size());
+                P.chunk0.push_back(chunk);
+                chunk += chunks_for((int)rc[2 * i], (int)rc[2 * i + 1]);
+            }
+            P.buckets.push_back(B);
         }
-        P.buckets.push_back(B);
+        S.b_end = (int)P.buckets.size();
+        P.sgroups.push_back(S);
     }
     P.total_chunks = chunk;
     P.off_partials = take(sizeof(double) * std::max(chunk, 1));
+    P.n_upart = n_upart;
+    P.off_upart = take(sizeof(double) * (size_t)std::max(n_upart, 1LL));
     P.bytes = align_up(off, 256);
     return P;
 }
@@ -256,10 +321,23 @@ Scalars scalars_of(const Plan& P, uint8_t* ws) {
     return sc;
 }
 
+// How the tensor-core Newton-Schulz path meets its neighbours, for the
+// matrices of fusable buckets (row length a multiple of 4):
+//   in   the first apply reads X from each matrix's own input (the
+//        momentum kernel writes the NsIO table and no fp32 copy of X)
+//   out  the last apply writes U = W - lr*O and its ||U||^2 partials
+//   pair the partials' layout is the pair kernel's (else the 1-SM kernel's)
+struct NsFuse {
+    bool in = false;
+    bool out = false;
+    bool pair = true;
+    float lr = 0.f;
+};
+
 // Descriptor batches in bucket order.  `x_in_alt` points the hyperball /
 // emit view of X at the second fp32 buffer (fp32 check mode, odd step count).
 std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, uint8_t* ws, bool x_in_alt,
-                                    bool with_momentum) {
+                                    bool with_momentum, const NsFuse& fuse = NsFuse()) {
     std::vector<DescBatch> out;
     const int n = P.n;
     for (int b0 = 0; b0 < n; b0 += kMaxDescPerLaunch) {
@@ -277,7 +355,7 @@ std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, u
             D.wb = with_momentum ? m.w_bf16 : nullptr;
             D.g = with_momentum ? m.grad : m.w;
             D.m = with_momentum ? m.mom : nullptr;
-            const size_t xoff = (size_t)P.slot[p] * bk.s * bk.ld_x;
+            const size_t xoff = (size_t)P.slot[p] * bk.R * bk.ld_x;
             float* xs = reinterpret_cast<float*>(ws + bk.off_xs);
             float* x2 = reinterpret_cast<float*>(ws + bk.off_xo);
             D.xs = (x_in_alt ? x2 : xs) + xoff;
@@ -287,7 +365,18 @@ std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, u
             D.ld = bk.ld_x;
             D.chunk0 = P.chunk0[p];
             D.user_index = u;
-            D.pad_ = 0;
+            D.part0 = 0;
+            D.npart = 0;
+            D.fused = 0;
+            if (bk.fusable) {
+                if (fuse.in) D.fused |= kFusedIn;
+                if (fuse.out) {
+                    const int per = fuse.pair ? bk.tiles2 * tc::kUPartsPerTilePair : bk.tiles1 * tc::kUPartsPerTile1;
+                    D.fused |= kFusedOut;
+                    D.part0 = (int)(bk.upart0 + (long long)P.slot[p] * per);
+                    D.npart = per;
+                }
+            }
         }
         B.chunk_begin = P.chunk0[b0];
         B.chunk_end = (b0 + B.n < n) ? P.chunk0[b0 + B.n] : P.total_chunks;
@@ -314,116 +403,171 @@ struct Sync {
     }
 };
 
-// Newton-Schulz over every bucket.  Returns MUONH_OK or an error code;
-// *x_in_alt tells where the fp32 result sits (check mode).
+// Newton-Schulz over every bucket: per iteration and s-group, the Gram of
+// each bucket, one polynomial launch for the group, the apply of each bucket.
+// Returns MUONH_OK or an error code; *x_in_alt tells where the fp32 result
+// sits (check mode).
 int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_steps, const float* coeffs,
-                      uint32_t flags, uint32_t* status, Sync& sy, bool* x_in_alt) {
+                      uint32_t flags, uint32_t* status, Sync& sy, bool* x_in_alt, const NsFuse& fuse) {
     const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
     const bool pair = (flags & MUONH_FLAG_GEMM_1SM) == 0;
     *x_in_alt = false;
+
+    // ---- fp32 check mode (CUDA cores) ----
+    auto simt_gram = [&](const Bucket& B, int it) {
+        float* xs = reinterpret_cast<float*>(ws + B.off_xs);
+        float* x2 = reinterpret_cast<float*>(ws + B.off_xo);
+        float* xc = (it & 1) ? x2 : xs;
+        const long long xstr = (long long)B.R * B.ld_x, sstr = (long long)B.s * B.ld_s;
+        // X X^T (wide) reads X rows as [m][k]; X^T X (tall) reads them as [k][m]
+        SimtParams g{};
+        g.mode = NS_GRAM; g.G = B.G; g.M = B.s; g.N = B.s; g.K = B.l;
+        g.a_km = B.tall; g.b_kn = B.tall;
+        g.a = xc; g.lda = B.ld_x; g.a_bstride = xstr;
+        g.b = xc; g.ldb = B.ld_x; g.b_bstride = xstr;
+        g.out = reinterpret_cast<float*>(ws + B.off_af); g.ldo = B.ld_s; g.out_bstride = sstr;
+        g.scale = it == 0 ? sc.inv_nu2 + B.first : nullptr;
+        const double G = B.G, S = B.s, L = B.l;
+        Trace tr(K_SIMT_GRAM, sy.st);
+        return sy.check(tr.done(launch_simt_gemm(g, sy.st), G * S * S * L, G * S * L * 4 + G * S * S * 4),
+                        "fp32 Gram launch");
+    };
+    auto simt_poly = [&](const SGroup& Q) {
+        const long long sstr = (long long)Q.s * Q.ld_s;
+        float* af = reinterpret_cast<float*>(ws + Q.off_af);
+        SimtParams q{};
+        q.mode = NS_POLY; q.G = Q.G; q.M = Q.s; q.N = Q.s; q.K = Q.s;
+        q.a = af; q.lda = Q.ld_s; q.a_bstride = sstr;
+        q.b = af; q.ldb = Q.ld_s; q.b_bstride = sstr;
+        q.addend = af; q.ld_add = Q.ld_s; q.add_bstride = sstr;
+        q.out = reinterpret_cast<float*>(ws + Q.off_aop); q.ldo = Q.ld_s; q.out_bstride = sstr;
+        q.cb = coeffs[1]; q.cc = coeffs[2];
+        const double G = Q.G, S = Q.s;
+        Trace tr(K_SIMT_POLY, sy.st);
+        return sy.check(tr.done(launch_simt_gemm(q, sy.st), G * S * S * S, G * S * S * 12), "fp32 polynomial launch");
+    };
+    auto simt_apply = [&](const Bucket& B, int it) {
+        float* xs = reinterpret_cast<float*>(ws + B.off_xs);
+        float* x2 = reinterpret_cast<float*>(ws + B.off_xo);
+        float* xc = (it & 1) ? x2 : xs;
+        float* xn = (it & 1) ? xs : x2;
+        const long long xstr = (long long)B.R * B.ld_x, sstr = (long long)B.s * B.ld_s;
+        float* bf = reinterpret_cast<float*>(ws + B.off_bf32);
+        // B X (wide: A = B, B = X rows [k][n]) or X B (tall: A = X rows [m][k],
+        // B = B, symmetric, read as [k][n])
+        SimtParams a{};
+        a.mode = NS_APPLY; a.G = B.G; a.M = B.R; a.N = B.C; a.K = B.s;
+        a.b_kn = 1;
+        if (B.tall) {
+            a.a = xc; a.lda = B.ld_x; a.a_bstride = xstr;
+            a.b = bf; a.ldb = B.ld_s; a.b_bstride = sstr;
+        } else {
+            a.a = bf; a.lda = B.ld_s; a.a_bstride = sstr;
+            a.b = xc; a.ldb = B.ld_x; a.b_bstride = xstr;
+        }
+        a.addend = xc; a.ld_add = B.ld_x; a.add_bstride = xstr;
+        a.out = xn; a.ldo = B.ld_x; a.out_bstride = xstr;
+        a.scale = it == 0 ? sc.inv_nu + B.first : nullptr;
+        a.ca = coeffs[0];
+        const double G = B.G, S = B.s, L = B.l;
+        Trace tr(K_SIMT_APPLY, sy.st);
+        return sy.check(tr.done(launch_simt_gemm(a, sy.st), 2 * G * S * S * L, G * S * S * 4 + G * S * L * 12),
+                        "fp32 apply launch");
+    };
+
+    // ---- tensor cores ----
+    auto x_ops = [&](const Bucket& B, int it, __nv_bfloat16** xc, __nv_bfloat16** xn) {
+        __nv_bfloat16* xo0 = reinterpret_cast<__nv_bfloat16*>(ws + B.off_xo);
+        __nv_bfloat16* xo1 = xo0 + B.x_elems();
+        *xc = (it & 1) ? xo1 : xo0;
+        *xn = (it & 1) ? xo0 : xo1;
+    };
+    auto tc_gram = [&](const Bucket& B, int it) {
+        __nv_bfloat16 *xc, *xn;
+        x_ops(B, it, &xc, &xn);
+        const char* why = "";
+        // K-major rows of X (wide) or MN-major columns (tall)
+        GemmParams g{};
+        g.mode = NS_GRAM; g.G = B.G; g.M = B.s; g.N = B.s; g.K = B.l;
+        g.a_mn = g.b_mn = B.tall;
+        g.ld_x = B.ld_x; g.ld_s = B.ld_s;
+        g.a_f32 = reinterpret_cast<float*>(ws + B.off_af);
+        g.sym_bf16 = reinterpret_cast<__nv_bfloat16*>(ws + B.off_aop);
+        g.scale = it == 0 ? sc.inv_nu2 + B.first : nullptr;
+        g.status = status;
+        const double G = B.G, S = B.s, L = B.l;
+        cudaError_t e;
+        {
+            Trace tr(K_GRAM, sy.st);
+            e = tr.done(tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, pair, sy.st, &why), G * S * S * L,
+                        G * S * L * 2 + G * S * S * 6);
+        }
+        return sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 Gram launch");
+    };
+    auto tc_poly = [&](const SGroup& Q) {
+        const char* why = "";
+        __nv_bfloat16* aop = reinterpret_cast<__nv_bfloat16*>(ws + Q.off_aop);
+        GemmParams q{};
+        q.mode = NS_POLY; q.G = Q.G; q.M = Q.s; q.N = Q.s; q.K = Q.s;
+        q.ld_s = Q.ld_s;
+        q.a_f32 = reinterpret_cast<float*>(ws + Q.off_af);
+        q.sym_bf16 = reinterpret_cast<__nv_bfloat16*>(ws + Q.off_bop);
+        q.cb = coeffs[1]; q.cc = coeffs[2];
+        q.status = status;
+        const double G = Q.G, S = Q.s;
+        cudaError_t e;
+        {
+            Trace tr(K_POLY, sy.st);
+            e = tr.done(tc::launch_ns_gemm(q, aop, Q.ld_s, aop, Q.ld_s, pair, sy.st, &why), G * S * S * S,
+                        G * S * S * 8);
+        }
+        return sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 polynomial launch");
+    };
+    auto tc_apply = [&](const Bucket& B, int it) {
+        __nv_bfloat16 *xc, *xn;
+        x_ops(B, it, &xc, &xn);
+        __nv_bfloat16* bop = reinterpret_cast<__nv_bfloat16*>(ws + B.off_bop);
+        const char* why = "";
+        // B X (wide: A = B_op, B = X_op MN-major) or X B (tall: A = X_op,
+        // B = B_op, both K-major; B is symmetric)
+        GemmParams a{};
+        a.mode = NS_APPLY; a.G = B.G; a.M = B.R; a.N = B.C; a.K = B.s;
+        a.b_mn = !B.tall;
+        a.m_outer = B.tall;
+        a.ld_x = B.ld_x; a.ld_s = B.ld_s;
+        a.x_state = reinterpret_cast<float*>(ws + B.off_xs);
+        a.x_op_out = (it + 1 < ns_steps) ? xn : nullptr;
+        a.scale = it == 0 ? sc.inv_nu + B.first : nullptr;
+        a.ca = coeffs[0];
+        a.status = status;
+        if (B.fusable)
+            a.variant = (fuse.in && it == 0 ? NS_IN_SRC : 0) | (fuse.out && it + 1 == ns_steps ? NS_OUT_U : 0);
+        a.io = reinterpret_cast<const NsIO*>(ws + P.off_io) + B.first;
+        a.upart = reinterpret_cast<double*>(ws + P.off_upart) + B.upart0;
+        a.nlr = -fuse.lr;
+        const double G = B.G, S = B.s, L = B.l;
+        cudaError_t e;
+        {
+            // bytes: B_op, X read and written (fp32), X_op written unless last, W read when fused
+            const double per_el = 8.0 + (a.x_op_out ? 2.0 : 0.0) + ((a.variant & NS_OUT_U) ? 4.0 : 0.0);
+            Trace tr(K_APPLY + a.variant, sy.st);
+            e = tr.done(B.tall ? tc::launch_ns_gemm(a, xc, B.ld_x, bop, B.ld_s, pair, sy.st, &why)
+                               : tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, pair, sy.st, &why),
+                        2 * G * S * S * L, G * S * S * 2 + G * S * L * per_el);
+        }
+        return sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 apply launch");
+    };
+
     for (int it = 0; it < ns_steps; ++it) {
-        for (const Bucket& B : P.buckets) {
-            float* xs = reinterpret_cast<float*>(ws + B.off_xs);
-            float* af = reinterpret_cast<float*>(ws + B.off_af);
-            const float* inv = sc.inv_nu + B.first;
-            const float* inv2 = sc.inv_nu2 + B.first;
-            if (check) {
-                float* x2 = reinterpret_cast<float*>(ws + B.off_xo);
-                float* bf = reinterpret_cast<float*>(ws + B.off_aop);
-                float* xc = (it & 1) ? x2 : xs;
-                float* xn = (it & 1) ? xs : x2;
-                const long long xstr = (long long)B.s * B.ld_x, sstr = (long long)B.s * B.ld_s;
-                SimtParams g{};
-                g.mode = NS_GRAM; g.G = B.G; g.M = B.s; g.N = B.s; g.K = B.l;
-                g.a = xc; g.lda = B.ld_x; g.a_bstride = xstr;
-                g.b = xc; g.ldb = B.ld_x; g.b_bstride = xstr;
-                g.out = af; g.ldo = B.ld_s; g.out_bstride = sstr;
-                g.scale = it == 0 ? inv2 : nullptr;
-                const double G = B.G, S = B.s, L = B.l;
-                int r;
-                {
-                    Trace tr(K_SIMT_GRAM, sy.st);
-                    r = sy.check(tr.done(launch_simt_gemm(g, sy.st), G * S * S * L, G * S * L * 4 + G * S * S * 4),
-                                 "fp32 Gram launch");
-                }
+        for (const SGroup& Q : P.sgroups) {
+            for (int b = Q.b_begin; b < Q.b_end; ++b) {
+                const int r = check ? simt_gram(P.buckets[b], it) : tc_gram(P.buckets[b], it);
                 if (r) return r;
-                SimtParams q{};
-                q.mode = NS_POLY; q.G = B.G; q.M = B.s; q.N = B.s; q.K = B.s;
-                q.a = af; q.lda = B.ld_s; q.a_bstride = sstr;
-                q.b = af; q.ldb = B.ld_s; q.b_bstride = sstr;
-                q.addend = af; q.ld_add = B.ld_s; q.add_bstride = sstr;
-                q.out = bf; q.ldo = B.ld_s; q.out_bstride = sstr;
-                q.cb = coeffs[1]; q.cc = coeffs[2];
-                {
-                    Trace tr(K_SIMT_POLY, sy.st);
-                    r = sy.check(tr.done(launch_simt_gemm(q, sy.st), G * S * S * S, G * S * S * 12),
-                                 "fp32 polynomial launch");
-                }
-                if (r) return r;
-                SimtParams a{};
-                a.mode = NS_APPLY; a.G = B.G; a.M = B.s; a.N = B.l; a.K = B.s;
-                a.a = bf; a.lda = B.ld_s; a.a_bstride = sstr;
-                a.b = xc; a.ldb = B.ld_x; a.b_bstride = xstr;
-                a.addend = xc; a.ld_add = B.ld_x; a.add_bstride = xstr;
-                a.out = xn; a.ldo = B.ld_x; a.out_bstride = xstr;
-                a.scale = it == 0 ? inv : nullptr;
-                a.ca = coeffs[0];
-                {
-                    Trace tr(K_SIMT_APPLY, sy.st);
-                    r = sy.check(tr.done(launch_simt_gemm(a, sy.st), 2 * G * S * S * L, G * S * S * 4 + G * S * L * 12),
-                                 "fp32 apply launch");
-                }
-                if (r) return r;
-            } else {
-                __nv_bfloat16* xo0 = reinterpret_cast<__nv_bfloat16*>(ws + B.off_xo);
-                __nv_bfloat16* xo1 = xo0 + B.x_elems();
-                __nv_bfloat16* aop = reinterpret_cast<__nv_bfloat16*>(ws + B.off_aop);
-                __nv_bfloat16* bop = aop + B.s_elems();
-                __nv_bfloat16* xc = (it & 1) ? xo1 : xo0;
-                __nv_bfloat16* xn = (it & 1) ? xo0 : xo1;
-                const char* why = "";
-                GemmParams g{};
-                g.mode = NS_GRAM; g.G = B.G; g.M = B.s; g.N = B.s; g.K = B.l;
-                g.ld_x = B.ld_x; g.ld_s = B.ld_s;
-                g.a_f32 = af; g.sym_bf16 = aop;
-                g.scale = it == 0 ? inv2 : nullptr;
-                g.status = status;
-                const double G = B.G, S = B.s, L = B.l;
-                cudaError_t e;
-                {
-                    Trace tr(K_GRAM, sy.st);
-                    e = tr.done(tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, pair, sy.st, &why), G * S * S * L,
-                                G * S * L * 2 + G * S * S * 6);
-                }
-                int r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 Gram launch");
-                if (r) return r;
-                GemmParams q{};
-                q.mode = NS_POLY; q.G = B.G; q.M = B.s; q.N = B.s; q.K = B.s;
-                q.ld_x = B.ld_x; q.ld_s = B.ld_s;
-                q.a_f32 = af; q.sym_bf16 = bop;
-                q.cb = coeffs[1]; q.cc = coeffs[2];
-                q.status = status;
-                {
-                    Trace tr(K_POLY, sy.st);
-                    e = tr.done(tc::launch_ns_gemm(q, aop, B.ld_s, aop, B.ld_s, pair, sy.st, &why), G * S * S * S,
-                                G * S * S * 8);
-                }
-                r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 polynomial launch");
-                if (r) return r;
-                GemmParams a{};
-                a.mode = NS_APPLY; a.G = B.G; a.M = B.s; a.N = B.l; a.K = B.s;
-                a.ld_x = B.ld_x; a.ld_s = B.ld_s;
-                a.x_state = xs;
-                a.x_op_out = (it + 1 < ns_steps) ? xn : nullptr;
-                a.scale = it == 0 ? inv : nullptr;
-                a.ca = coeffs[0];
-                a.status = status;
-                {
-                    Trace tr(K_APPLY, sy.st);
-                    e = tr.done(tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, pair, sy.st, &why), 2 * G * S * S * L,
-                                G * S * S * 2 + G * S * L * (a.x_op_out ? 12 : 10));
-                }
-                r = sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 apply launch");
+            }
+            int r = check ? simt_poly(Q) : tc_poly(Q);
+            if (r) return r;
+            for (int b = Q.b_begin; b < Q.b_end; ++b) {
+                r = check ? simt_apply(P.buckets[b], it) : tc_apply(P.buckets[b], it);
                 if (r) return r;
             }
         }
@@ -547,12 +691,35 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     const Scalars sc = scalars_of(P, ws);
     double* partials = reinterpret_cast<double*>(ws + P.off_partials);
 
-    std::vector<DescBatch> batches = make_batches(P, mats, ws, false, true);
+    // Tensor-core path with at least one iteration, for the matrices whose
+    // row length is a multiple of 4: momentum writes no fp32 copy of X (the
+    // first apply reads M), and the last apply writes U = W - lr*O with its
+    // ||U||^2 partials, so their hyperball step is one finalize plus a
+    // rescale.  Other matrices, the fp32 check mode and ns_steps = 0 keep the
+    // separate norm and apply passes.
+    const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
+    NsFuse fuse;
+    fuse.in = fuse.out = !check && ns_steps >= 1;
+    fuse.pair = (flags & MUONH_FLAG_GEMM_1SM) == 0;
+    fuse.lr = lr;
+    if (fuse.out && P.n_upart > INT32_MAX)
+        return fail(MUONH_ERR_UNSUPPORTED, "too many matrices/tiles for one step: split the list");
+    NsIO* io = fuse.in ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
+    const double* upart = reinterpret_cast<const double*>(ws + P.off_upart);
+
+    std::vector<DescBatch> batches = make_batches(P, mats, ws, false, true, fuse);
+    // elements of the batch's matrices with and without a fusion bit
+    auto elems = [](const DescBatch& b, int bit, bool with) {
+        double e = 0;
+        for (int k = 0; k < b.n; ++k)
+            if (((b.d[k].fused & bit) != 0) == with) e += (double)b.d[k].rows * b.d[k].cols;
+        return e;
+    };
     for (const DescBatch& B : batches) {
-        const double e = batch_elems(B);
+        const double bytes = 14 * elems(B, kFusedIn, true) + 18 * elems(B, kFusedIn, false);
         {
             Trace tr(K_MOMENTUM, st);
-            r = sy.check(tr.done(launch_momentum(B, beta, partials, st), 0, e * 18), "momentum launch");
+            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, st), 0, bytes), "momentum launch");
         }
         if (r) return r;
         {
@@ -562,26 +729,28 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
         if (r) return r;
     }
     bool x_alt = false;
-    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt);
+    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
     if (r) return r;
     if (x_alt) batches = make_batches(P, mats, ws, true, true);
     const float* o_scale = ns_steps == 0 ? sc.inv_nu : nullptr;
     for (const DescBatch& B : batches) {
-        const double e = batch_elems(B);
-        {
+        const double e_sep = elems(B, kFusedOut, false), e_fused = elems(B, kFusedOut, true);
+        if (e_sep > 0) {
             Trace tr(K_HB_NORM, st);
-            r = sy.check(tr.done(launch_hyperball_norm(B, lr, partials, o_scale, st), 0, e * 8), "hyperball norm launch");
+            r = sy.check(tr.done(launch_hyperball_norm(B, lr, partials, o_scale, st), 0, e_sep * 8),
+                         "hyperball norm launch");
+            if (r) return r;
         }
-        if (r) return r;
         {
             Trace tr(K_HB_FIN, st);
-            r = sy.check(tr.done(launch_hyperball_finalize(B, partials, sc, r0_dev, st), 0, 0),
+            r = sy.check(tr.done(launch_hyperball_finalize(B, partials, upart, sc, r0_dev, st), 0, 0),
                          "hyperball finalize launch");
         }
         if (r) return r;
         {
-            Trace tr(K_HB_APPLY, st);
-            r = sy.check(tr.done(launch_hyperball_apply(B, lr, sc, o_scale, st), 0, e * 14), "hyperball apply launch");
+            Trace tr(e_sep > 0 ? K_HB_APPLY : K_HB_SCALE, st);
+            r = sy.check(tr.done(launch_hyperball_finish(B, lr, sc, o_scale, st), 0, e_sep * 14 + e_fused * 10),
+                         "hyperball finish launch");
         }
         if (r) return r;
     }
@@ -624,11 +793,16 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     m.w = const_cast<float*>(in);
     m.rows = rows;
     m.cols = cols;
-    std::vector<DescBatch> batches = make_batches(P, &m, ws, false, false);
     const double el = (double)rows * cols;
+    NsFuse fuse;
+    fuse.in = (flags & MUONH_FLAG_FP32_CHECK) == 0 && ns_steps >= 1;
+    NsIO* io = fuse.in ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
+    std::vector<DescBatch> batches = make_batches(P, &m, ws, false, false, fuse);
+    const bool in_fused = (batches[0].d[0].fused & kFusedIn) != 0;
     {
         Trace tr(K_MOMENTUM, st);
-        r = sy.check(tr.done(launch_momentum(batches[0], 0.f, partials, st), 0, el * 10), "momentum launch");
+        r = sy.check(tr.done(launch_momentum(batches[0], 0.f, partials, io, st), 0, el * (in_fused ? 6 : 10)),
+                     "momentum launch");
     }
     if (r) return r;
     {
@@ -638,7 +812,7 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     }
     if (r) return r;
     bool x_alt = false;
-    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt);
+    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
     if (r) return r;
     m.w = out;
     batches = make_batches(P, &m, ws, x_alt, false);

@@ -9,14 +9,34 @@ namespace muonh {
 
 enum NsMode { NS_GRAM = 0, NS_POLY = 1, NS_APPLY = 2 };
 
-// One launch = one Newton-Schulz stage over a bucket of G matrices, all
-// s x l (ld_x = row stride of X buffers, ld_s = row stride of s x s buffers).
-//   GRAM : M = N = s, K = l.  a_f32 <- scale*X X^T, sym_bf16 <- bf16 of it
+// Variants of the apply stage (bit set):
+//   NS_IN_SRC   X is read from the matrix's own unscaled input (NsIO::src, W
+//               orientation) instead of the fp32 state: the first iteration
+//   NS_OUT_U    the epilogue finishes O = X and writes U = W - lr*O (X
+//               orientation) into the fp32 state, plus deterministic per-warp
+//               partial sums of ||U||^2: the last iteration of a MuonH step
+enum NsApplyVariant { NS_IN_SRC = 1, NS_OUT_U = 2 };
+
+struct NsIO;
+
+// One launch = one Newton-Schulz stage over a bucket of G same-shape
+// matrices.  X keeps the matrix's own orientation, R x C (row stride ld_x);
+// s = min(R, C), l = max(R, C); ld_s = row stride of the s x s buffers.
+//   GRAM : M = N = s, K = l.  a_f32 <- scale*Gram, sym_bf16 <- bf16 of it,
+//          Gram = X X^T (wide, R <= C) or X^T X (tall, R > C)
 //   POLY : M = N = K = s.     sym_bf16 <- cb*a_f32 + cc*(A A)
-//   APPLY: M = s, N = l, K = s.  x_state <- scale*(ca*x_state + B X);
-//          x_op_out <- bf16(x_state) unless null
+//   APPLY: M = R, N = C, K = s.  x_state <- scale*(ca*x_state + P), with
+//          P = B X (wide) or X B (tall); x_op_out <- bf16(x_state) unless
+//          null.  `variant` (NS_IN_SRC, NS_OUT_U) selects where X comes
+//          from and what is written.
+// Operand tiles are K-major (rows of the operand run along M or N, K
+// contiguous) unless a_mn / b_mn say MN-major (K runs along the rows).
 struct GemmParams {
     int mode;
+    int variant;            // apply only: NsApplyVariant bits
+    int a_mn, b_mn;         // operand A / B stored MN-major
+    int m_outer;            // apply: tiles ordered row panels outermost (consecutive tiles
+                            // share their A panel) instead of column panels outermost
     int G, M, N, K;
     int tiles_m, tiles_n, tiles_per_mat;   // filled by the launcher
     int ld_x, ld_s;
@@ -25,6 +45,9 @@ struct GemmParams {
     float* a_f32;
     __nv_bfloat16* sym_bf16;
     const float* scale;     // per-matrix factor (bucket-local index) or null
+    const NsIO* io;         // NS_IN_SRC / NS_OUT_U: per-matrix buffers (bucket-local index)
+    double* upart;          // NS_OUT_U: ||U||^2 partials, warps_per_tile per tile, tile order
+    float nlr;              // NS_OUT_U: -lr
     float ca, cb, cc;
     uint32_t* status;       // device status word
 };
@@ -33,17 +56,24 @@ namespace tc {
 cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld, bool pair,
                            cudaStream_t st, const char** why);
 int tiles_per_matrix(int mode, int M, int N);
+int pair_tiles_per_matrix(int mode, int M, int N);
+// ||U||^2 partials one apply tile writes: one per epilogue warp (8 per CTA,
+// two CTAs per tile in the pair kernel).
+constexpr int kUPartsPerTile1 = 8, kUPartsPerTilePair = 16;
 }  // namespace tc
 
-// fp32 CUDA-core GEMM for the accuracy-check mode.  Operands fp32:
-//   GRAM : a = X [G][s][ld_x]                 -> out = scale*X X^T (full s x s, ld_s)
-//   POLY : a = A [G][s][ld_s]                 -> out = cb*A + cc*A A
-//   APPLY: a = B [G][s][ld_s], x = X [G][s][ld_x] -> out = scale*(ca*X + B X) (ld_x)
+// fp32 CUDA-core GEMM for the accuracy-check mode: out = epilogue(A B) with
+// A M x K and B K x N.  a stored [m][k] (or [k][m] with a_km), b stored
+// [n][k] (or [k][n] with b_kn).  Epilogues:
+//   GRAM : out = scale*(A B)           (full s x s, ld_s)
+//   POLY : out = cb*addend + cc*(A B)
+//   APPLY: out = scale*(ca*addend + A B)
 struct SimtParams {
     int mode;
+    int a_km, b_kn;
     int G, M, N, K;
     const float* a; int lda; long long a_bstride;
-    const float* b; int ldb; long long b_bstride;   // GRAM/POLY: [N][K] rows; APPLY: [K][N] rows
+    const float* b; int ldb; long long b_bstride;
     const float* addend; int ld_add; long long add_bstride;  // POLY: A; APPLY: X
     float* out; int ldo; long long out_bstride;
     const float* scale;

@@ -1,9 +1,10 @@
 // fp32 CUDA-core GEMMs for the Newton-Schulz accuracy-check mode
 // (MUONH_FLAG_FP32_CHECK): the same three stages as the tensor-core path --
-// Gram X X^T, polynomial b*A + c*A A, apply a*X + B X -- with fp32 operands
-// and fp32 accumulation, so the result can be held to a 1e-4 relative
-// tolerance against the float64 oracle.  Plain 128x128 tiles, 8x8 outputs
-// per thread, no symmetry shortcuts: this path is for checking, not speed.
+// Gram (X X^T, or X^T X for a tall matrix), polynomial b*A + c*A A, apply
+// (a*X + B X, or a*X + X B) -- with fp32 operands and fp32 accumulation, so
+// the result can be held to a 1e-4 relative tolerance against the float64
+// oracle.  Plain 128x128 tiles, 8x8 outputs per thread, no symmetry
+// shortcuts: this path is for checking, not speed.
 
 #include "common.cuh"
 #include "ns_gemm.h"
@@ -29,8 +30,16 @@ __global__ void __launch_bounds__(ST) simt_gemm_kernel(const SimtParams p) {
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
     for (int k0 = 0; k0 < p.K; k0 += SK) {
-        // A tile: 128 rows x 8 k; thread -> row t/2, k (t&1)*4 .. +3
-        {
+        if (p.a_km) {
+            // A stored [k][m]: 8 x 128; thread -> k t/32, m (t&31)*4 .. +3
+            const int kk = t >> 5, mq = (t & 31) * 4;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int gk = k0 + kk, gi = m0 + mq + u;
+                As[kk][mq + u] = (gk < p.K && gi < p.M) ? A[(size_t)gk * p.lda + gi] : 0.f;
+            }
+        } else {
+            // A tile: 128 rows x 8 k; thread -> row t/2, k (t&1)*4 .. +3
             const int r = t >> 1, kq = (t & 1) * 4;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -38,7 +47,7 @@ __global__ void __launch_bounds__(ST) simt_gemm_kernel(const SimtParams p) {
                 As[kq + u][r] = (gi < p.M && gk < p.K) ? A[(size_t)gi * p.lda + gk] : 0.f;
             }
         }
-        if (MODE == NS_APPLY) {
+        if (p.b_kn) {
             // B rows are k: 8 x 128; thread -> k t/32, n (t&31)*4 .. +3
             const int kk = t >> 5, nq = (t & 31) * 4;
 #pragma unroll

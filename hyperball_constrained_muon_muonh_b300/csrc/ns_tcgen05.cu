@@ -1,21 +1,26 @@
 // Newton-Schulz GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
 // operands staged by TMA.  One iteration of the orthogonalisation (Puro-2B
 // digest, section "The load-bearing tricks aren't in the abstract": Muon's
-// Newton-Schulz iterations) on a bucket of G same-shape s x l matrices X:
+// Newton-Schulz iterations) on a bucket of G same-shape matrices X, each kept
+// in its own orientation R x C (s = min(R, C), l = max(R, C)):
 //
-//   GRAM   A = X X^T           (s x s, K = l)  symmetric: upper tiles only,
-//                                               epilogue writes A fp32, A bf16
-//                                               and their mirror images
+//   GRAM   A = X X^T (wide) or X^T X (tall)   (s x s, K = l)  symmetric: upper
+//                                               tiles only; epilogue writes A
+//                                               fp32, A bf16 and their mirrors
 //   POLY   B = b*A + c*A A     (s x s, K = s)  symmetric (A A = A A^T):
 //                                               upper tiles, B bf16 + mirror
-//   APPLY  X <- a*X + B X      (s x l, K = s)  X fp32 state read/written in the
-//                                               epilogue, bf16 operand copy out
+//   APPLY  X <- a*X + B X (wide) or a*X + X B (tall)   (R x C, K = s): X fp32
+//          state read/written in the epilogue, bf16 operand copy out
+//
+// A tall matrix is never transposed: its Gram reads both operands MN-major
+// (the instruction descriptor's transpose bits), and its apply multiplies by
+// B on the right, which reads both operands K-major.
 //
 // Persistent, warp-specialised kernel, one CTA per SM:
 //   warp 0      TMA producer (one thread) and TMEM allocator
 //   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, bf16 in,
 //               fp32 accumulate in TMEM, 128 x 256 tile, K step 16
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32*(w%4)..+31), fused arithmetic, global stores
 // Shared memory: 4-stage ring of (A 128x64, B 256x64) bf16 tiles, 128-byte
 // swizzle.  TMEM: two 256-column fp32 accumulators so the epilogue of one
@@ -124,11 +129,22 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
     return d;
 }
 
-// Instruction descriptor, kind::f16: D f32, A/B bf16, A K-major, B K- or
-// MN-major, N = 256, M = 128.
-__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) |
-           ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor, kind::f16: D f32, A/B bf16, A and B each K- or
+// MN-major (bits 15 / 16), N = 256, M = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+// Per-kk increment of an operand descriptor (start address field, 16-byte
+// units): 32 B along K for K-major tiles, 16 K-rows = 2048 B for MN-major.
+__device__ __forceinline__ uint64_t operand_desc_step(bool mn_major) { return mn_major ? (2048 >> 4) : (32 >> 4); }
+
+// Descriptor of the kk-th K=16 slice of a staged operand tile.  K-major: rows
+// of 64 K-elements (128 B, swizzled), 8-row groups 1024 B apart.  MN-major:
+// 64-element MN chunks of 64 K-rows each (8 KB apart), K rows 128 B apart.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk, bool mn_major) {
+    return mn_major ? sdesc(base + kk * 2048, 64 * BK * 2, 1024) : sdesc(base + kk * 32, 16, 1024);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -167,9 +183,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // (nj+1)*BN > mi*BM, i.e. nj >= mi/2 (BN = 2*BM).
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int local, int& mi, int& nj) {
     if (p.mode == NS_APPLY) {
-        // column panels outermost: consecutive CTAs share the X_op panel
-        nj = local / p.tiles_m;
-        mi = local - nj * p.tiles_m;
+        // the panel of the large operand X_op outermost, so consecutive CTAs
+        // share it: its column panel (wide, B operand) or row panel (tall, A)
+        if (p.m_outer) {
+            mi = local / p.tiles_n;
+            nj = local - mi * p.tiles_n;
+        } else {
+            nj = local / p.tiles_m;
+            mi = local - nj * p.tiles_m;
+        }
         return;
     }
     int m = 0;
@@ -218,17 +240,19 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
     *reinterpret_cast<uint2*>(dst) = u;
 }
 
-// Prefetch for APPLY: X[i0 + 4k + lane/8][j0 + 4*(lane%8) .. +3], k = 0..7.
-// Row strides are multiples of 8 elements, so a 4-wide access at a column
-// < N stays inside the padded row (padding columns are never read back).
-__device__ __forceinline__ void prefetch_x(const GemmParams& p, int g, int i0, int lane, int j0, float4 (&xp)[8]) {
+// Prefetch for APPLY: X[i0 + 4k + lane/8][j0 + 4*(lane%8) .. +3], k = 0..7,
+// from a row-major array with row stride `ld`.  For the fp32 state the row
+// stride is a multiple of 8 elements, so a 4-wide access at a column < N
+// stays inside the padded row (padding columns are never read back); a
+// caller's buffer (row stride N) is read this way only when N % 4 == 0.
+__device__ __forceinline__ void prefetch_rm(const float* base, int ld, int M, int N, int i0, int lane, int j0,
+                                            float4 (&xp)[8]) {
     const int col = j0 + (lane & 7) * 4;
-    const float* xs = p.x_state + (size_t)g * p.ld_x * p.M;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int row = i0 + k * 4 + (lane >> 3);
-        xp[k] = (row < p.M && col < p.N) ? __ldcs(reinterpret_cast<const float4*>(xs + (size_t)row * p.ld_x + col))
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        xp[k] = (row < M && col < N) ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)row * ld + col))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -244,8 +268,13 @@ __device__ __forceinline__ void prefetch_a(const GemmParams& p, int g, int i0, i
     }
 }
 
+// APPLY slice: X read in the staged layout (the fp32 state, or with
+// NS_IN_SRC the matrix's own input, row stride N).  y = sc*(a*x + (B X)); with NS_OUT_U, u = W - lr*y replaces
+// y and u^2 is added to hacc for the elements inside the matrix.
+template <int VAR>
 __device__ __forceinline__ void apply_slice(const GemmParams& p, int g, int i0, int lane, int j0,
-                                            const float (&v)[32], float* st, const float4 (&xp)[8], float sc) {
+                                            const float (&v)[32], float* st, const float4 (&xp)[8],
+                                            const float4 (&wp)[8], float sc, float& hacc) {
     stage_rows(st, lane, v);
     const int col = j0 + (lane & 7) * 4;
     float* xs = p.x_state + (size_t)g * p.ld_x * p.M;
@@ -260,6 +289,17 @@ __device__ __forceinline__ void apply_slice(const GemmParams& p, int g, int i0, 
             y.y = sc * fmaf(p.ca, xp[k].y, a.y);
             y.z = sc * fmaf(p.ca, xp[k].z, a.z);
             y.w = sc * fmaf(p.ca, xp[k].w, a.w);
+            if (VAR & NS_OUT_U) {
+                y.x = fmaf(p.nlr, y.x, wp[k].x);
+                y.y = fmaf(p.nlr, y.y, wp[k].y);
+                y.z = fmaf(p.nlr, y.z, wp[k].z);
+                y.w = fmaf(p.nlr, y.w, wp[k].w);
+                const int nv = p.N - col;
+                hacc = fmaf(y.x, y.x, hacc);
+                if (nv > 1) hacc = fmaf(y.y, y.y, hacc);
+                if (nv > 2) hacc = fmaf(y.z, y.z, hacc);
+                if (nv > 3) hacc = fmaf(y.w, y.w, hacc);
+            }
             const size_t off = (size_t)row * p.ld_x + col;
             *reinterpret_cast<float4*>(xs + off) = y;
             if (xo) store_bf16x4(xo + off, y);
@@ -317,8 +357,91 @@ __device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, in
     }
 }
 
+// One accumulator tile's epilogue for one warp: rows i0..i0+31 (TMEM lane
+// quarter of this warp), columns jb..jb+127 (four 32-column slices).  Loads
+// the operands the epilogue reads one slice ahead, waits for the
+// accumulator, releases it after the last TMEM read (`release`), and for
+// NS_OUT_U writes this warp's ||U||^2 partial to *upart_slot (0 when the
+// warp's rows or columns fall outside the matrix).  False if the wait gave up.
+template <int MODE, int VAR, class Release>
+__device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0, int jb, uint32_t tfull_bar,
+                                              uint32_t acc_phase, uint32_t trow, float* st, int lane,
+                                              volatile int* abort_flag, double* upart_slot, Release release) {
+    const int nsl = max(0, min(BN / 64, (p.N - jb + 31) / 32));
+    float sc = 1.f;
+    if (MODE != NS_POLY && p.scale) sc = p.scale[g];
+    // X source of the apply epilogue: the fp32 state (row stride ld_x), or
+    // the matrix's own input (row stride N; the variants need N % 4 == 0)
+    NsIO io{nullptr, nullptr};
+    const float* xbase = nullptr;
+    int xld = p.ld_x;
+    if (MODE == NS_APPLY) {
+        if (VAR != 0) io = p.io[g];
+        if (VAR & NS_IN_SRC) {
+            xbase = io.src;
+            xld = p.N;
+        } else {
+            xbase = p.x_state + (size_t)g * p.ld_x * p.M;
+        }
+    }
+    // Operands the epilogue reads are loaded one slice ahead.  With
+    // NS_OUT_U both X and W are read for the current slice only, at its
+    // start (the register budget holds two 32-value slices, not four).
+    constexpr bool ahead = !(MODE == NS_APPLY && (VAR & NS_OUT_U));
+    float4 xc[8], xn[8], wc[8];
+    float ac[32], an[32];
+    if (nsl > 0) {
+        if (MODE == NS_APPLY) prefetch_rm(xbase, xld, p.M, p.N, i0, lane, jb, xc);
+        if (MODE == NS_APPLY && (VAR & NS_OUT_U)) prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, jb, wc);
+        if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, jb, ac);
+    }
+    if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status)) return false;
+    tc_fence_after();
+    if (nsl == 0) release();
+    float hacc = 0.f;
+#pragma unroll
+    for (int k = 0; k < BN / 64; ++k) {
+        if (k < nsl) {
+            const int j0 = jb + 32 * k;
+            if (!ahead && k > 0) {
+                prefetch_rm(xbase, xld, p.M, p.N, i0, lane, j0, xc);
+                prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, j0, wc);
+            }
+            float v[32];
+            tmem_ld32(trow + 32 * k, v);
+            if (k == nsl - 1) {
+                // last read of this accumulator by this warp
+                tc_fence_before();
+                release();
+            }
+            if (k + 1 < nsl) {
+                if (MODE == NS_APPLY && ahead) prefetch_rm(xbase, xld, p.M, p.N, i0, lane, j0 + 32, xn);
+                if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, j0 + 32, an);
+            }
+            if (MODE == NS_APPLY) {
+                apply_slice<VAR>(p, g, i0, lane, j0, v, st, xc, wc, sc, hacc);
+                if (ahead) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) xc[u] = xn[u];
+                }
+            } else {
+                sym_slice<MODE>(p, g, i0, lane, j0, v, st, ac, sc);
+                if (MODE == NS_POLY) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ac[u] = an[u];
+                }
+            }
+        }
+    }
+    if (MODE == NS_APPLY && (VAR & NS_OUT_U)) {
+        const double s = warp_sum((double)hacc);
+        if (lane == 0) *upart_slot = s;
+    }
+    return true;
+}
+
 // ---- the kernel ----------------------------------------------------------------
-template <int MODE>
+template <int MODE, int VAR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ GemmParams p) {
@@ -363,7 +486,6 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 
     const int total = p.G * p.tiles_per_mat;
     const int num_kb = (p.K + BK - 1) / BK;
-    constexpr bool b_mn = (MODE == NS_APPLY);
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer ----------------
@@ -380,8 +502,13 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 mbar_expect_tx(fb, STAGE_BYTES);
                 const uint32_t sa = smem_u32(smem_a + stage * A_BYTES);
                 const uint32_t sb = smem_u32(smem_b + stage * B_BYTES);
-                tma_load_3d(sa, &tm_a, fb, kb * BK, mi * BM, g);
-                if (!b_mn) {
+                if (!p.a_mn) {
+                    tma_load_3d(sa, &tm_a, fb, kb * BK, mi * BM, g);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BM / 64; ++c) tma_load_3d(sa + c * (64 * BK * 2), &tm_a, fb, mi * BM + c * 64, kb * BK, g);
+                }
+                if (!p.b_mn) {
                     tma_load_3d(sb, &tm_b, fb, kb * BK, nj * BN, g);
                 } else {
 #pragma unroll
@@ -401,7 +528,10 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
-        const uint32_t idesc = idesc_bf16(b_mn);
+        const uint32_t idesc = idesc_bf16(p.a_mn != 0, p.b_mn != 0);
+        const uint64_t a_desc0 = operand_desc(smem_u32(smem_a), 0, p.a_mn != 0);
+        const uint64_t b_desc0 = operand_desc(smem_u32(smem_b), 0, p.b_mn != 0);
+        const uint64_t a_step = operand_desc_step(p.a_mn != 0), b_step = operand_desc_step(p.b_mn != 0);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -414,14 +544,12 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem_a + stage * A_BYTES);
-                const uint32_t sb = smem_u32(smem_b + stage * B_BYTES);
+                // descriptors: stage base plus add-only steps along K
+                const uint64_t ad = a_desc0 + (uint64_t)(stage * (A_BYTES >> 4));
+                const uint64_t bd = b_desc0 + (uint64_t)(stage * (B_BYTES >> 4));
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t ad = sdesc(sa + kk * 32, 16, 1024);
-                    const uint64_t bd = b_mn ? sdesc(sb + kk * 2048, 64 * BK * 2, 1024) : sdesc(sb + kk * 32, 16, 1024);
-                    mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_bf16(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc, (kb | kk) ? 1u : 0u);
                 mma_commit(empty0 + 8 * stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
@@ -432,60 +560,24 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
         // warp w reads TMEM lane quarter w%4; warps 2..5 take accumulator
-        // columns 0..127, warps 6..9 columns 128..255 (four 32-column slices)
+        // columns 0..127, warps 6..9 columns 128..255
         const int e = warp - 2;
         const int q = warp & 3;
         const int h = e >> 2;
         float* st = stage_base + e * ST_FLOATS;
         int acc = 0;
         uint32_t acc_phase = 0;
+        const uint32_t tempty_bar = tempty0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const int g = t / p.tiles_per_mat;
             int mi, nj;
             tile_coords(p, t - g * p.tiles_per_mat, mi, nj);
-            const int i0 = mi * BM + q * 32;
-            const int jb = nj * BN + h * (BN / 2);
-            const int nsl = max(0, min(BN / 64, (p.N - jb + 31) / 32));
-            float sc = 1.f;
-            if (MODE != NS_POLY && p.scale) sc = p.scale[g];
-            float4 xc[8], xn[8];
-            float ac[32], an[32];
-            if (nsl > 0) {
-                if (MODE == NS_APPLY) prefetch_x(p, g, i0, lane, jb, xc);
-                if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, jb, ac);
-            }
-            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.status)) break;
-            tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + h * (BN / 2));
-            if (nsl == 0) mbar_arrive(tempty0 + 8 * acc);
-#pragma unroll
-            for (int k = 0; k < BN / 64; ++k) {
-                if (k < nsl) {
-                    const int j0 = jb + 32 * k;
-                    float v[32];
-                    tmem_ld32(trow + 32 * k, v);
-                    if (k == nsl - 1) {
-                        // last read of this accumulator by this warp
-                        tc_fence_before();
-                        mbar_arrive(tempty0 + 8 * acc);
-                    }
-                    if (k + 1 < nsl) {
-                        if (MODE == NS_APPLY) prefetch_x(p, g, i0, lane, j0 + 32, xn);
-                        if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, j0 + 32, an);
-                    }
-                    if (MODE == NS_APPLY) {
-                        apply_slice(p, g, i0, lane, j0, v, st, xc, sc);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) xc[u] = xn[u];
-                    } else {
-                        sym_slice<MODE>(p, g, i0, lane, j0, v, st, ac, sc);
-                        if (MODE == NS_POLY) {
-#pragma unroll
-                            for (int u = 0; u < 32; ++u) ac[u] = an[u];
-                        }
-                    }
-                }
-            }
+            const uint32_t te = tempty_bar + 8 * acc;
+            double* slot = (VAR & NS_OUT_U) ? p.upart + (size_t)t * kUPartsPerTile1 + e : nullptr;
+            if (!epilogue_tile<MODE, VAR>(p, g, mi * BM + q * 32, nj * BN + h * (BN / 2), tfull0 + 8 * acc,
+                                          acc_phase, trow, st, lane, abort_flag, slot, [&]() { mbar_arrive(te); }))
+                break;
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
     }
@@ -570,17 +662,22 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
         : "memory");
 }
 
-__host__ __device__ constexpr uint32_t idesc_pair(bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) |
-           ((uint32_t)((2 * BM) >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_pair(bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((2 * BM) >> 4) << 24);
 }
 
 // Pair tile (mp, nj): rows mp*256 .. +255, columns nj*256 .. +255.
 // Symmetric modes keep nj >= mp.
 __device__ __forceinline__ void pair_coords(const GemmParams& p, int local, int& mp, int& nj) {
     if (p.mode == NS_APPLY) {
-        nj = local / p.tiles_m;
-        mp = local - nj * p.tiles_m;
+        if (p.m_outer) {
+            mp = local / p.tiles_n;
+            nj = local - mp * p.tiles_n;
+        } else {
+            nj = local / p.tiles_m;
+            mp = local - nj * p.tiles_m;
+        }
         return;
     }
     int m = 0;
@@ -594,7 +691,7 @@ __device__ __forceinline__ void pair_coords(const GemmParams& p, int local, int&
     nj = m + local;
 }
 
-template <int MODE>
+template <int MODE, int VAR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ GemmParams p) {
@@ -642,7 +739,6 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
 
     const int total = p.G * p.tiles_per_mat;
     const int num_kb = (p.K + BK - 1) / BK;
-    constexpr bool b_mn = (MODE == NS_APPLY);
     const int cid = (int)cluster_id(), ncl = (int)cluster_count();
 
     if (warp == 0 && lane == 0) {
@@ -663,8 +759,14 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
                 if (leader) mbar_expect_tx(fb_local, 2 * STAGE2_BYTES);
                 const uint32_t sa = smem_u32(smem_a + stage * A2_BYTES);
                 const uint32_t sb = smem_u32(smem_b + stage * B2_BYTES);
-                tma_load_3d_pair(sa, &tm_a, fb, kb * BK, row_a, g);
-                if (!b_mn) {
+                if (!p.a_mn) {
+                    tma_load_3d_pair(sa, &tm_a, fb, kb * BK, row_a, g);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BM / 64; ++c)
+                        tma_load_3d_pair(sa + c * (64 * BK * 2), &tm_a, fb, row_a + c * 64, kb * BK, g);
+                }
+                if (!p.b_mn) {
                     tma_load_3d_pair(sb, &tm_b, fb, kb * BK, row_b, g);
                 } else {
 #pragma unroll
@@ -684,7 +786,10 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ---------------- MMA issuer (even CTA only) ----------------
-        const uint32_t idesc = idesc_pair(b_mn);
+        const uint32_t idesc = idesc_pair(p.a_mn != 0, p.b_mn != 0);
+        const uint64_t a_desc0 = operand_desc(smem_u32(smem_a), 0, p.a_mn != 0);
+        const uint64_t b_desc0 = operand_desc(smem_u32(smem_b), 0, p.b_mn != 0);
+        const uint64_t a_step = operand_desc_step(p.a_mn != 0), b_step = operand_desc_step(p.b_mn != 0);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -697,14 +802,11 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem_a + stage * A2_BYTES);
-                const uint32_t sb = smem_u32(smem_b + stage * B2_BYTES);
+                const uint64_t ad = a_desc0 + (uint64_t)(stage * (A2_BYTES >> 4));
+                const uint64_t bd = b_desc0 + (uint64_t)(stage * (B2_BYTES >> 4));
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t ad = sdesc(sa + kk * 32, 16, 1024);
-                    const uint64_t bd = b_mn ? sdesc(sb + kk * 2048, 64 * BK * 2, 1024) : sdesc(sb + kk * 32, 16, 1024);
-                    mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_bf16_pair(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc, (kb | kk) ? 1u : 0u);
                 mma_commit_pair(empty0 + 8 * stage);
                 if (++stage == STAGES2) { stage = 0; phase ^= 1; }
             }
@@ -725,52 +827,18 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             const int g = t / p.tiles_per_mat;
             int mp, nj;
             pair_coords(p, t - g * p.tiles_per_mat, mp, nj);
-            const int i0 = mp * 2 * BM + (int)rank * BM + q * 32;
-            const int jb = nj * BN + h * (BN / 2);
-            const int nsl = max(0, min(BN / 64, (p.N - jb + 31) / 32));
-            float sc = 1.f;
-            if (MODE != NS_POLY && p.scale) sc = p.scale[g];
-            float4 xc[8], xn[8];
-            float ac[32], an[32];
-            if (nsl > 0) {
-                if (MODE == NS_APPLY) prefetch_x(p, g, i0, lane, jb, xc);
-                if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, jb, ac);
-            }
-            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag, p.status)) break;
-            tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + h * (BN / 2));
-            if (nsl == 0) {
-                __syncwarp();
-                if (lane == 0) remote_arrive(tempty_leader + 8 * acc);
-            }
-#pragma unroll
-            for (int k = 0; k < BN / 64; ++k) {
-                if (k < nsl) {
-                    const int j0 = jb + 32 * k;
-                    float v[32];
-                    tmem_ld32(trow + 32 * k, v);
-                    if (k == nsl - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) remote_arrive(tempty_leader + 8 * acc);
-                    }
-                    if (k + 1 < nsl) {
-                        if (MODE == NS_APPLY) prefetch_x(p, g, i0, lane, j0 + 32, xn);
-                        if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, j0 + 32, an);
-                    }
-                    if (MODE == NS_APPLY) {
-                        apply_slice(p, g, i0, lane, j0, v, st, xc, sc);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) xc[u] = xn[u];
-                    } else {
-                        sym_slice<MODE>(p, g, i0, lane, j0, v, st, ac, sc);
-                        if (MODE == NS_POLY) {
-#pragma unroll
-                            for (int u = 0; u < 32; ++u) ac[u] = an[u];
-                        }
-                    }
-                }
-            }
+            const uint32_t te = tempty_leader + 8 * acc;
+            double* slot = (VAR & NS_OUT_U)
+                               ? p.upart + ((size_t)t * 2 + rank) * (kUPartsPerTilePair / 2) + e
+                               : nullptr;
+            if (!epilogue_tile<MODE, VAR>(p, g, mp * 2 * BM + (int)rank * BM + q * 32, nj * BN + h * (BN / 2),
+                                          tfull0 + 8 * acc, acc_phase, trow, st, lane, abort_flag, slot,
+                                          [&]() {
+                                              __syncwarp();
+                                              if (lane == 0) remote_arrive(te);
+                                          }))
+                break;
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
     }
@@ -845,10 +913,10 @@ int pair_tiles_per_matrix(int mode, int M, int N) {
     return cnt;
 }
 
-template <int MODE>
+template <int MODE, int VAR>
 static int max_pair_clusters() {
-    static int cached[3] = {0, 0, 0};
-    if (cached[MODE]) return cached[MODE];
+    static int cached = 0;
+    if (cached) return cached;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 148, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
@@ -861,85 +929,96 @@ static int max_pair_clusters() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair::ns_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, pair::ns_gemm_pair_kernel<MODE, VAR>, &cfg) != cudaSuccess || n <= 0) {
         (void)cudaGetLastError();
         n = sm_count() / 2;
     }
-    cached[MODE] = n;
+    cached = n;
     return n;
 }
 
-template <int MODE>
+template <int MODE, int VAR>
 static cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, long long total,
                                cudaStream_t st) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(pair::ns_gemm_pair_kernel<MODE>,
+        cudaError_t e = cudaFuncSetAttribute(pair::ns_gemm_pair_kernel<MODE, VAR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM2_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const long long clusters = total < max_pair_clusters<MODE>() ? total : max_pair_clusters<MODE>();
-    pair::ns_gemm_pair_kernel<MODE><<<(int)(2 * clusters), NUM_THREADS, pair::SMEM2_BYTES, st>>>(ta, tb, p);
+    const int maxc = max_pair_clusters<MODE, VAR>();
+    const long long clusters = total < maxc ? total : maxc;
+    pair::ns_gemm_pair_kernel<MODE, VAR><<<(int)(2 * clusters), NUM_THREADS, pair::SMEM2_BYTES, st>>>(ta, tb, p);
     return cudaGetLastError();
 }
 
-// Operand tensors: GRAM A = B = X_op [G][s][ld_x] (K = l);
-// POLY A = B = A_op [G][s][ld_s] (K = s);  APPLY A = B_op [G][s][ld_s],
-// B = X_op (MN-major: rows = k).  `pair` selects the 2-SM kernel.
-cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld, bool pair,
-                           cudaStream_t st, const char** why) {
-    if (pair) {
-        CUtensorMap ta, tb;
-        if (!encode_bf16_3d(&ta, a_op, p.K, p.M, p.G, a_ld, BM)) { *why = "cuTensorMapEncodeTiled (A) failed"; return cudaErrorInvalidValue; }
-        const bool okb = (p.mode == NS_APPLY) ? encode_bf16_3d(&tb, b_op, p.N, p.K, p.G, b_ld, 64)
-                                              : encode_bf16_3d(&tb, b_op, p.K, p.N, p.G, b_ld, BN / 2);
-        if (!okb) { *why = "cuTensorMapEncodeTiled (B) failed"; return cudaErrorInvalidValue; }
-        p.tiles_m = (p.M + 2 * BM - 1) / (2 * BM);
-        p.tiles_n = (p.N + BN - 1) / BN;
-        p.tiles_per_mat = pair_tiles_per_matrix(p.mode, p.M, p.N);
-        const long long total = (long long)p.G * p.tiles_per_mat;
-        if (total <= 0) return cudaSuccess;
-        cudaError_t e;
-        if (p.mode == NS_GRAM) e = launch_pair<NS_GRAM>(ta, tb, p, total, st);
-        else if (p.mode == NS_POLY) e = launch_pair<NS_POLY>(ta, tb, p, total, st);
-        else e = launch_pair<NS_APPLY>(ta, tb, p, total, st);
-        if (e != cudaSuccess) *why = "2-SM GEMM launch failed";
-        return e;
-    }
-    CUtensorMap ta, tb;
-    // A operand: rows = M, cols = K
-    if (!encode_bf16_3d(&ta, a_op, p.K, p.M, p.G, a_ld, BM)) { *why = "cuTensorMapEncodeTiled (A) failed"; return cudaErrorInvalidValue; }
-    bool okb;
-    if (p.mode == NS_APPLY)  // B operand X_op: rows = K (= s), cols = N (= l), box 64 x 64
-        okb = encode_bf16_3d(&tb, b_op, p.N, p.K, p.G, b_ld, 64);
-    else                     // B operand: rows = N, cols = K
-        okb = encode_bf16_3d(&tb, b_op, p.K, p.N, p.G, b_ld, BN);
-    if (!okb) { *why = "cuTensorMapEncodeTiled (B) failed"; return cudaErrorInvalidValue; }
-    p.tiles_m = (p.M + BM - 1) / BM;
-    p.tiles_n = (p.N + BN - 1) / BN;
-    p.tiles_per_mat = tiles_per_matrix(p.mode, p.M, p.N);
-    const long long total = (long long)p.G * p.tiles_per_mat;
-    if (total <= 0) return cudaSuccess;
+template <int MODE, int VAR>
+static cudaError_t launch_single(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, long long total,
+                                 cudaStream_t st) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<NS_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(ns_gemm_kernel<MODE, VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ns_gemm_kernel<NS_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(ns_gemm_kernel<NS_APPLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) { *why = "cudaFuncSetAttribute failed"; return e; }
+        if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int grid = (int)(total < sm_count() ? total : sm_count());
-    if (p.mode == NS_GRAM)
-        ns_gemm_kernel<NS_GRAM><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
-    else if (p.mode == NS_POLY)
-        ns_gemm_kernel<NS_POLY><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
-    else
-        ns_gemm_kernel<NS_APPLY><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+    ns_gemm_kernel<MODE, VAR><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
     return cudaGetLastError();
+}
+
+template <bool PAIR>
+static cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, long long total,
+                            cudaStream_t st) {
+#define MUONH_LAUNCH(M_, V_) (PAIR ? launch_pair<M_, V_>(ta, tb, p, total, st) : launch_single<M_, V_>(ta, tb, p, total, st))
+    if (p.mode == NS_GRAM) return MUONH_LAUNCH(NS_GRAM, 0);
+    if (p.mode == NS_POLY) return MUONH_LAUNCH(NS_POLY, 0);
+    switch (p.variant) {
+        case 0: return MUONH_LAUNCH(NS_APPLY, 0);
+        case NS_IN_SRC: return MUONH_LAUNCH(NS_APPLY, NS_IN_SRC);
+        case NS_OUT_U: return MUONH_LAUNCH(NS_APPLY, NS_OUT_U);
+        case NS_IN_SRC | NS_OUT_U: return MUONH_LAUNCH(NS_APPLY, NS_IN_SRC | NS_OUT_U);
+        default: return cudaErrorInvalidValue;
+    }
+#undef MUONH_LAUNCH
+}
+
+// Operand tensors ([G][rows][ld] bf16, ld = a_ld / b_ld):
+//   K-major operand:  rows = M (or N), cols = K; box 64 x 128 (or 256, or 128
+//                     per CTA for B in the pair kernel)
+//   MN-major operand: rows = K, cols = M (or N); box 64 x 64
+// GRAM wide: A = B = X_op (K-major);  GRAM tall: A = B = X_op (MN-major);
+// POLY: A = B = A_op (K-major);  APPLY wide: A = B_op (K-major), B = X_op
+// (MN-major);  APPLY tall: A = X_op, B = B_op (both K-major).
+// `pair` selects the 2-SM kernel.
+cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld, bool pair,
+                           cudaStream_t st, const char** why) {
+    if (p.mode != NS_APPLY) p.variant = 0;
+    if (p.variant != 0 && !p.io) { *why = "apply variant without per-matrix buffers"; return cudaErrorInvalidValue; }
+    if ((p.variant & NS_OUT_U) && !p.upart) { *why = "apply variant without partial buffer"; return cudaErrorInvalidValue; }
+    if (p.variant != 0 && (p.N & 3) != 0) { *why = "apply variant needs a row length that is a multiple of 4"; return cudaErrorInvalidValue; }
+    CUtensorMap ta, tb;
+    const bool oka = p.a_mn ? encode_bf16_3d(&ta, a_op, p.M, p.K, p.G, a_ld, 64)
+                            : encode_bf16_3d(&ta, a_op, p.K, p.M, p.G, a_ld, BM);
+    if (!oka) { *why = "cuTensorMapEncodeTiled (A) failed"; return cudaErrorInvalidValue; }
+    const bool okb = p.b_mn ? encode_bf16_3d(&tb, b_op, p.N, p.K, p.G, b_ld, 64)
+                            : encode_bf16_3d(&tb, b_op, p.K, p.N, p.G, b_ld, pair ? BN / 2 : BN);
+    if (!okb) { *why = "cuTensorMapEncodeTiled (B) failed"; return cudaErrorInvalidValue; }
+    if (pair) {
+        p.tiles_m = (p.M + 2 * BM - 1) / (2 * BM);
+        p.tiles_n = (p.N + BN - 1) / BN;
+        p.tiles_per_mat = pair_tiles_per_matrix(p.mode, p.M, p.N);
+    } else {
+        p.tiles_m = (p.M + BM - 1) / BM;
+        p.tiles_n = (p.N + BN - 1) / BN;
+        p.tiles_per_mat = tiles_per_matrix(p.mode, p.M, p.N);
+    }
+    const long long total = (long long)p.G * p.tiles_per_mat;
+    if (total <= 0) return cudaSuccess;
+    cudaError_t e = pair ? dispatch<true>(ta, tb, p, total, st) : dispatch<false>(ta, tb, p, total, st);
+    if (e != cudaSuccess) *why = pair ? "2-SM GEMM launch failed" : "GEMM launch failed";
+    return e;
 }
 
 }  // namespace tc

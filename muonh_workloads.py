@@ -120,13 +120,17 @@ def qwen3_layer() -> Workload:
     return Workload("qwen3_layer_d2048", list(LAYER_SHAPES), labels=list(LAYER_LABELS))
 
 
-def qwen3_2b(steps: int = 10) -> Workload:
-    """28 layers of decoder matrices: 196 matrices, 1.409 G parameters."""
+def qwen3_2b(steps: int = 10, layers: int = N_LAYERS) -> Workload:
+    """28 layers of decoder matrices: 196 matrices, 1.409 G parameters.
+
+    `layers` < 28 gives the first layers of the same set (same seeds), a
+    smaller case with the same bucket shapes for profiling."""
     shapes, labels = [], []
-    for layer in range(N_LAYERS):
+    for layer in range(layers):
         shapes += LAYER_SHAPES
         labels += [f"{layer}.{n}" for n in LAYER_LABELS]
-    return Workload("qwen3_2b_28layers", shapes, steps=steps, labels=labels)
+    name = "qwen3_2b_28layers" if layers == N_LAYERS else f"qwen3_2b_first{layers}layers"
+    return Workload(name, shapes, steps=steps, labels=labels)
 
 
 def batched_256(count: int = 1024) -> Workload:

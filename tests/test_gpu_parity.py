@@ -169,6 +169,18 @@ def test_step_ragged_shapes_three_steps(mode):
     _check_step(work, w0, r0, hist, fp32_check)
 
 
+@pytest.mark.parametrize("mode", ["pair", "1sm"])
+@pytest.mark.parametrize("ns_steps", [0, 1, 2])
+def test_step_short_iteration_counts(ns_steps, mode):
+    # one iteration: the same apply launch reads X from the momentum and
+    # writes U = W - lr*O; zero iterations: O is the normalised momentum
+    work = wl.ragged([(300, 200), (200, 300), (13, 37), (37, 13), (77, 77), (520, 129), (8, 1)])
+    work.ns_steps = ns_steps
+    w0, r0, hist, status = _run_steps(work, 2, False, flags=MODES[mode])
+    assert status == 0
+    _check_step(work, w0, r0, hist, False)
+
+
 @pytest.mark.parametrize("mode", list(MODES))
 def test_step_qwen3_layer(mode):
     fp32_check = mode == "fp32"
