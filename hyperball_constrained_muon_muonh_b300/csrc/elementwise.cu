@@ -1,16 +1,18 @@
 // HBM-bound kernels of the MuonH step: momentum (+ ||M||^2 + the Newton-
-// Schulz input X), the hyperball retraction (||W - lr*O||^2, then the
-// rescale), and the initial-norm capture.
+// Schulz input X), the hyperball retraction (||W - lr*O||^2 where the last
+// apply GEMM has not already summed it, then the rescale), and the
+// initial-norm capture.
 //
 // Method: Puro-2B digest (jacksunwei.me), section "The load-bearing tricks
 // aren't in the abstract" -- Muon momentum orthogonalised by Newton-Schulz,
 // and every weight matrix held at its initial Frobenius norm.  Model card
 // (axforge.ai), section "Training": fp32 master weights and optimizer state.
 //
-// Work split: a chunk is a band of rows of one matrix (64-row bands for
-// tall matrices, whose X is the transpose).  Each CTA takes one chunk and
-// writes one fp64 partial sum; a one-thread-per-matrix finalize kernel adds
-// a matrix's partials in index order, so every norm is deterministic.
+// Work split: a chunk is a band of about 64 K elements (whole rows) of one
+// matrix; every buffer keeps the matrix's own orientation, so each kernel
+// streams row-major.  Each CTA takes one chunk and writes one fp64 partial
+// sum; a one-warp-per-matrix finalize kernel adds a matrix's partials in a
+// fixed order, so every norm is deterministic.
 
 #include <cooperative_groups.h>
 

@@ -13,17 +13,20 @@
  * with gradient G and momentum M (fp32, same shape) and radius r0:
  *
  *   M  <- beta*M + G                               (heavy-ball momentum)
- *   X  <- M / (||M||_F + eps), transposed when rows > cols (so X is s x l,
- *         s = min(rows, cols) <= l = max(rows, cols))
- *   ns_steps times:  A = X X^T;  B = b*A + c*A A;  X <- a*X + B X
- *         with (a, b, c) = ns_coeffs
- *   O  <- X, transposed back
+ *   X  <- M / (||M||_F + eps)
+ *   ns_steps times, with (a, b, c) = ns_coeffs:
+ *       rows <= cols:  A = X X^T;  B = b*A + c*A A;  X <- a*X + B X
+ *       rows >  cols:  A = X^T X;  B = b*A + c*A A;  X <- a*X + X B
+ *     (the second form is the first applied to X^T and transposed back; A
+ *     is always s x s, s = min(rows, cols))
+ *   O  <- X
  *   U  <- W - lr*O;   W <- r0 * U / ||U||_F;   W_bf16 <- bf16(W)  (RNE)
  *
  * The pages leave open the momentum form, the Newton-Schulz coefficients and
- * step count, eps, the transpose rule and any update scaling; here they are
- * explicit arguments (momentum form and transpose rule as above, update
- * scale 1, no weight decay).
+ * step count, eps, which side of a non-square matrix the iteration works on,
+ * and any update scaling; here they are explicit arguments or fixed as above
+ * (heavy-ball momentum, the Gram on the short side, update scale 1, no
+ * weight decay).
  *
  * Conventions for every entry point:
  *  - Device pointers are CUDA device (or managed) addresses on the current
