@@ -310,7 +310,7 @@ def main():
         "ns_share_of_step": ns_ms / max(ms_total, 1e-9),
     }
     hbm = {}
-    for k in ("momentum", "hyperball_norm", "hyperball_apply"):
+    for k in ("momentum", "hyperball_norm", "hyperball_apply", "hyperball_scale"):
         if k in prof and prof[k]["ms"] > 0:
             gbs = prof[k]["bytes"] / (prof[k]["ms"] / 1000.0) / 1e9
             hbm[k] = {"GB/s": gbs, "frac": gbs / peaks["hbm_gbs"], "ms_per_step": prof[k]["ms"] / args.steps}
