@@ -13,8 +13,9 @@ Reported beside it:
                 aware algorithmic TFLOP/s from CUDA events recorded by the
                 library around each launch, against the measured sustained
                 bf16 peak
-  cpu_baseline  the float64 oracle on this host, on one decoder layer's
-                matrices (1/28 of a step), scaled to steps/s of the full set
+  cpu_baseline  the float64 oracle on this host, on one matrix of each shape
+                (three steps), scaled to steps/s of the full set by the
+                sample's share of the Newton-Schulz flops
   e2e           steps/s with gradients copied in from pinned host memory and
                 the status word read back every step
   clocks        nvidia-smi samples taken during the timed region
@@ -127,46 +128,59 @@ def _ns_traffic_from_profiles():
         return None
 
 
-def oracle_sample(work, repeats=1):
-    """Time the oracle on one decoder layer's matrices (or a bounded subset)."""
-    import numpy as np
-    from oracle import muonh as om
+def _oracle_cores():
     try:
         from threadpoolctl import threadpool_info
-        cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
+        return max((i.get("num_threads", 1) for i in threadpool_info()), default=os.cpu_count())
     except Exception:  # threadpoolctl missing: report the host's logical cores
-        cores = os.cpu_count()
-    n_all = len(work.shapes)
-    if work.name.startswith("qwen3_2b"):
-        idx = list(range(7))            # one decoder layer: 1/28 of the step
-    elif work.name.startswith("batched"):
-        idx = list(range(64))
-    elif work.name.startswith("aspect"):
-        idx = [0, 4]
-    else:
-        idx = list(range(n_all))
+        return os.cpu_count()
+
+
+def _ns_flops(shapes):
+    return sum(3 * min(r, c) ** 2 * max(r, c) + min(r, c) ** 3 for r, c in shapes)
+
+
+def oracle_sample_indices(work):
+    """A bounded sample of the workload for the oracle: the first matrix of
+    every distinct shape (4 of the 2B set's 196 matrices), capped at 64."""
+    seen, idx = set(), []
+    for i, sh in enumerate(work.shapes):
+        if sh not in seen:
+            seen.add(sh)
+            idx.append(i)
+    return idx[:64]
+
+
+def oracle_sample(work, repeats=1, warmup=0):
+    """Time the float64 oracle on the sample; returns steps/s of the whole
+    workload (sample time scaled by the sample's share of the step's
+    Newton-Schulz flops), threads used and a description."""
+    import numpy as np
+    from oracle import muonh as om
+    idx = oracle_sample_indices(work)
     ws = [w.numpy() for w in work.weights("cpu", idx)]
     gs = [g.numpy() for g in work.grads(0, "cpu", idx)]
     ms = [np.zeros_like(w) for w in ws]
     r0 = om.capture_norms(ws)
+    for _ in range(warmup):
+        om.muonh_step(ws, gs, ms, r0, work.lr, work.beta, work.ns_steps, work.coeffs, work.eps)
     t0 = time.perf_counter()
     for _ in range(repeats):
         om.muonh_step(ws, gs, ms, r0, work.lr, work.beta, work.ns_steps, work.coeffs, work.eps)
-    dt = (time.perf_counter() - t0) / repeats
-    # scale by the workload's Newton-Schulz flops
-    def flops(shapes):
-        return sum(3 * min(r, c) ** 2 * max(r, c) + min(r, c) ** 3 for r, c in shapes)
-    frac = flops([work.shapes[i] for i in idx]) / flops(work.shapes)
-    steps_per_s = frac / dt
-    sample = f"oracle (NumPy float64) on {len(idx)} of {n_all} matrices, {repeats} step(s), {dt:.2f} s; " \
-             f"scaled by their share ({frac:.4f}) of the step's Newton-Schulz flops"
-    return steps_per_s, cores, sample
+    dt = (time.perf_counter() - t0) / max(repeats, 1)
+    frac = _ns_flops([work.shapes[i] for i in idx]) / _ns_flops(work.shapes)
+    sample = (f"oracle (NumPy float64) on {len(idx)} of {len(work.shapes)} matrices (one of each shape), "
+              f"{repeats} timed step(s) of {dt:.2f} s each; scaled by their share ({frac:.4f}) of the "
+              f"step's Newton-Schulz flops")
+    return frac / dt, _oracle_cores(), sample
 
 
 def run_reference(args, work, world, rank):
+    """The reference arm: the oracle, as it stands, on this host's cores;
+    W untimed and K timed steps, each on the bounded sample."""
     if rank != 0:
         return
-    v, cores, sample = oracle_sample(work)
+    v, cores, sample = oracle_sample(work, repeats=args.steps, warmup=args.warmup)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v, "higher_is_better": True,
@@ -211,7 +225,7 @@ def main():
     # the oracle's BLAS pool is started before any CUDA work
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_sample(work)
+        cpu = oracle_sample(work, repeats=3)
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
