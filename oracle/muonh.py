@@ -38,6 +38,18 @@ Readings where the pages are silent (each is an explicit argument here)
 
 Parity of ``muonh_step`` as a whole is pinned by invariants and closed forms
 only: the pages print no worked example.
+
+Neighbours of the MuonH step on the same pages
+----------------------------------------------
+* Muon, the baseline MuonH is compared with (Puro-2B paper part 6, section
+  4.3.1 "Cost-Saving Factors", the matched-ladder comparison), and "standard
+  weight decay" (digest footnote 3).  The pages give no formula; the reading
+  here is the same momentum and Newton-Schulz, then
+  ``W <- (1 - lr*wd)*W - lr*O`` (decoupled weight decay), ``wd`` an argument.
+* AdamW for the parameters outside the MuonH group, weight decay 0.1 (model
+  card, section "Training").  The pages give no other hyperparameter; the
+  oracle is the textbook decoupled-weight-decay Adam with bias correction,
+  ``beta1``, ``beta2``, ``eps`` and ``wd`` arguments.
 """
 
 from __future__ import annotations
@@ -152,3 +164,69 @@ def muonh_step(weights, grads, moms, r0, lr, beta, ns_steps, coeffs, eps,
         out["status"].append(status)
     return out
 
+
+
+def muon_update(w: np.ndarray, o: np.ndarray, lr: float, weight_decay: float) -> np.ndarray:
+    """Muon's weight update with decoupled weight decay (the reading above):
+    ``(1 - lr*wd) * W - lr * O`` in float64."""
+    return (1.0 - lr * weight_decay) * np.asarray(w, np.float64) - lr * np.asarray(o, np.float64)
+
+
+def muon_step(weights, grads, moms, lr, beta, weight_decay, ns_steps, coeffs, eps, state_dtype=np.float32):
+    """One plain Muon step over a list of matrices (the baseline of the
+    matched-ladder comparison): momentum and Newton-Schulz as in
+    ``muonh_step``, then ``muon_update``.  Same return dict as
+    ``muonh_step``; a matrix whose momentum is non-finite keeps its W."""
+    out = {"w": [], "w_bf16": [], "m": [], "o": [], "status": []}
+    for w, g, m in zip(weights, grads, moms):
+        m_new = momentum(m, g, beta)
+        if state_dtype is not None:
+            m_new = m_new.astype(state_dtype)
+        status = 0
+        if not np.all(np.isfinite(m_new)):
+            o = np.full(np.shape(w), np.nan)
+            w_new = np.array(w, dtype=np.float64)
+            status = STATUS_NONFINITE_INPUT
+        else:
+            o = newton_schulz(m_new, ns_steps, coeffs, eps)
+            w_new = muon_update(w, o, lr, weight_decay)
+        if state_dtype is not None:
+            w_new = w_new.astype(state_dtype)
+        out["w"].append(w_new)
+        out["w_bf16"].append(bf16_round(np.asarray(w_new, np.float32)))
+        out["m"].append(m_new)
+        out["o"].append(o)
+        out["status"].append(status)
+    return out
+
+
+def adamw_step(params, grads, exp_avgs, exp_avg_sqs, step, lr, beta1, beta2, eps, weight_decay,
+               state_dtype=np.float32):
+    """One AdamW step (decoupled weight decay, bias-corrected moments) over a
+    list of tensors of any shape, float64 arithmetic.  ``step`` is the
+    1-based index of this step.  For each tensor:
+
+        m <- beta1*m + (1 - beta1)*g
+        v <- beta2*v + (1 - beta2)*g^2
+        m_hat = m / (1 - beta1^step);   v_hat = v / (1 - beta2^step)
+        p <- (1 - lr*wd)*p - lr * m_hat / (sqrt(v_hat) + eps)
+
+    Returns a dict with ``p``, ``p_bf16``, ``m``, ``v`` (``state_dtype``
+    unless None)."""
+    out = {"p": [], "p_bf16": [], "m": [], "v": []}
+    bc1 = 1.0 - beta1 ** step
+    bc2 = 1.0 - beta2 ** step
+    for p, g, m, v in zip(params, grads, exp_avgs, exp_avg_sqs):
+        p64, g64 = np.asarray(p, np.float64), np.asarray(g, np.float64)
+        m_new = beta1 * np.asarray(m, np.float64) + (1.0 - beta1) * g64
+        v_new = beta2 * np.asarray(v, np.float64) + (1.0 - beta2) * g64 * g64
+        m_hat = m_new / bc1
+        v_hat = v_new / bc2
+        p_new = (1.0 - lr * weight_decay) * p64 - lr * m_hat / (np.sqrt(v_hat) + eps)
+        if state_dtype is not None:
+            p_new, m_new, v_new = (x.astype(state_dtype) for x in (p_new, m_new, v_new))
+        out["p"].append(p_new)
+        out["p_bf16"].append(bf16_round(np.asarray(p_new, np.float32)))
+        out["m"].append(m_new)
+        out["v"].append(v_new)
+    return out
