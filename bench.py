@@ -36,6 +36,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MuonH steps/s on a 2B param set (1 B300); NS GEMM % of bf16 tensor peak"
+METRIC_MUON = "Muon steps/s on a 2B param set (1 B300); NS GEMM % of bf16 tensor peak"
+MUON_WD = 0.1
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
@@ -204,6 +206,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--gemm-1sm", action="store_true", help="one-SM Newton-Schulz GEMM kernel")
+    ap.add_argument("--optimizer", default="muonh", choices=["muonh", "muon"],
+                    help="muon: plain Muon (decoupled weight decay 0.1, no hyperball), the baseline MuonH is "
+                         "compared with")
     args = ap.parse_args()
 
     import muonh_workloads as wl
@@ -235,8 +240,13 @@ def main():
 
     ws = work.weights(dev)
     grads = [work.grads(t, dev) for t in range(2)]   # two gradient sets, alternated
-    opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps, ns_coeffs=work.coeffs,
-                   eps=work.eps, bf16_copies=True, flags=mh.FLAG_GEMM_1SM if args.gemm_1sm else 0)
+    gemm_flags = mh.FLAG_GEMM_1SM if args.gemm_1sm else 0
+    if args.optimizer == "muon":
+        opt = mh.Muon(ws, lr=work.lr, beta=work.beta, weight_decay=MUON_WD, ns_steps=work.ns_steps,
+                      ns_coeffs=work.coeffs, eps=work.eps, bf16_copies=True, flags=gemm_flags)
+    else:
+        opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps, ns_coeffs=work.coeffs,
+                       eps=work.eps, bf16_copies=True, flags=gemm_flags)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -306,7 +316,8 @@ def main():
         return
 
     peaks = _peaks()
-    ns_kinds = ("ns_gram", "ns_poly", "ns_apply", "ns_apply_in", "ns_apply_out", "ns_apply_in_out")
+    ns_kinds = ("ns_gram", "ns_poly", "ns_apply", "ns_apply_in", "ns_apply_out", "ns_apply_in_out", "ns_apply_outw",
+                "ns_apply_in_outw")
     ns_ms = sum(prof[k]["ms"] for k in ns_kinds if k in prof)
     ns_flops = sum(prof[k]["flops"] for k in ns_kinds if k in prof)
     ns_launches = sum(prof[k]["launches"] for k in ns_kinds if k in prof)
@@ -324,12 +335,13 @@ def main():
         "ns_share_of_step": ns_ms / max(ms_total, 1e-9),
     }
     hbm = {}
-    for k in ("momentum", "hyperball_norm", "hyperball_apply", "hyperball_scale"):
+    for k in ("momentum", "hyperball_norm", "hyperball_apply", "hyperball_scale", "muon_finish"):
         if k in prof and prof[k]["ms"] > 0:
             gbs = prof[k]["bytes"] / (prof[k]["ms"] / 1000.0) / 1e9
             hbm[k] = {"GB/s": gbs, "frac": gbs / peaks["hbm_gbs"], "ms_per_step": prof[k]["ms"] / args.steps}
     line = {
-        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_MUON if args.optimizer == "muon" else METRIC, "value": value, "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": work.name, "matrices": len(work.shapes), "params": work.n_params,
@@ -337,7 +349,8 @@ def main():
                    "eps": work.eps, "state": "fp32 W/M/G + bf16 W copy; NS bf16 operands, fp32 state",
                    "l2": "inputs larger than L2 (about 20 GB of optimizer state touched per step)",
                    "parallelism": f"replica x{world}",
-                   "ns_gemm": "1-SM 128x256 tiles" if args.gemm_1sm else "2-SM pair 256x256 tiles"},
+                   "ns_gemm": "1-SM 128x256 tiles" if args.gemm_1sm else "2-SM pair 256x256 tiles",
+                   "optimizer": "muon (weight decay 0.1)" if args.optimizer == "muon" else "muonh"},
         "ns_tflops": achieved,
         "roofline": roofline,
         "hbm_kernels": hbm,

@@ -25,7 +25,7 @@ from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_SYNC_DEBUG, STATUS_DEGEN
 
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
 
-__all__ = ["MuonH", "capture_norms", "workspace_size", "step", "orthogonalize",
+__all__ = ["MuonH", "Muon", "capture_norms", "workspace_size", "step", "muon_step", "orthogonalize",
            "orthogonalize_workspace_size", "get_status", "profile_read", "MuonHError", "NS_COEFFS"]
 
 
@@ -94,6 +94,13 @@ def step(arr, r0, lr, beta, ns_steps, coeffs, eps, flags, workspace, stream=None
     check(lib.muonh_step(arr, len(arr), ctypes.c_void_p(r0.data_ptr()), lr, beta, ns_steps, c, eps, flags,
                          ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream)),
           "muonh_step")
+
+
+def muon_step(arr, lr, beta, weight_decay, ns_steps, coeffs, eps, flags, workspace, stream=None) -> None:
+    """One muon_step call (plain Muon, decoupled weight decay) on a prebuilt matrix array."""
+    c = (ctypes.c_float * 3)(*coeffs)
+    check(lib.muon_step(arr, len(arr), lr, beta, weight_decay, ns_steps, c, eps, flags,
+                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream)), "muon_step")
 
 
 def orthogonalize_workspace_size(rows: int, cols: int, flags: int = 0) -> int:
@@ -193,3 +200,33 @@ class MuonH:
         for m, src in zip(self.moms, sd["moms"]):
             m.copy_(src)
         self.r0.copy_(sd["r0"])
+
+
+class Muon:
+    """Plain Muon (the baseline MuonH is compared with) over a fixed list of
+    fp32 2-D CUDA weight matrices: momentum, Newton-Schulz, then
+    W <- (1 - lr*weight_decay)*W - lr*O.  Momenta start at zero."""
+
+    def __init__(self, weights, lr=0.02, beta=0.95, weight_decay=0.0, ns_steps=5, ns_coeffs=NS_COEFFS, eps=1e-7,
+                 bf16_copies=False, fp32_check=False, flags=0):
+        self.weights = list(weights)
+        self.lr, self.beta, self.weight_decay = float(lr), float(beta), float(weight_decay)
+        self.ns_steps, self.eps = int(ns_steps), float(eps)
+        self.ns_coeffs = tuple(float(v) for v in ns_coeffs)
+        self.flags = (FLAG_FP32_CHECK if fp32_check else 0) | int(flags)
+        self.moms = [torch.zeros_like(w) for w in self.weights]
+        self.bf16 = [torch.empty_like(w, dtype=torch.bfloat16) for w in self.weights] if bf16_copies else None
+        self._grads_ptrs = None
+        self._arr = None
+        self.workspace = torch.empty(workspace_size([tuple(w.shape) for w in self.weights], self.flags),
+                                     dtype=torch.uint8, device=self.weights[0].device)
+
+    def step(self, grads=None, stream=None) -> None:
+        if grads is None:
+            grads = [w.grad for w in self.weights]
+        ptrs = tuple(g.data_ptr() for g in grads)
+        if ptrs != self._grads_ptrs:
+            self._arr = matrix_array(self.weights, grads, self.moms, self.bf16)
+            self._grads_ptrs = ptrs
+        muon_step(self._arr, self.lr, self.beta, self.weight_decay, self.ns_steps, self.ns_coeffs, self.eps,
+                  self.flags, self.workspace, stream)

@@ -36,7 +36,7 @@ EXPORTS = (
     "muonh_orthogonalize_workspace_size", "muonh_orthogonalize", "muonh_get_status",
     "muonh_status_string", "muonh_last_error", "muonh_version",
     "muonh_profile_enable", "muonh_profile_read", "muonh_launch_count",
-    "muonh_orthogonalize_static",
+    "muonh_orthogonalize_static", "muon_step",
 )
 
 STATIC_SCRATCH_BYTES = 80 * 1024 * 1024
@@ -84,6 +84,7 @@ def _load():
     lib.muonh_capture_norms.argtypes = [mp, I, P, P]
     lib.muonh_workspace_size.argtypes = [mp, I, U32, ctypes.POINTER(SZ)]
     lib.muonh_step.argtypes = [mp, I, P, F, F, I, fp, F, U32, P, SZ, P]
+    lib.muon_step.argtypes = [mp, I, F, F, F, I, fp, F, U32, P, SZ, P]
     lib.muonh_orthogonalize_workspace_size.argtypes = [I64, I64, U32, ctypes.POINTER(SZ)]
     lib.muonh_orthogonalize.argtypes = [P, P, I64, I64, I, fp, F, U32, P, SZ, P]
     lib.muonh_orthogonalize_static.argtypes = [P, P, I64, I64, I, fp, F, U32, P]

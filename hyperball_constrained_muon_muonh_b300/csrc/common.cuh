@@ -33,7 +33,9 @@ struct MatDesc {
 //              itself, so the momentum kernel writes no fp32 copy of X
 //   kFusedOut  the last apply GEMM writes U = W - lr*O and the partials of
 //              ||U||^2 (part0, npart), so the hyperball step only rescales
-constexpr int kFusedIn = 1, kFusedOut = 2;
+//   kFusedOutW the last apply GEMM of a plain Muon step writes the new
+//              weight (1 - lr*wd)*W - lr*O and its bf16 copy itself
+constexpr int kFusedIn = 1, kFusedOut = 2, kFusedOutW = 4;
 static_assert(sizeof(MatDesc) == 80, "MatDesc layout");
 
 // Largest descriptor batch one launch carries in its parameter space
@@ -47,12 +49,16 @@ constexpr int kMaxDescPerLaunch = 396;
 //   src: the unscaled Newton-Schulz input (the momentum M, or the input of a
 //        standalone orthogonalisation), read by the first apply in place of
 //        an fp32 copy of X
-//   w:   the master weight, read by the last apply of a MuonH step
+//   w:   the master weight, read by the last apply of a MuonH step (and
+//        written by the last apply of a plain Muon step)
+//   wb:  the bf16 weight copy (or null), written by the last apply of a
+//        plain Muon step
 struct NsIO {
     const float* src;
-    const float* w;
+    float* w;
+    uint16_t* wb;
 };
-static_assert(sizeof(NsIO) == 16, "NsIO layout");
+static_assert(sizeof(NsIO) == 24, "NsIO layout");
 
 struct DescBatch {
     int n;                // matrices in this batch

@@ -123,6 +123,7 @@ momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restr
         NsIO r;
         r.src = D.m ? D.m : D.g;
         r.w = D.w;
+        r.wb = D.wb;
         io[b.first + mi] = r;
     }
     const int cr = chunk_rows_for(D.rows, cols);
@@ -169,8 +170,10 @@ __global__ void momentum_finalize(const __grid_constant__ DescBatch b, const dou
 //   HB_SCALE  W <- factor*U, W_bf16 = bf16(W), where X_state already holds U
 //             (written by the last apply GEMM, which also summed ||U||^2)
 // ---------------------------------------------------------------------------
-enum { HB_NORM = 0, HB_APPLY = 1, HB_SCALE = 2 };
+enum { HB_NORM = 0, HB_APPLY = 1, HB_SCALE = 2, HB_MUON = 3 };
 
+// HB_MUON is plain Muon's weight update on the same stream:
+// W <- f*W - lr*O (f = 1 - lr*weight_decay), W_bf16 = bf16(W).
 template <int HB>
 __device__ __forceinline__ void hyperball_chunk(const MatDesc& D, int r_begin, int r_end, float nlr, float f,
                                                 float& acc) {
@@ -183,14 +186,19 @@ __device__ __forceinline__ void hyperball_chunk(const MatDesc& D, int r_begin, i
         // U for four values (from W and O, or as read); write f*U or add ||U||^2
         auto visit4 = [&](float4 w, float4 o, size_t widx) {
             float4 u;
-            if (READ_W) {
+            if (HB == HB_MUON) {
+                u.x = fmaf(nlr, o.x, f * w.x); u.y = fmaf(nlr, o.y, f * w.y);
+                u.z = fmaf(nlr, o.z, f * w.z); u.w = fmaf(nlr, o.w, f * w.w);
+            } else if (READ_W) {
                 u.x = fmaf(nlr, o.x, w.x); u.y = fmaf(nlr, o.y, w.y);
                 u.z = fmaf(nlr, o.z, w.z); u.w = fmaf(nlr, o.w, w.w);
             } else {
                 u = o;
             }
-            if (WRITE) {
+            if (HB != HB_MUON && WRITE) {
                 u.x *= f; u.y *= f; u.z *= f; u.w *= f;
+            }
+            if (WRITE) {
                 *reinterpret_cast<float4*>(D.w + widx) = u;
                 if (D.wb) store_bf16x4(reinterpret_cast<__nv_bfloat16*>(D.wb) + widx, u);
             } else {
@@ -219,9 +227,9 @@ __device__ __forceinline__ void hyperball_chunk(const MatDesc& D, int r_begin, i
             const size_t r = r_begin + e / cols, c = e % cols;
             const size_t wi = r * cols + c;
             const float o = D.xs[r * ld + c];
-            const float u = READ_W ? fmaf(nlr, o, D.w[wi]) : o;
+            const float u = HB == HB_MUON ? fmaf(nlr, o, f * D.w[wi]) : (READ_W ? fmaf(nlr, o, D.w[wi]) : o);
             if (WRITE) {
-                const float y = u * f;
+                const float y = HB == HB_MUON ? u : u * f;
                 D.w[wi] = y;
                 if (D.wb) D.wb[wi] = bf16_bits(y);
             } else {
@@ -274,6 +282,25 @@ hyperball_finish_kernel(const __grid_constant__ DescBatch b, float lr, const flo
         const float nlr = o_scale ? -lr * o_scale[p] : -lr;
         hyperball_chunk<HB_APPLY>(D, r_begin, r_end, nlr, factor[p], unused);
     }
+}
+
+// Plain Muon's weight update for the matrices whose last apply GEMM did not
+// write it (no kFusedOutW): W <- (1 - lr*wd)*W - lr*O, W_bf16 = bf16(W).
+// Matrices with a status bit keep W.
+__global__ void __launch_bounds__(kThreads)
+muon_finish_kernel(const __grid_constant__ DescBatch b, float lr, float wdecay, const uint32_t* __restrict__ flags,
+                   const float* __restrict__ o_scale) {
+    const int chunk = b.chunk_begin + blockIdx.x;
+    const int mi = find_matrix(b, chunk);
+    const MatDesc& D = b.d[mi];
+    const int p = b.first + mi;
+    if ((D.fused & kFusedOutW) || flags[p] != 0) return;
+    const int cr = chunk_rows_for(D.rows, D.cols);
+    const int r_begin = (chunk - D.chunk0) * cr;
+    const int r_end = min(D.rows, r_begin + cr);
+    const float nlr = o_scale ? -lr * o_scale[p] : -lr;
+    float unused = 0.f;
+    hyperball_chunk<HB_MUON>(D, r_begin, r_end, nlr, wdecay, unused);
 }
 
 // Standalone orthogonalisation output: out (D.w) = o_scale * X_state.
@@ -402,6 +429,14 @@ cudaError_t launch_hyperball_finish(const DescBatch& b, float lr, const Scalars&
     const int nblk = b.chunk_end - b.chunk_begin;
     if (nblk <= 0) return cudaSuccess;
     hyperball_finish_kernel<<<nblk, kThreads, 0, st>>>(b, lr, sc.factor, sc.flags, o_scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_muon_finish(const DescBatch& b, float lr, float wdecay, const Scalars& sc, const float* o_scale,
+                               cudaStream_t st) {
+    const int nblk = b.chunk_end - b.chunk_begin;
+    if (nblk <= 0) return cudaSuccess;
+    muon_finish_kernel<<<nblk, kThreads, 0, st>>>(b, lr, wdecay, sc.flags, o_scale);
     return cudaGetLastError();
 }
 

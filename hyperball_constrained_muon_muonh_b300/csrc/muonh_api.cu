@@ -37,6 +37,8 @@ cudaError_t launch_hyperball_finalize(const DescBatch& b, const double* partials
                                       const Scalars& sc, const float* r0, cudaStream_t st);
 cudaError_t launch_hyperball_finish(const DescBatch& b, float lr, const Scalars& sc, const float* o_scale,
                                     cudaStream_t st);
+cudaError_t launch_muon_finish(const DescBatch& b, float lr, float wdecay, const Scalars& sc, const float* o_scale,
+                               cudaStream_t st);
 cudaError_t launch_emit(const DescBatch& b, const float* o_scale, cudaStream_t st);
 cudaError_t launch_capture_norms(const DescBatch& b, float* r0, cudaStream_t st);
 cudaError_t status_word(uint32_t** ptr);
@@ -59,13 +61,28 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ---- tracing: per-kernel CUDA-event timing ---------------------------------
 // ns_apply_in / _out / _in_out: the apply launches that read X from the
-// matrices' own input, write U = W - lr*O, or both (first / last iteration)
-enum Kind { K_MOMENTUM, K_MOM_FIN, K_GRAM, K_POLY, K_APPLY, K_APPLY_IN, K_APPLY_OUT, K_APPLY_IN_OUT, K_HB_NORM,
-            K_HB_FIN, K_HB_APPLY, K_HB_SCALE, K_EMIT, K_CAPTURE, K_SIMT_GRAM, K_SIMT_POLY, K_SIMT_APPLY, K_COUNT };
+// matrices' own input, write U = W - lr*O, or both (first / last iteration);
+// ns_apply_outw / _in_outw: the last apply of a plain Muon step, which writes
+// the new weight
+enum Kind { K_MOMENTUM, K_MOM_FIN, K_GRAM, K_POLY, K_APPLY, K_APPLY_IN, K_APPLY_OUT, K_APPLY_IN_OUT,
+            K_APPLY_OUTW, K_APPLY_IN_OUTW, K_HB_NORM, K_HB_FIN, K_HB_APPLY, K_HB_SCALE, K_MUON_FIN, K_EMIT,
+            K_CAPTURE, K_SIMT_GRAM, K_SIMT_POLY, K_SIMT_APPLY, K_ADAMW, K_COUNT };
 const char* const kKindName[K_COUNT] = {"momentum", "momentum_finalize", "ns_gram", "ns_poly", "ns_apply",
-                                        "ns_apply_in", "ns_apply_out", "ns_apply_in_out", "hyperball_norm",
-                                        "hyperball_finalize", "hyperball_apply", "hyperball_scale", "emit",
-                                        "capture_norms", "fp32_gram", "fp32_poly", "fp32_apply"};
+                                        "ns_apply_in", "ns_apply_out", "ns_apply_in_out", "ns_apply_outw",
+                                        "ns_apply_in_outw", "hyperball_norm", "hyperball_finalize",
+                                        "hyperball_apply", "hyperball_scale", "muon_finish", "emit",
+                                        "capture_norms", "fp32_gram", "fp32_poly", "fp32_apply", "adamw"};
+
+int apply_kind(int variant) {
+    switch (variant) {
+        case NS_IN_SRC: return K_APPLY_IN;
+        case NS_OUT_U: return K_APPLY_OUT;
+        case NS_IN_SRC | NS_OUT_U: return K_APPLY_IN_OUT;
+        case NS_OUT_W: return K_APPLY_OUTW;
+        case NS_IN_SRC | NS_OUT_W: return K_APPLY_IN_OUTW;
+        default: return K_APPLY;
+    }
+}
 
 std::atomic<long long> g_launches{0};
 
@@ -120,11 +137,20 @@ struct Trace {
 };
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Matrices whose short side is at most this run Newton-Schulz on fp32 CUDA
+// cores.  Their s x s Gram is smaller than one tensor-core tile, so the
+// tensor cores gain nothing, and with only a few singular values the bf16
+// rounding of B (|B| ~ 2.7 against a result ~0.7 per step) is not averaged
+// out: rank-1 inputs lose several percent in bf16, none in fp32.
+constexpr int kSmallSide = 32;
+
 struct Bucket {
     int R, C;             // matrix shape (rows, cols)
     int s, l, G;          // short side, long side, matrices
     bool tall;            // R > C
-    bool fusable;         // C % 4 == 0: the apply GEMM can read and write the matrices' own buffers
+    bool small;           // s <= kSmallSide: Newton-Schulz on fp32 CUDA cores
+    bool fusable;         // tensor-core bucket with C % 4 == 0: the apply GEMM can read and write the
+                          // matrices' own buffers
     int first;            // bucket-order index of its first matrix
     int ld_x, ld_s;
     size_t off_xs, off_xo;                    // byte offsets in the workspace
@@ -231,7 +257,8 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
             B.s = S.s;
             B.l = std::max(B.R, B.C);
             B.tall = B.R > B.C;
-            B.fusable = (B.C & 3) == 0;
+            B.small = B.s <= kSmallSide;
+            B.fusable = !B.small && (B.C & 3) == 0;
             B.G = (int)sh.idx.size();
             B.first = (int)P.order.size();
             B.ld_x = (int)align_up(B.C, 8);
@@ -326,16 +353,22 @@ Scalars scalars_of(const Plan& P, uint8_t* ws) {
 //   in   the first apply reads X from each matrix's own input (the
 //        momentum kernel writes the NsIO table and no fp32 copy of X)
 //   out  the last apply writes U = W - lr*O and its ||U||^2 partials
+//   out_w the last apply writes Muon's new weight (1 - lr*wd)*W - lr*O
 //   pair the partials' layout is the pair kernel's (else the 1-SM kernel's)
 struct NsFuse {
     bool in = false;
     bool out = false;
+    bool out_w = false;   // plain Muon: the last apply writes the new weight
     bool pair = true;
+    bool check = false;   // fp32 check mode: every bucket on CUDA cores
     float lr = 0.f;
+    float wdecay = 1.f;   // out_w: 1 - lr*weight_decay
 };
 
-// Descriptor batches in bucket order.  `x_in_alt` points the hyperball /
-// emit view of X at the second fp32 buffer (fp32 check mode, odd step count).
+// Descriptor batches in bucket order.  With `x_in_alt`, the hyperball /
+// emit view of X of every bucket that ran Newton-Schulz on CUDA cores (all
+// of them in the fp32 check mode, else the small ones) points at the second
+// fp32 buffer, where an odd number of those iterations leaves the result.
 std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, uint8_t* ws, bool x_in_alt,
                                     bool with_momentum, const NsFuse& fuse = NsFuse()) {
     std::vector<DescBatch> out;
@@ -358,7 +391,7 @@ std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, u
             const size_t xoff = (size_t)P.slot[p] * bk.R * bk.ld_x;
             float* xs = reinterpret_cast<float*>(ws + bk.off_xs);
             float* x2 = reinterpret_cast<float*>(ws + bk.off_xo);
-            D.xs = (x_in_alt ? x2 : xs) + xoff;
+            D.xs = ((x_in_alt && (fuse.check || bk.small)) ? x2 : xs) + xoff;
             D.xo = reinterpret_cast<__nv_bfloat16*>(ws + bk.off_xo) + xoff;
             D.rows = (int)m.rows;
             D.cols = (int)m.cols;
@@ -370,6 +403,7 @@ std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, u
             D.fused = 0;
             if (bk.fusable) {
                 if (fuse.in) D.fused |= kFusedIn;
+                if (fuse.out_w) D.fused |= kFusedOutW;
                 if (fuse.out) {
                     const int per = fuse.pair ? bk.tiles2 * tc::kUPartsPerTilePair : bk.tiles1 * tc::kUPartsPerTile1;
                     D.fused |= kFusedOut;
@@ -405,8 +439,8 @@ struct Sync {
 
 // Newton-Schulz over every bucket: per iteration and s-group, the Gram of
 // each bucket, one polynomial launch for the group, the apply of each bucket.
-// Returns MUONH_OK or an error code; *x_in_alt tells where the fp32 result
-// sits (check mode).
+// Returns MUONH_OK or an error code; *x_in_alt tells whether the buckets
+// that ran on CUDA cores left their result in the second fp32 buffer.
 int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_steps, const float* coeffs,
                       uint32_t flags, uint32_t* status, Sync& sy, bool* x_in_alt, const NsFuse& fuse) {
     const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
@@ -540,17 +574,24 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         a.scale = it == 0 ? sc.inv_nu + B.first : nullptr;
         a.ca = coeffs[0];
         a.status = status;
-        if (B.fusable)
-            a.variant = (fuse.in && it == 0 ? NS_IN_SRC : 0) | (fuse.out && it + 1 == ns_steps ? NS_OUT_U : 0);
+        if (B.fusable) {
+            const bool last = it + 1 == ns_steps;
+            a.variant = (fuse.in && it == 0 ? NS_IN_SRC : 0) | (fuse.out && last ? NS_OUT_U : 0) |
+                        (fuse.out_w && last ? NS_OUT_W : 0);
+        }
         a.io = reinterpret_cast<const NsIO*>(ws + P.off_io) + B.first;
         a.upart = reinterpret_cast<double*>(ws + P.off_upart) + B.upart0;
+        a.mflags = sc.flags + B.first;
         a.nlr = -fuse.lr;
+        a.wdecay = fuse.wdecay;
         const double G = B.G, S = B.s, L = B.l;
         cudaError_t e;
         {
-            // bytes: B_op, X read and written (fp32), X_op written unless last, W read when fused
-            const double per_el = 8.0 + (a.x_op_out ? 2.0 : 0.0) + ((a.variant & NS_OUT_U) ? 4.0 : 0.0);
-            Trace tr(K_APPLY + a.variant, sy.st);
+            // bytes: B_op, X read and written (fp32), X_op written unless last, W read when fused;
+            // NS_OUT_W writes the weight (fp32 and bf16) in place of X
+            double per_el = 8.0 + (a.x_op_out ? 2.0 : 0.0) + ((a.variant & NS_OUT_U) ? 4.0 : 0.0);
+            if (a.variant & NS_OUT_W) per_el = 4.0 + 4.0 + 4.0 + 2.0;
+            Trace tr(apply_kind(a.variant), sy.st);
             e = tr.done(B.tall ? tc::launch_ns_gemm(a, xc, B.ld_x, bop, B.ld_s, pair, sy.st, &why)
                                : tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, pair, sy.st, &why),
                         2 * G * S * S * L, G * S * S * 2 + G * S * L * per_el);
@@ -560,19 +601,21 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
 
     for (int it = 0; it < ns_steps; ++it) {
         for (const SGroup& Q : P.sgroups) {
+            // every bucket of an s-group has the same s, so the same path
+            const bool simt = check || Q.s <= kSmallSide;
             for (int b = Q.b_begin; b < Q.b_end; ++b) {
-                const int r = check ? simt_gram(P.buckets[b], it) : tc_gram(P.buckets[b], it);
+                const int r = simt ? simt_gram(P.buckets[b], it) : tc_gram(P.buckets[b], it);
                 if (r) return r;
             }
-            int r = check ? simt_poly(Q) : tc_poly(Q);
+            int r = simt ? simt_poly(Q) : tc_poly(Q);
             if (r) return r;
             for (int b = Q.b_begin; b < Q.b_end; ++b) {
-                r = check ? simt_apply(P.buckets[b], it) : tc_apply(P.buckets[b], it);
+                r = simt ? simt_apply(P.buckets[b], it) : tc_apply(P.buckets[b], it);
                 if (r) return r;
             }
         }
     }
-    if (check) *x_in_alt = (ns_steps & 1) != 0;
+    *x_in_alt = (ns_steps & 1) != 0;
     return MUONH_OK;
 }
 
@@ -701,6 +744,7 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     NsFuse fuse;
     fuse.in = fuse.out = !check && ns_steps >= 1;
     fuse.pair = (flags & MUONH_FLAG_GEMM_1SM) == 0;
+    fuse.check = check;
     fuse.lr = lr;
     if (fuse.out && P.n_upart > INT32_MAX)
         return fail(MUONH_ERR_UNSUPPORTED, "too many matrices/tiles for one step: split the list");
@@ -731,7 +775,7 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     bool x_alt = false;
     r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
     if (r) return r;
-    if (x_alt) batches = make_batches(P, mats, ws, true, true);
+    if (x_alt) batches = make_batches(P, mats, ws, true, true, fuse);
     const float* o_scale = ns_steps == 0 ? sc.inv_nu : nullptr;
     for (const DescBatch& B : batches) {
         const double e_sep = elems(B, kFusedOut, false), e_fused = elems(B, kFusedOut, true);
@@ -752,6 +796,79 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
             r = sy.check(tr.done(launch_hyperball_finish(B, lr, sc, o_scale, st), 0, e_sep * 14 + e_fused * 10),
                          "hyperball finish launch");
         }
+        if (r) return r;
+    }
+    return MUONH_OK;
+}
+
+int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float weight_decay, int ns_steps,
+              const float ns_coeffs[3], float eps, uint32_t flags, void* workspace, size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    std::vector<int64_t> rc;
+    int r = check_shapes(mats, n, rc, true);
+    if (r) return r;
+    if (!std::isfinite(lr) || !std::isfinite(beta) || !std::isfinite(weight_decay))
+        return fail(MUONH_ERR_INVALID_ARG, "lr, beta and weight_decay must be finite");
+    r = check_scalars(ns_steps, ns_coeffs, eps, flags);
+    if (r) return r;
+    const Plan& P = get_plan(rc.data(), n, flags);
+    r = check_workspace(workspace, ws_bytes, P.bytes);
+    if (r) return r;
+    uint32_t* status = nullptr;
+    r = get_status_ptr(&status);
+    if (r) return r;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Sync sy{(flags & MUONH_FLAG_SYNC_DEBUG) != 0, st};
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const Scalars sc = scalars_of(P, ws);
+    double* partials = reinterpret_cast<double*>(ws + P.off_partials);
+
+    // Same momentum and Newton-Schulz as muonh_step; for the matrices of
+    // fusable buckets the last apply writes the new weight itself, the rest
+    // get it from muon_finish_kernel.
+    const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
+    NsFuse fuse;
+    fuse.in = fuse.out_w = !check && ns_steps >= 1;
+    fuse.pair = (flags & MUONH_FLAG_GEMM_1SM) == 0;
+    fuse.check = check;
+    fuse.lr = lr;
+    fuse.wdecay = 1.f - lr * weight_decay;
+    NsIO* io = fuse.in ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
+
+    std::vector<DescBatch> batches = make_batches(P, mats, ws, false, true, fuse);
+    for (const DescBatch& B : batches) {
+        double e_in = 0, e_all = 0;
+        for (int k = 0; k < B.n; ++k) {
+            const double e = (double)B.d[k].rows * B.d[k].cols;
+            e_all += e;
+            if (B.d[k].fused & kFusedIn) e_in += e;
+        }
+        {
+            Trace tr(K_MOMENTUM, st);
+            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, st), 0, 14 * e_in + 18 * (e_all - e_in)),
+                         "momentum launch");
+        }
+        if (r) return r;
+        {
+            Trace tr(K_MOM_FIN, st);
+            r = sy.check(tr.done(launch_momentum_finalize(B, partials, sc, eps, st), 0, 0), "momentum finalize launch");
+        }
+        if (r) return r;
+    }
+    bool x_alt = false;
+    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
+    if (r) return r;
+    if (x_alt) batches = make_batches(P, mats, ws, true, true, fuse);
+    const float* o_scale = ns_steps == 0 ? sc.inv_nu : nullptr;
+    for (const DescBatch& B : batches) {
+        double e_sep = 0;
+        for (int k = 0; k < B.n; ++k)
+            if (!(B.d[k].fused & kFusedOutW)) e_sep += (double)B.d[k].rows * B.d[k].cols;
+        if (e_sep == 0) continue;
+        Trace tr(K_MUON_FIN, st);
+        r = sy.check(tr.done(launch_muon_finish(B, lr, fuse.wdecay, sc, o_scale, st), 0, e_sep * 14),
+                     "muon finish launch");
         if (r) return r;
     }
     return MUONH_OK;
@@ -795,7 +912,8 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     m.cols = cols;
     const double el = (double)rows * cols;
     NsFuse fuse;
-    fuse.in = (flags & MUONH_FLAG_FP32_CHECK) == 0 && ns_steps >= 1;
+    fuse.check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
+    fuse.in = !fuse.check && ns_steps >= 1;
     NsIO* io = fuse.in ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
     std::vector<DescBatch> batches = make_batches(P, &m, ws, false, false, fuse);
     const bool in_fused = (batches[0].d[0].fused & kFusedIn) != 0;
@@ -815,7 +933,7 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
     if (r) return r;
     m.w = out;
-    batches = make_batches(P, &m, ws, x_alt, false);
+    batches = make_batches(P, &m, ws, x_alt, false, fuse);
     {
         Trace tr(K_EMIT, st);
         r = sy.check(tr.done(launch_emit(batches[0], ns_steps == 0 ? sc.inv_nu : nullptr, st), 0, el * 8),

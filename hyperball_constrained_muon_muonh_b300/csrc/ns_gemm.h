@@ -12,10 +12,14 @@ enum NsMode { NS_GRAM = 0, NS_POLY = 1, NS_APPLY = 2 };
 // Variants of the apply stage (bit set):
 //   NS_IN_SRC   X is read from the matrix's own unscaled input (NsIO::src, W
 //               orientation) instead of the fp32 state: the first iteration
-//   NS_OUT_U    the epilogue finishes O = X and writes U = W - lr*O (X
-//               orientation) into the fp32 state, plus deterministic per-warp
-//               partial sums of ||U||^2: the last iteration of a MuonH step
-enum NsApplyVariant { NS_IN_SRC = 1, NS_OUT_U = 2 };
+//   NS_OUT_U    the epilogue finishes O = X and writes U = W - lr*O into
+//               the fp32 state, plus deterministic per-warp partial sums of
+//               ||U||^2: the last iteration of a MuonH step
+//   NS_OUT_W    the epilogue finishes O = X and writes the new weight
+//               wdecay*W - lr*O (fp32, and bf16 when NsIO::wb is set) into
+//               the caller's buffers, unless the matrix's status flag is set:
+//               the last iteration of a plain Muon step
+enum NsApplyVariant { NS_IN_SRC = 1, NS_OUT_U = 2, NS_OUT_W = 4 };
 
 struct NsIO;
 
@@ -47,7 +51,9 @@ struct GemmParams {
     const float* scale;     // per-matrix factor (bucket-local index) or null
     const NsIO* io;         // NS_IN_SRC / NS_OUT_U: per-matrix buffers (bucket-local index)
     double* upart;          // NS_OUT_U: ||U||^2 partials, warps_per_tile per tile, tile order
-    float nlr;              // NS_OUT_U: -lr
+    const uint32_t* mflags; // NS_OUT_W: per-matrix status bits (bucket-local); set = keep W
+    float nlr;              // NS_OUT_U / NS_OUT_W: -lr
+    float wdecay;           // NS_OUT_W: 1 - lr*weight_decay
     float ca, cb, cc;
     uint32_t* status;       // device status word
 };

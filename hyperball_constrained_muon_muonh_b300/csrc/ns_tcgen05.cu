@@ -272,9 +272,9 @@ __device__ __forceinline__ void prefetch_a(const GemmParams& p, int g, int i0, i
 // NS_IN_SRC the matrix's own input, row stride N).  y = sc*(a*x + (B X)); with NS_OUT_U, u = W - lr*y replaces
 // y and u^2 is added to hacc for the elements inside the matrix.
 template <int VAR>
-__device__ __forceinline__ void apply_slice(const GemmParams& p, int g, int i0, int lane, int j0,
-                                            const float (&v)[32], float* st, const float4 (&xp)[8],
-                                            const float4 (&wp)[8], float sc, float& hacc) {
+__device__ __forceinline__ void apply_slice(const GemmParams& p, const NsIO& io, bool keep_w, int g, int i0,
+                                            int lane, int j0, const float (&v)[32], float* st,
+                                            const float4 (&xp)[8], const float4 (&wp)[8], float sc, float& hacc) {
     stage_rows(st, lane, v);
     const int col = j0 + (lane & 7) * 4;
     float* xs = p.x_state + (size_t)g * p.ld_x * p.M;
@@ -299,6 +299,20 @@ __device__ __forceinline__ void apply_slice(const GemmParams& p, int g, int i0, 
                 if (nv > 1) hacc = fmaf(y.y, y.y, hacc);
                 if (nv > 2) hacc = fmaf(y.z, y.z, hacc);
                 if (nv > 3) hacc = fmaf(y.w, y.w, hacc);
+            }
+            if (VAR & NS_OUT_W) {
+                // new weight, written to the caller's buffers (row stride N)
+                if (!keep_w) {
+                    float4 u;
+                    u.x = fmaf(p.nlr, y.x, p.wdecay * wp[k].x);
+                    u.y = fmaf(p.nlr, y.y, p.wdecay * wp[k].y);
+                    u.z = fmaf(p.nlr, y.z, p.wdecay * wp[k].z);
+                    u.w = fmaf(p.nlr, y.w, p.wdecay * wp[k].w);
+                    const size_t woff = (size_t)row * p.N + col;
+                    *reinterpret_cast<float4*>(io.w + woff) = u;
+                    if (io.wb) store_bf16x4(reinterpret_cast<__nv_bfloat16*>(io.wb) + woff, u);
+                }
+                continue;
             }
             const size_t off = (size_t)row * p.ld_x + col;
             *reinterpret_cast<float4*>(xs + off) = y;
@@ -372,7 +386,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
     if (MODE != NS_POLY && p.scale) sc = p.scale[g];
     // X source of the apply epilogue: the fp32 state (row stride ld_x), or
     // the matrix's own input (row stride N; the variants need N % 4 == 0)
-    NsIO io{nullptr, nullptr};
+    NsIO io{nullptr, nullptr, nullptr};
     const float* xbase = nullptr;
     int xld = p.ld_x;
     if (MODE == NS_APPLY) {
@@ -385,14 +399,16 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
         }
     }
     // Operands the epilogue reads are loaded one slice ahead.  With
-    // NS_OUT_U both X and W are read for the current slice only, at its
-    // start (the register budget holds two 32-value slices, not four).
-    constexpr bool ahead = !(MODE == NS_APPLY && (VAR & NS_OUT_U));
+    // NS_OUT_U / NS_OUT_W both X and W are read for the current slice only,
+    // at its start (the register budget holds two 32-value slices, not four).
+    constexpr bool reads_w = MODE == NS_APPLY && (VAR & (NS_OUT_U | NS_OUT_W));
+    constexpr bool ahead = !reads_w;
+    const bool keep_w = (MODE == NS_APPLY && (VAR & NS_OUT_W)) ? p.mflags[g] != 0 : false;
     float4 xc[8], xn[8], wc[8];
     float ac[32], an[32];
     if (nsl > 0) {
         if (MODE == NS_APPLY) prefetch_rm(xbase, xld, p.M, p.N, i0, lane, jb, xc);
-        if (MODE == NS_APPLY && (VAR & NS_OUT_U)) prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, jb, wc);
+        if (reads_w) prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, jb, wc);
         if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, jb, ac);
     }
     if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status)) return false;
@@ -419,7 +435,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
                 if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, j0 + 32, an);
             }
             if (MODE == NS_APPLY) {
-                apply_slice<VAR>(p, g, i0, lane, j0, v, st, xc, wc, sc, hacc);
+                apply_slice<VAR>(p, io, keep_w, g, i0, lane, j0, v, st, xc, wc, sc, hacc);
                 if (ahead) {
 #pragma unroll
                     for (int u = 0; u < 8; ++u) xc[u] = xn[u];
@@ -979,6 +995,8 @@ static cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const 
         case NS_IN_SRC: return MUONH_LAUNCH(NS_APPLY, NS_IN_SRC);
         case NS_OUT_U: return MUONH_LAUNCH(NS_APPLY, NS_OUT_U);
         case NS_IN_SRC | NS_OUT_U: return MUONH_LAUNCH(NS_APPLY, NS_IN_SRC | NS_OUT_U);
+        case NS_OUT_W: return MUONH_LAUNCH(NS_APPLY, NS_OUT_W);
+        case NS_IN_SRC | NS_OUT_W: return MUONH_LAUNCH(NS_APPLY, NS_IN_SRC | NS_OUT_W);
         default: return cudaErrorInvalidValue;
     }
 #undef MUONH_LAUNCH
@@ -997,6 +1015,8 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
     if (p.mode != NS_APPLY) p.variant = 0;
     if (p.variant != 0 && !p.io) { *why = "apply variant without per-matrix buffers"; return cudaErrorInvalidValue; }
     if ((p.variant & NS_OUT_U) && !p.upart) { *why = "apply variant without partial buffer"; return cudaErrorInvalidValue; }
+    if ((p.variant & NS_OUT_W) && !p.mflags) { *why = "apply variant without status flags"; return cudaErrorInvalidValue; }
+    if ((p.variant & NS_OUT_U) && (p.variant & NS_OUT_W)) { *why = "conflicting apply variants"; return cudaErrorInvalidValue; }
     if (p.variant != 0 && (p.N & 3) != 0) { *why = "apply variant needs a row length that is a multiple of 4"; return cudaErrorInvalidValue; }
     CUtensorMap ta, tb;
     const bool oka = p.a_mn ? encode_bf16_3d(&ta, a_op, p.M, p.K, p.G, a_ld, 64)

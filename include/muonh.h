@@ -124,6 +124,20 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev,
                uint32_t flags, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * One plain Muon step (the optimizer MuonH is compared with: Puro-2B paper
+ * part 6, section 4.3.1, and the digest's "standard weight decay"): the same
+ * momentum and Newton-Schulz as muonh_step, then
+ *     W <- (1 - lr*weight_decay) * W - lr*O,   W_bf16 <- bf16(W)  (RNE)
+ * with no norm constraint (no r0).  Arguments as muonh_step; the workspace
+ * is sized by muonh_workspace_size for the same list and flags.  A matrix
+ * whose momentum turns non-finite keeps its W and sets
+ * MUONH_STATUS_NONFINITE_INPUT.
+ */
+int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float weight_decay,
+              int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags,
+              void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Workspace bytes for muonh_orthogonalize of one rows x cols matrix.
  */
 int muonh_orthogonalize_workspace_size(int64_t rows, int64_t cols, uint32_t flags, size_t* bytes);

@@ -20,7 +20,7 @@ def _declared():
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names |= set(re.findall(r"\b(muonh_[a-z0-9_]+)\s*\(", text))
+            names |= set(re.findall(r"\b((?:muonh|muon|adamw)_[a-z0-9_]+)\s*\(", text))
     return names
 
 
@@ -93,7 +93,7 @@ def test_workspace_size_layout():
     # X fp32 + 2 X bf16 (128 x 256) + A fp32 + A/B bf16 (128 x 128), plus scalars
     assert sz >= 128 * 256 * (4 + 4) + 128 * 128 * (4 + 4)
     assert sz % 256 == 0
-    # a tall and a wide matrix of the same sides share one bucket
+    # a tall and a wide matrix of the same sides share their s x s buffers
     assert mh.workspace_size([(256, 128), (128, 256)]) < 2 * sz + 4096
     # padding: l rounded up to 8 elements
     assert mh.workspace_size([(3, 5)]) >= 3 * 8 * 8
@@ -109,3 +109,22 @@ def test_qwen3_2b_workspace_fits():
     sz = mh.workspace_size(w.shapes)
     assert 10e9 < sz < 20e9
     assert w.n_params == 1_409_286_144
+
+
+def test_muon_step_rejects_bad_arguments_before_launch():
+    good = _arr([(4, 4)])
+    m = _lib.lib.muon_step
+
+    def call(arr=good, n=1, lr=0.02, beta=0.95, wd=0.1, steps=5, coeffs=COEFFS, eps=1e-7, flags=0, ws=256,
+             ws_bytes=1 << 40):
+        return m(arr, n, lr, beta, wd, steps, coeffs, eps, flags, ctypes.c_void_p(ws), ws_bytes, None)
+
+    assert m(None, 1, 0.02, 0.95, 0.1, 5, COEFFS, 1e-7, 0, None, 0, None) == _lib.ERR_INVALID_ARG
+    assert call(n=0) == _lib.ERR_INVALID_ARG
+    assert call(arr=_arr([(4, 4)], ptr=260)) == _lib.ERR_INVALID_ARG
+    assert call(wd=float("inf")) == _lib.ERR_INVALID_ARG
+    assert call(lr=float("nan")) == _lib.ERR_INVALID_ARG
+    assert call(steps=65) == _lib.ERR_INVALID_ARG
+    assert call(flags=0x80) == _lib.ERR_UNSUPPORTED
+    assert call(ws=0) == _lib.ERR_WORKSPACE
+    assert call(ws_bytes=16) == _lib.ERR_WORKSPACE
