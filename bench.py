@@ -37,7 +37,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MuonH steps/s on a 2B param set (1 B300); NS GEMM % of bf16 tensor peak"
 METRIC_MUON = "Muon steps/s on a 2B param set (1 B300); NS GEMM % of bf16 tensor peak"
+METRIC_ADAMW = "AdamW steps/s on the 2B model's non-matrix group (1 B300); % of HBM bandwidth"
 MUON_WD = 0.1
+ADAMW_BETAS, ADAMW_EPS, ADAMW_WD = (0.9, 0.95), 1e-8, 0.1
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
@@ -153,10 +155,35 @@ def oracle_sample_indices(work):
     return idx[:64]
 
 
-def oracle_sample(work, repeats=1, warmup=0):
-    """Time the float64 oracle on the sample; returns steps/s of the whole
-    workload (sample time scaled by the sample's share of the step's
-    Newton-Schulz flops), threads used and a description."""
+def oracle_sample_adamw(work, repeats=1, warmup=0):
+    """The AdamW oracle on a bounded sample of the AdamW group: the first
+    16384 rows of the embedding and every norm vector; scaled to steps/s of
+    the whole group by the sample's share of the elements (the method is
+    elementwise)."""
+    import numpy as np
+    from oracle import muonh as om
+    rows = 16384
+    ps = [work.weight(0, "cpu")[:rows].numpy()] + [w.numpy() for w in work.weights("cpu", range(1, len(work.shapes)))]
+    gs = [work.grad(0, 0, "cpu")[:rows].numpy()] + [g.numpy() for g in work.grads(0, "cpu", range(1, len(work.shapes)))]
+    ms = [np.zeros_like(p) for p in ps]
+    vs = [np.zeros_like(p) for p in ps]
+    for t in range(warmup):
+        om.adamw_step(ps, gs, ms, vs, t + 1, work.lr, *ADAMW_BETAS, ADAMW_EPS, ADAMW_WD)
+    t0 = time.perf_counter()
+    for t in range(repeats):
+        om.adamw_step(ps, gs, ms, vs, t + 1, work.lr, *ADAMW_BETAS, ADAMW_EPS, ADAMW_WD)
+    dt = (time.perf_counter() - t0) / max(repeats, 1)
+    frac = sum(p.size for p in ps) / work.n_params
+    sample = (f"oracle (NumPy float64) AdamW on {sum(p.size for p in ps)} of {work.n_params} elements (first "
+              f"{rows} embedding rows and all norm vectors), {repeats} timed step(s) of {dt:.2f} s each; scaled by "
+              f"the element share ({frac:.4f})")
+    return frac / dt, _oracle_cores(), sample
+
+
+def oracle_sample(work, repeats=1, warmup=0, optimizer="muonh"):
+    """Time the float64 oracle (MuonH, or plain Muon) on the sample; returns
+    steps/s of the whole workload (sample time scaled by the sample's share
+    of the step's Newton-Schulz flops), threads used and a description."""
     import numpy as np
     from oracle import muonh as om
     idx = oracle_sample_indices(work)
@@ -164,11 +191,17 @@ def oracle_sample(work, repeats=1, warmup=0):
     gs = [g.numpy() for g in work.grads(0, "cpu", idx)]
     ms = [np.zeros_like(w) for w in ws]
     r0 = om.capture_norms(ws)
+
+    def one():
+        if optimizer == "muon":
+            om.muon_step(ws, gs, ms, work.lr, work.beta, MUON_WD, work.ns_steps, work.coeffs, work.eps)
+        else:
+            om.muonh_step(ws, gs, ms, r0, work.lr, work.beta, work.ns_steps, work.coeffs, work.eps)
     for _ in range(warmup):
-        om.muonh_step(ws, gs, ms, r0, work.lr, work.beta, work.ns_steps, work.coeffs, work.eps)
+        one()
     t0 = time.perf_counter()
     for _ in range(repeats):
-        om.muonh_step(ws, gs, ms, r0, work.lr, work.beta, work.ns_steps, work.coeffs, work.eps)
+        one()
     dt = (time.perf_counter() - t0) / max(repeats, 1)
     frac = _ns_flops([work.shapes[i] for i in idx]) / _ns_flops(work.shapes)
     sample = (f"oracle (NumPy float64) on {len(idx)} of {len(work.shapes)} matrices (one of each shape), "
@@ -182,9 +215,13 @@ def run_reference(args, work, world, rank):
     W untimed and K timed steps, each on the bounded sample."""
     if rank != 0:
         return
-    v, cores, sample = oracle_sample(work, repeats=args.steps, warmup=args.warmup)
+    if args.optimizer == "adamw":
+        v, cores, sample = oracle_sample_adamw(work, repeats=args.steps, warmup=args.warmup)
+    else:
+        v, cores, sample = oracle_sample(work, repeats=args.steps, warmup=args.warmup, optimizer=args.optimizer)
     line = {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": {"muon": METRIC_MUON, "adamw": METRIC_ADAMW}.get(args.optimizer, METRIC),
+        "value": v, "unit": "steps/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": work.name, "matrices": len(work.shapes), "params": work.n_params},
@@ -206,9 +243,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--gemm-1sm", action="store_true", help="one-SM Newton-Schulz GEMM kernel")
-    ap.add_argument("--optimizer", default="muonh", choices=["muonh", "muon"],
+    ap.add_argument("--optimizer", default="muonh", choices=["muonh", "muon", "adamw"],
                     help="muon: plain Muon (decoupled weight decay 0.1, no hyperball), the baseline MuonH is "
-                         "compared with")
+                         "compared with; adamw: AdamW on the non-matrix group (workload qwen3_2b_adamw_group)")
     args = ap.parse_args()
 
     import muonh_workloads as wl
@@ -216,6 +253,8 @@ def main():
         if args.workload != "qwen3_2b_28layers":
             raise SystemExit("--layers applies to the qwen3_2b_28layers workload only")
         work = wl.qwen3_2b(layers=args.layers)
+    elif args.optimizer == "adamw" and args.workload == "qwen3_2b_28layers":
+        work = wl.adamw_group()
     else:
         work = wl.ALL[args.workload]()
     world, rank, local = _dist()
@@ -230,7 +269,8 @@ def main():
     # the oracle's BLAS pool is started before any CUDA work
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_sample(work, repeats=3)
+        cpu = (oracle_sample_adamw(work, repeats=3) if args.optimizer == "adamw"
+               else oracle_sample(work, repeats=3, optimizer=args.optimizer))
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -241,7 +281,11 @@ def main():
     ws = work.weights(dev)
     grads = [work.grads(t, dev) for t in range(2)]   # two gradient sets, alternated
     gemm_flags = mh.FLAG_GEMM_1SM if args.gemm_1sm else 0
-    if args.optimizer == "muon":
+    if args.optimizer == "adamw":
+        ws = [w.reshape(-1) for w in ws]
+        grads = [[g.reshape(-1) for g in gs] for gs in grads]
+        opt = mh.AdamW(ws, lr=work.lr, betas=ADAMW_BETAS, eps=ADAMW_EPS, weight_decay=ADAMW_WD, bf16_copies=True)
+    elif args.optimizer == "muon":
         opt = mh.Muon(ws, lr=work.lr, beta=work.beta, weight_decay=MUON_WD, ns_steps=work.ns_steps,
                       ns_coeffs=work.coeffs, eps=work.eps, bf16_copies=True, flags=gemm_flags)
     else:
@@ -323,24 +367,35 @@ def main():
     ns_launches = sum(prof[k]["launches"] for k in ns_kinds if k in prof)
     achieved = ns_flops / (ns_ms / 1000.0) / 1e12 if ns_ms > 0 else 0.0
     tr = _ns_traffic_from_profiles()
-    roofline = {
-        "bound": "tensor", "kernel": "ns_gemm_kernel (Gram, polynomial, apply launches)",
-        "achieved": achieved, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-        "frac": achieved / peaks["bf16_sustained"],
-        "peak_kind": f"bf16 dense sustained, {peaks['source']}",
-        "frac_of_burst": achieved / peaks["bf16"],
-        "traffic": tr["bytes_per_launch"] if tr and tr.get("current") else None,
-        "launches": ns_launches, "flops_per_launch": ns_flops / max(ns_launches, 1),
-        "ms_per_launch": ns_ms / max(ns_launches, 1),
-        "ns_share_of_step": ns_ms / max(ms_total, 1e-9),
-    }
+    if args.optimizer == "adamw":
+        a = prof.get("adamw", {"ms": 0.0, "bytes": 0.0, "launches": 0})
+        gbs = a["bytes"] / (a["ms"] / 1000.0) / 1e9 if a["ms"] > 0 else 0.0
+        roofline = {
+            "bound": "hbm", "kernel": "adamw_kernel", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": gbs / peaks["hbm_gbs"], "peak_kind": f"HBM copy bandwidth, {peaks['source']}",
+            "traffic": None, "launches": a["launches"], "bytes_per_launch": a["bytes"] / max(a["launches"], 1),
+            "ms_per_launch": a["ms"] / max(a["launches"], 1),
+        }
+    else:
+        roofline = {
+            "bound": "tensor", "kernel": "ns_gemm_kernel (Gram, polynomial, apply launches)",
+            "achieved": achieved, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_sustained"],
+            "peak_kind": f"bf16 dense sustained, {peaks['source']}",
+            "frac_of_burst": achieved / peaks["bf16"],
+            "traffic": tr["bytes_per_launch"] if tr and tr.get("current") else None,
+            "launches": ns_launches, "flops_per_launch": ns_flops / max(ns_launches, 1),
+            "ms_per_launch": ns_ms / max(ns_launches, 1),
+            "ns_share_of_step": ns_ms / max(ms_total, 1e-9),
+        }
     hbm = {}
     for k in ("momentum", "hyperball_norm", "hyperball_apply", "hyperball_scale", "muon_finish"):
         if k in prof and prof[k]["ms"] > 0:
             gbs = prof[k]["bytes"] / (prof[k]["ms"] / 1000.0) / 1e9
             hbm[k] = {"GB/s": gbs, "frac": gbs / peaks["hbm_gbs"], "ms_per_step": prof[k]["ms"] / args.steps}
     line = {
-        "metric": METRIC_MUON if args.optimizer == "muon" else METRIC, "value": value, "unit": "steps/s",
+        "metric": {"muon": METRIC_MUON, "adamw": METRIC_ADAMW}.get(args.optimizer, METRIC), "value": value,
+        "unit": "steps/s",
         "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -350,7 +405,9 @@ def main():
                    "l2": "inputs larger than L2 (about 20 GB of optimizer state touched per step)",
                    "parallelism": f"replica x{world}",
                    "ns_gemm": "1-SM 128x256 tiles" if args.gemm_1sm else "2-SM pair 256x256 tiles",
-                   "optimizer": "muon (weight decay 0.1)" if args.optimizer == "muon" else "muonh"},
+                   "optimizer": {"muon": "muon (weight decay 0.1)",
+                                 "adamw": f"adamw (betas {ADAMW_BETAS}, eps {ADAMW_EPS}, weight decay {ADAMW_WD})"
+                                 }.get(args.optimizer, "muonh")},
         "ns_tflops": achieved,
         "roofline": roofline,
         "hbm_kernels": hbm,

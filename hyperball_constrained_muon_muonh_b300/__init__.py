@@ -25,7 +25,7 @@ from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_SYNC_DEBUG, STATUS_DEGEN
 
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
 
-__all__ = ["MuonH", "Muon", "capture_norms", "workspace_size", "step", "muon_step", "orthogonalize",
+__all__ = ["MuonH", "Muon", "AdamW", "adamw_step", "capture_norms", "workspace_size", "step", "muon_step", "orthogonalize",
            "orthogonalize_workspace_size", "get_status", "profile_read", "MuonHError", "NS_COEFFS"]
 
 
@@ -230,3 +230,51 @@ class Muon:
             self._grads_ptrs = ptrs
         muon_step(self._arr, self.lr, self.beta, self.weight_decay, self.ns_steps, self.ns_coeffs, self.eps,
                   self.flags, self.workspace, stream)
+
+
+def adamw_array(params, grads, exp_avgs, exp_avg_sqs, bf16=None):
+    """Build the adamw_param_t array for lists of contiguous fp32 CUDA tensors."""
+    arr = (_lib.AdamParamT * len(params))()
+    for i, p in enumerate(params):
+        for t, nm in ((p, "params"), (grads[i], "grads"), (exp_avgs[i], "exp_avgs"), (exp_avg_sqs[i], "exp_avg_sqs")):
+            if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+                raise ValueError(f"{nm}[{i}] must be a contiguous CUDA float32 tensor")
+        arr[i].p, arr[i].grad = p.data_ptr(), grads[i].data_ptr()
+        arr[i].exp_avg, arr[i].exp_avg_sq = exp_avgs[i].data_ptr(), exp_avg_sqs[i].data_ptr()
+        arr[i].numel = p.numel()
+        if bf16 is not None and bf16[i] is not None:
+            arr[i].p_bf16 = bf16[i].data_ptr()
+    return arr
+
+
+def adamw_step(arr, step, lr, beta1, beta2, eps, weight_decay, stream=None) -> None:
+    """One adamw_step call on a prebuilt adamw_param_t array."""
+    check(lib.adamw_step(arr, len(arr), int(step), lr, beta1, beta2, eps, weight_decay, _stream(stream)),
+          "adamw_step")
+
+
+class AdamW:
+    """AdamW (decoupled weight decay, bias-corrected moments) over a fixed
+    list of contiguous fp32 CUDA tensors: the optimizer of the parameters
+    outside the MuonH group.  Moments start at zero."""
+
+    def __init__(self, params, lr=2e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, bf16_copies=False):
+        self.params = list(params)
+        self.lr, self.eps, self.weight_decay = float(lr), float(eps), float(weight_decay)
+        self.beta1, self.beta2 = (float(b) for b in betas)
+        self.exp_avgs = [torch.zeros_like(p) for p in self.params]
+        self.exp_avg_sqs = [torch.zeros_like(p) for p in self.params]
+        self.bf16 = [torch.empty_like(p, dtype=torch.bfloat16) for p in self.params] if bf16_copies else None
+        self.t = 0
+        self._grads_ptrs = None
+        self._arr = None
+
+    def step(self, grads=None, stream=None) -> None:
+        if grads is None:
+            grads = [p.grad for p in self.params]
+        ptrs = tuple(g.data_ptr() for g in grads)
+        if ptrs != self._grads_ptrs:
+            self._arr = adamw_array(self.params, grads, self.exp_avgs, self.exp_avg_sqs, self.bf16)
+            self._grads_ptrs = ptrs
+        self.t += 1
+        adamw_step(self._arr, self.t, self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, stream)

@@ -36,7 +36,7 @@ EXPORTS = (
     "muonh_orthogonalize_workspace_size", "muonh_orthogonalize", "muonh_get_status",
     "muonh_status_string", "muonh_last_error", "muonh_version",
     "muonh_profile_enable", "muonh_profile_read", "muonh_launch_count",
-    "muonh_orthogonalize_static", "muon_step",
+    "muonh_orthogonalize_static", "muon_step", "adamw_step",
 )
 
 STATIC_SCRATCH_BYTES = 80 * 1024 * 1024
@@ -51,6 +51,18 @@ class MatrixT(ctypes.Structure):
         ("mom", ctypes.c_void_p),
         ("rows", ctypes.c_int64),
         ("cols", ctypes.c_int64),
+    ]
+
+
+class AdamParamT(ctypes.Structure):
+    """adamw_param_t"""
+    _fields_ = [
+        ("p", ctypes.c_void_p),
+        ("p_bf16", ctypes.c_void_p),
+        ("grad", ctypes.c_void_p),
+        ("exp_avg", ctypes.c_void_p),
+        ("exp_avg_sq", ctypes.c_void_p),
+        ("numel", ctypes.c_int64),
     ]
 
 
@@ -85,6 +97,7 @@ def _load():
     lib.muonh_workspace_size.argtypes = [mp, I, U32, ctypes.POINTER(SZ)]
     lib.muonh_step.argtypes = [mp, I, P, F, F, I, fp, F, U32, P, SZ, P]
     lib.muon_step.argtypes = [mp, I, F, F, F, I, fp, F, U32, P, SZ, P]
+    lib.adamw_step.argtypes = [ctypes.POINTER(AdamParamT), I, I, F, F, F, F, F, P]
     lib.muonh_orthogonalize_workspace_size.argtypes = [I64, I64, U32, ctypes.POINTER(SZ)]
     lib.muonh_orthogonalize.argtypes = [P, P, I64, I64, I, fp, F, U32, P, SZ, P]
     lib.muonh_orthogonalize_static.argtypes = [P, P, I64, I64, I, fp, F, U32, P]

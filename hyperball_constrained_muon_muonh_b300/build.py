@@ -12,7 +12,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmuonh.so")
-SOURCES = ["muonh_api.cu", "elementwise.cu", "ns_tcgen05.cu", "ns_simt.cu", "noalloc.cu"]
+SOURCES = ["muonh_api.cu", "elementwise.cu", "ns_tcgen05.cu", "ns_simt.cu", "adamw.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "ns_gemm.h"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",

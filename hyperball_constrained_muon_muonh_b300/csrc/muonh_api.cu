@@ -42,6 +42,8 @@ cudaError_t launch_muon_finish(const DescBatch& b, float lr, float wdecay, const
 cudaError_t launch_emit(const DescBatch& b, const float* o_scale, cudaStream_t st);
 cudaError_t launch_capture_norms(const DescBatch& b, float* r0, cudaStream_t st);
 cudaError_t status_word(uint32_t** ptr);
+int adamw_launch(const adamw_param_t* params, int n, int step, float lr, float beta1, float beta2, float eps,
+                 float weight_decay, cudaStream_t st, int* launches, double* bytes);
 
 namespace {
 
@@ -872,6 +874,20 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
         if (r) return r;
     }
     return MUONH_OK;
+}
+
+int adamw_step(const adamw_param_t* params, int n, int step, float lr, float beta1, float beta2, float eps,
+               float weight_decay, void* stream) {
+    g_last_error.clear();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Trace tr(K_ADAMW, st);
+    int launches = 0;
+    double bytes = 0;
+    const int r = adamw_launch(params, n, step, lr, beta1, beta2, eps, weight_decay, st, &launches, &bytes);
+    if (launches > 1) g_launches += launches - 1;
+    if (launches == 0) --g_launches;
+    tr.done(cudaSuccess, 0, bytes);
+    return r;
 }
 
 int muonh_orthogonalize_workspace_size(int64_t rows, int64_t cols, uint32_t flags, size_t* bytes) {

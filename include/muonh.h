@@ -137,6 +137,32 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
               int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags,
               void* workspace, size_t ws_bytes, void* stream);
 
+/* One tensor of the AdamW group: fp32, any shape, contiguous, numel
+ * elements; every pointer 16-byte aligned. */
+typedef struct adamw_param {
+    float*       p;           /* in/out: parameter                              */
+    uint16_t*    p_bf16;      /* out (optional, NULL = skip): bf16 copy of p    */
+    const float* grad;        /* in: gradient                                   */
+    float*       exp_avg;     /* in/out: first moment m (zero at the start)     */
+    float*       exp_avg_sq;  /* in/out: second moment v (zero at the start)    */
+    int64_t      numel;       /* >= 1 */
+} adamw_param_t;
+
+/*
+ * One AdamW step over params[0..n) (host array), for the parameters outside
+ * the MuonH group (Puro-2B model card, section "Training": AdamW, weight
+ * decay 0.1).  `step` is the 1-based index of this step (bias correction):
+ *   m <- beta1*m + (1 - beta1)*g;   v <- beta2*v + (1 - beta2)*g^2
+ *   p <- (1 - lr*weight_decay)*p - lr * m_hat / (sqrt(v_hat) + eps)
+ *   with m_hat = m / (1 - beta1^step), v_hat = v / (1 - beta2^step);
+ *   p_bf16 <- bf16(p) (RNE)
+ * beta1, beta2 in [0, 1); eps >= 0 (eps = 0 with v = 0 gives NaN).  Needs
+ * no workspace.  Non-finite gradients propagate into p, m and v (no status
+ * bit), as in the textbook method.
+ */
+int adamw_step(const adamw_param_t* params, int n, int step, float lr, float beta1, float beta2,
+               float eps, float weight_decay, void* stream);
+
 /*
  * Workspace bytes for muonh_orthogonalize of one rows x cols matrix.
  */

@@ -147,12 +147,24 @@ def aspect_16384x1024() -> Workload:
                     labels=[f"tall{i}" for i in range(4)] + [f"wide{i}" for i in range(4)])
 
 
+def adamw_group() -> Workload:
+    """The parameters outside the MuonH group of a Qwen3-style 2B model, for
+    AdamW: a token embedding of 151936 x 2048 (the pages give no vocabulary
+    size; this is the Qwen3 family's), two RMSNorm weights per layer and the
+    final one (57 x 2048), and the q/k head norms (56 x 128).  Vectors are
+    1 x n matrices here.  lr 2e-3 is the MuonH rate divided by the model
+    card's 10x multiplier."""
+    shapes = [(151936, D_MODEL)] + [(1, D_MODEL)] * (2 * N_LAYERS + 1) + [(1, HEAD_DIM)] * (2 * N_LAYERS)
+    return Workload("qwen3_2b_adamw_group", shapes, lr=2e-3, g_scale=1e-2)
+
+
 ALL = {
     "single_256x128": single_256x128,
     "qwen3_layer_d2048": qwen3_layer,
     "qwen3_2b_28layers": qwen3_2b,
     "batched_1024x256x256": batched_256,
     "aspect_16384x1024": aspect_16384x1024,
+    "qwen3_2b_adamw_group": adamw_group,
 }
 
 

@@ -128,3 +128,26 @@ def test_muon_step_rejects_bad_arguments_before_launch():
     assert call(flags=0x80) == _lib.ERR_UNSUPPORTED
     assert call(ws=0) == _lib.ERR_WORKSPACE
     assert call(ws_bytes=16) == _lib.ERR_WORKSPACE
+
+
+def test_adamw_step_rejects_bad_arguments_before_launch():
+    def arr(numel=8, ptr=256):
+        a = (_lib.AdamParamT * 1)()
+        a[0].p = a[0].grad = a[0].exp_avg = a[0].exp_avg_sq = ptr
+        a[0].numel = numel
+        return a
+
+    f = _lib.lib.adamw_step
+
+    def call(a=None, n=1, step=1, lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1):
+        return f(arr() if a is None else a, n, step, lr, b1, b2, eps, wd, None)
+
+    assert f(None, 1, 1, 1e-3, 0.9, 0.95, 1e-8, 0.1, None) == _lib.ERR_INVALID_ARG
+    assert call(n=0) == _lib.ERR_INVALID_ARG
+    assert call(step=0) == _lib.ERR_INVALID_ARG
+    assert call(b1=1.0) == _lib.ERR_INVALID_ARG
+    assert call(b2=-0.1) == _lib.ERR_INVALID_ARG
+    assert call(eps=-1.0) == _lib.ERR_INVALID_ARG
+    assert call(lr=float("nan")) == _lib.ERR_INVALID_ARG
+    assert call(a=arr(numel=0)) == _lib.ERR_INVALID_ARG
+    assert call(a=arr(ptr=264)) == _lib.ERR_INVALID_ARG
