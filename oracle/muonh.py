@@ -131,8 +131,35 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     return out.reshape(np.shape(x))
 
 
+def ns_input(m_new: np.ndarray, g: np.ndarray, beta: float, nesterov: bool) -> np.ndarray:
+    """The matrix Newton-Schulz orthogonalises: the momentum itself, or with
+    Nesterov momentum (a variant the pages do not name, offered as a flag)
+    the look-ahead ``G + beta * M_new``."""
+    if not nesterov:
+        return np.asarray(m_new, np.float64)
+    return np.asarray(g, np.float64) + beta * np.asarray(m_new, np.float64)
+
+
+def update_scale(rows: int, cols: int, kind: str) -> float:
+    """Factor applied to O before the weight update (the pages use none).
+
+    ``none``  1
+    ``shape`` sqrt(max(1, rows/cols)): a tall matrix's update is scaled up
+              so that its per-row step matches a square one's
+    ``rms``   0.2 * sqrt(max(rows, cols)): O's RMS entry becomes about 0.2,
+              the RMS of a typical AdamW update
+    """
+    if kind == "none":
+        return 1.0
+    if kind == "shape":
+        return float(np.sqrt(max(1.0, rows / cols)))
+    if kind == "rms":
+        return 0.2 * float(np.sqrt(max(rows, cols)))
+    raise ValueError(kind)
+
+
 def muonh_step(weights, grads, moms, r0, lr, beta, ns_steps, coeffs, eps,
-               state_dtype=np.float32):
+               state_dtype=np.float32, nesterov=False, scale="none"):
     """One MuonH step over a list of matrices.
 
     For each matrix: momentum, Newton-Schulz of the momentum, hyperball
@@ -140,20 +167,23 @@ def muonh_step(weights, grads, moms, r0, lr, beta, ns_steps, coeffs, eps,
     ``w`` (new weights, ``state_dtype``), ``w_bf16`` (bfloat16 copy of the new
     weights as float32 values), ``m`` (new momenta, ``state_dtype``), ``o``
     (the float64 Newton-Schulz outputs) and ``status`` (per-matrix bits).
-    With ``state_dtype=None`` the state stays float64.
+    With ``state_dtype=None`` the state stays float64.  ``nesterov`` and
+    ``scale`` select the variants of ``ns_input`` and ``update_scale``; ``o``
+    is the scaled update.
     """
     out = {"w": [], "w_bf16": [], "m": [], "o": [], "status": []}
     for w, g, m, radius in zip(weights, grads, moms, r0):
         m_new = momentum(m, g, beta)
         if state_dtype is not None:
             m_new = m_new.astype(state_dtype)
+        x = ns_input(m_new, g, beta, nesterov)
         status = 0
-        if not np.all(np.isfinite(m_new)):
+        if not np.all(np.isfinite(x)):
             o = np.full(np.shape(w), np.nan)
             w_new = np.array(w, dtype=np.float64)
             status = STATUS_NONFINITE_INPUT
         else:
-            o = newton_schulz(m_new, ns_steps, coeffs, eps)
+            o = update_scale(*np.shape(w), scale) * newton_schulz(x, ns_steps, coeffs, eps)
             w_new, status = hyperball(w, o, lr, float(radius))
         if state_dtype is not None:
             w_new = w_new.astype(state_dtype)
@@ -172,23 +202,26 @@ def muon_update(w: np.ndarray, o: np.ndarray, lr: float, weight_decay: float) ->
     return (1.0 - lr * weight_decay) * np.asarray(w, np.float64) - lr * np.asarray(o, np.float64)
 
 
-def muon_step(weights, grads, moms, lr, beta, weight_decay, ns_steps, coeffs, eps, state_dtype=np.float32):
+def muon_step(weights, grads, moms, lr, beta, weight_decay, ns_steps, coeffs, eps, state_dtype=np.float32,
+              nesterov=False, scale="none"):
     """One plain Muon step over a list of matrices (the baseline of the
     matched-ladder comparison): momentum and Newton-Schulz as in
-    ``muonh_step``, then ``muon_update``.  Same return dict as
-    ``muonh_step``; a matrix whose momentum is non-finite keeps its W."""
+    ``muonh_step``, then ``muon_update``.  Same return dict and variants as
+    ``muonh_step``; a matrix whose Newton-Schulz input is non-finite keeps
+    its W."""
     out = {"w": [], "w_bf16": [], "m": [], "o": [], "status": []}
     for w, g, m in zip(weights, grads, moms):
         m_new = momentum(m, g, beta)
         if state_dtype is not None:
             m_new = m_new.astype(state_dtype)
+        x = ns_input(m_new, g, beta, nesterov)
         status = 0
-        if not np.all(np.isfinite(m_new)):
+        if not np.all(np.isfinite(x)):
             o = np.full(np.shape(w), np.nan)
             w_new = np.array(w, dtype=np.float64)
             status = STATUS_NONFINITE_INPUT
         else:
-            o = newton_schulz(m_new, ns_steps, coeffs, eps)
+            o = update_scale(*np.shape(w), scale) * newton_schulz(x, ns_steps, coeffs, eps)
             w_new = muon_update(w, o, lr, weight_decay)
         if state_dtype is not None:
             w_new = w_new.astype(state_dtype)

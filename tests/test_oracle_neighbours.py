@@ -12,6 +12,7 @@ the textbook method) and by its closed-form first step.  Planted mistakes
 pin.
 """
 
+import math
 from fractions import Fraction
 
 import numpy as np
@@ -187,3 +188,63 @@ def test_planted_adamw_mistakes_are_caught(kind):
             out["v"].append(v)
         return out
     assert _adamw_worst(bad) > 1e-9
+
+
+# ---------------------------------------------------------------------------
+# Nesterov momentum and update scales (variants offered as flags)
+# ---------------------------------------------------------------------------
+
+def test_nesterov_input_small_integers():
+    # beta = 0.5, G = 1 every step: M = 1, 1.5, 1.75; look-ahead X = G + beta*M = 1.5, 1.75, 1.875
+    m = np.zeros((1, 1))
+    g = np.ones((1, 1))
+    for want_m, want_x in ((1.0, 1.5), (1.5, 1.75), (1.75, 1.875)):
+        m = om.momentum(m, g, 0.5)
+        assert m[0, 0] == want_m
+        assert om.ns_input(m, g, 0.5, True)[0, 0] == want_x
+        assert om.ns_input(m, g, 0.5, False)[0, 0] == want_m
+
+
+def test_nesterov_with_zero_beta_is_heavy_ball():
+    rng = np.random.default_rng(21)
+    w = [rng.standard_normal((6, 10))]
+    g = [rng.standard_normal((6, 10))]
+    m = [rng.standard_normal((6, 10))]
+    r0 = om.capture_norms(w)
+    a = om.muonh_step(w, g, m, r0, 0.02, 0.0, 5, COEFFS, 1e-7, state_dtype=None, nesterov=True)
+    b = om.muonh_step(w, g, m, r0, 0.02, 0.0, 5, COEFFS, 1e-7, state_dtype=None, nesterov=False)
+    assert np.array_equal(a["w"][0], b["w"][0])
+
+
+def test_nesterov_changes_the_step():
+    rng = np.random.default_rng(22)
+    w, g, m = (rng.standard_normal((6, 10)) for _ in range(3))
+    a = om.muon_step([w], [g], [m], 0.02, 0.9, 0.0, 5, COEFFS, 1e-7, state_dtype=None, nesterov=True)
+    want = om.muon_update(w, om.newton_schulz(g + 0.9 * (0.9 * m + g), 5, COEFFS, 1e-7), 0.02, 0.0)
+    assert _rel(a["w"][0], want) < 1e-14
+
+
+def test_update_scale_values():
+    assert om.update_scale(4, 4, "shape") == 1.0
+    assert om.update_scale(8, 2, "shape") == 2.0          # tall: sqrt(8/2)
+    assert om.update_scale(2, 8, "shape") == 1.0          # wide: max(1, 2/8)
+    assert om.update_scale(8, 2, "rms") == 0.2 * math.sqrt(8)
+    assert om.update_scale(2, 8, "rms") == 0.2 * math.sqrt(8)
+    assert om.update_scale(5, 3, "none") == 1.0
+
+
+@pytest.mark.parametrize("kind", ["shape", "rms"])
+def test_scaled_step_is_step_with_scaled_rate(kind):
+    # U = W - lr*(s*O) is the unscaled step at rate lr*s
+    rng = np.random.default_rng(23)
+    for shape in ((8, 2), (2, 8), (5, 5)):
+        w, g = rng.standard_normal(shape), rng.standard_normal(shape)
+        z = np.zeros(shape)
+        sc = om.update_scale(*shape, kind)
+        r0 = om.capture_norms([w])
+        a = om.muonh_step([w], [g], [z], r0, 0.02, 0.9, 5, COEFFS, 1e-7, state_dtype=None, scale=kind)
+        b = om.muonh_step([w], [g], [z], r0, 0.02 * sc, 0.9, 5, COEFFS, 1e-7, state_dtype=None)
+        assert _rel(a["w"][0], b["w"][0]) < 1e-14
+        c = om.muon_step([w], [g], [z], 0.02, 0.9, 0.1, 5, COEFFS, 1e-7, state_dtype=None, scale=kind)
+        o = om.newton_schulz(g, 5, COEFFS, 1e-7)
+        assert _rel(c["w"][0], (1 - 0.02 * 0.1) * w - 0.02 * sc * o) < 1e-14
