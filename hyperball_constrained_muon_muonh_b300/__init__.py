@@ -20,8 +20,9 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_SYNC_DEBUG, STATUS_DEGENERATE_NORM,  # noqa: F401
-                   STATUS_KERNEL_TIMEOUT, STATUS_NONFINITE_INPUT, MuonHError, check, lib)
+from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_NESTEROV, FLAG_SCALE_RMS, FLAG_SCALE_SHAPE,  # noqa: F401
+                   FLAG_SYNC_DEBUG, STATUS_DEGENERATE_NORM, STATUS_KERNEL_TIMEOUT, STATUS_NONFINITE_INPUT,
+                   MuonHError, check, lib)
 
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
 

@@ -25,8 +25,11 @@ STATUS_DEGENERATE_NORM = 0x2
 STATUS_KERNEL_TIMEOUT = 0x4
 
 FLAG_FP32_CHECK = 0x1
+FLAG_NESTEROV = 0x2
 FLAG_SYNC_DEBUG = 0x4
 FLAG_GEMM_1SM = 0x8
+FLAG_SCALE_SHAPE = 0x10
+FLAG_SCALE_RMS = 0x20
 
 MAX_SIDE = 65536
 

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "../../include/muonh.h"
@@ -86,6 +87,16 @@ __host__ __device__ inline int chunks_for(int rows, int cols) {
     return (rows + cr - 1) / cr;
 }
 
+// Update scale of a rows x cols matrix (MUONH_FLAG_SCALE_*), in float, the
+// same on host and device (IEEE division and square root).
+enum UpdateScale { kScaleNone = 0, kScaleShape = 1, kScaleRms = 2 };
+
+__host__ __device__ inline float update_scale(int rows, int cols, int mode) {
+    if (mode == kScaleShape) return sqrtf(fmaxf(1.f, (float)rows / (float)cols));
+    if (mode == kScaleRms) return 0.2f * sqrtf((float)(rows > cols ? rows : cols));
+    return 1.f;
+}
+
 // Per-matrix scalars in the workspace, indexed by bucket-order position.
 struct Scalars {
     double* nu2;          // ||M||_F^2
@@ -93,6 +104,8 @@ struct Scalars {
     float* inv_nu;        // 1 / (||M||_F + eps)
     float* inv_nu2;       // inv_nu^2
     float* factor;        // r0 / ||W - lr*O||_F
+    float* oscale;        // factor on X_state that gives O: the update scale, times
+                          // inv_nu when no Newton-Schulz iteration ran
     uint32_t* flags;      // per-matrix status bits
 };
 

@@ -45,16 +45,24 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, float4 v) {
 }
 
 // ---------------------------------------------------------------------------
-// K1: M <- beta*M + G; X_op = bf16(M) and, unless D.fused has kFusedIn (the
-// first apply GEMM then reads M itself), X_state = M, in the matrix's own
+// K1: M <- beta*M + G; the Newton-Schulz input X is M (or with Nesterov
+// momentum G + beta*M); X_op = bf16(X) and, unless D.fused has kFusedIn (the
+// first apply GEMM then reads M itself), X_state = X, in the matrix's own
 // orientation (unscaled: the 1/(||M||+eps) factor is folded into the
-// Newton-Schulz epilogues); partial ||M||^2 per chunk.  With D.m null the
+// Newton-Schulz epilogues); partial ||X||^2 per chunk.  With D.m null the
 // input G itself is the Newton-Schulz input (standalone orthogonalisation).
 // With `io` set, the CTA of each matrix's first chunk records where the
 // matrix's input and weight are (NsIO, indexed by bucket-order position).
 // ---------------------------------------------------------------------------
+// The Newton-Schulz input of one element: the new momentum v, or with
+// Nesterov momentum the look-ahead g + beta*v.
+__device__ __forceinline__ float ns_in(float v, float g, float beta, bool nesterov) {
+    return nesterov ? fmaf(beta, v, g) : v;
+}
+
 template <bool WRITE_XS>
-__device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, int r_end, float beta, float& acc) {
+__device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, int r_end, float beta, bool nesterov,
+                                               float& acc) {
     const int cols = D.cols, ld = D.ld;
     if (ld == cols && (cols & 3) == 0) {
         // flat float4 stream; four vectors per thread in flight
@@ -78,24 +86,29 @@ __device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, in
                     v.z = fmaf(beta, m[u].z, v.z); v.w = fmaf(beta, m[u].w, v.w);
                     *reinterpret_cast<float4*>(D.m + f) = v;
                 }
-                if (WRITE_XS) *reinterpret_cast<float4*>(D.xs + f) = v;
-                store_bf16x4(D.xo + f, v);
-                acc = fmaf(v.x, v.x, acc); acc = fmaf(v.y, v.y, acc);
-                acc = fmaf(v.z, v.z, acc); acc = fmaf(v.w, v.w, acc);
+                const float4 x = make_float4(ns_in(v.x, g[u].x, beta, nesterov), ns_in(v.y, g[u].y, beta, nesterov),
+                                             ns_in(v.z, g[u].z, beta, nesterov), ns_in(v.w, g[u].w, beta, nesterov));
+                if (WRITE_XS) *reinterpret_cast<float4*>(D.xs + f) = x;
+                store_bf16x4(D.xo + f, x);
+                acc = fmaf(x.x, x.x, acc); acc = fmaf(x.y, x.y, acc);
+                acc = fmaf(x.z, x.z, acc); acc = fmaf(x.w, x.w, acc);
             }
         }
         for (; e < e1; e += 4 * kThreads) {
-            float4 v = __ldcs(reinterpret_cast<const float4*>(D.g + e));
+            const float4 g = __ldcs(reinterpret_cast<const float4*>(D.g + e));
+            float4 v = g;
             if (D.m) {
                 const float4 m = *reinterpret_cast<const float4*>(D.m + e);
                 v.x = fmaf(beta, m.x, v.x); v.y = fmaf(beta, m.y, v.y);
                 v.z = fmaf(beta, m.z, v.z); v.w = fmaf(beta, m.w, v.w);
                 *reinterpret_cast<float4*>(D.m + e) = v;
             }
-            if (WRITE_XS) *reinterpret_cast<float4*>(D.xs + e) = v;
-            store_bf16x4(D.xo + e, v);
-            acc = fmaf(v.x, v.x, acc); acc = fmaf(v.y, v.y, acc);
-            acc = fmaf(v.z, v.z, acc); acc = fmaf(v.w, v.w, acc);
+            const float4 x = make_float4(ns_in(v.x, g.x, beta, nesterov), ns_in(v.y, g.y, beta, nesterov),
+                                         ns_in(v.z, g.z, beta, nesterov), ns_in(v.w, g.w, beta, nesterov));
+            if (WRITE_XS) *reinterpret_cast<float4*>(D.xs + e) = x;
+            store_bf16x4(D.xo + e, x);
+            acc = fmaf(x.x, x.x, acc); acc = fmaf(x.y, x.y, acc);
+            acc = fmaf(x.z, x.z, acc); acc = fmaf(x.w, x.w, acc);
         }
     } else {
         // any row length: the chunk's elements in row-major order
@@ -103,17 +116,20 @@ __device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, in
         for (size_t e = threadIdx.x; e < n; e += kThreads) {
             const size_t r = r_begin + e / cols, c = e % cols;
             const size_t wi = r * cols + c, xi = r * ld + c;
-            float m = D.g[wi];
+            const float g = D.g[wi];
+            float m = g;
             if (D.m) { m = fmaf(beta, D.m[wi], m); D.m[wi] = m; }
-            if (WRITE_XS) D.xs[xi] = m;
-            D.xo[xi] = __float2bfloat16_rn(m);
-            acc = fmaf(m, m, acc);
+            const float x = ns_in(m, g, beta, nesterov);
+            if (WRITE_XS) D.xs[xi] = x;
+            D.xo[xi] = __float2bfloat16_rn(x);
+            acc = fmaf(x, x, acc);
         }
     }
 }
 
 __global__ void __launch_bounds__(kThreads)
-momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restrict__ partials, NsIO* io) {
+momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restrict__ partials, NsIO* io,
+                bool nesterov) {
     __shared__ double red[kThreads / 32];
     const int chunk = b.chunk_begin + blockIdx.x;
     const int mi = find_matrix(b, chunk);
@@ -131,16 +147,18 @@ momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restr
     const int r_end = min(D.rows, r_begin + cr);
     float acc = 0.f;
     if (D.fused & kFusedIn)
-        momentum_chunk<false>(D, r_begin, r_end, beta, acc);
+        momentum_chunk<false>(D, r_begin, r_end, beta, nesterov, acc);
     else
-        momentum_chunk<true>(D, r_begin, r_end, beta, acc);
+        momentum_chunk<true>(D, r_begin, r_end, beta, nesterov, acc);
     double s = block_sum<kThreads>((double)acc, red);
     if (threadIdx.x == 0) partials[chunk] = s;
 }
 
-// Per matrix: nu^2 = sum of its partials (index order); 1/(nu+eps) factors.
+// Per matrix: nu^2 = sum of its partials (index order); 1/(nu+eps) factors;
+// oscale = the update scale (times 1/(nu+eps) when no Newton-Schulz
+// iteration runs, X_state then holding the unscaled input).
 __global__ void momentum_finalize(const __grid_constant__ DescBatch b, const double* __restrict__ partials,
-                                  Scalars sc, float eps) {
+                                  Scalars sc, float eps, int scale_mode, bool no_iterations) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= b.n) return;
     const MatDesc& D = b.d[i];
@@ -160,6 +178,8 @@ __global__ void momentum_finalize(const __grid_constant__ DescBatch b, const dou
     sc.inv_nu[p] = inv;
     sc.inv_nu2[p] = inv * inv;
     sc.flags[p] = f;
+    const float us = update_scale(D.rows, D.cols, scale_mode);
+    sc.oscale[p] = no_iterations ? us * inv : us;
 }
 
 // ---------------------------------------------------------------------------
@@ -397,16 +417,17 @@ capture_norms_kernel(const __grid_constant__ DescBatch b, float* __restrict__ r0
 // ---------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------
-cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, NsIO* io, cudaStream_t st) {
+cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, NsIO* io, bool nesterov,
+                            cudaStream_t st) {
     const int nblk = b.chunk_end - b.chunk_begin;
     if (nblk <= 0) return cudaSuccess;
-    momentum_kernel<<<nblk, kThreads, 0, st>>>(b, beta, partials, io);
+    momentum_kernel<<<nblk, kThreads, 0, st>>>(b, beta, partials, io, nesterov);
     return cudaGetLastError();
 }
 
 cudaError_t launch_momentum_finalize(const DescBatch& b, const double* partials, const Scalars& sc,
-                                     float eps, cudaStream_t st) {
-    momentum_finalize<<<(b.n + 127) / 128, 128, 0, st>>>(b, partials, sc, eps);
+                                     float eps, int scale_mode, bool no_iterations, cudaStream_t st) {
+    momentum_finalize<<<(b.n + 127) / 128, 128, 0, st>>>(b, partials, sc, eps, scale_mode, no_iterations);
     return cudaGetLastError();
 }
 

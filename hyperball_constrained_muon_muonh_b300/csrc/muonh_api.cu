@@ -28,9 +28,10 @@
 
 namespace muonh {
 
-cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, NsIO* io, cudaStream_t st);
+cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, NsIO* io, bool nesterov,
+                            cudaStream_t st);
 cudaError_t launch_momentum_finalize(const DescBatch& b, const double* partials, const Scalars& sc, float eps,
-                                     cudaStream_t st);
+                                     int scale_mode, bool no_iterations, cudaStream_t st);
 cudaError_t launch_hyperball_norm(const DescBatch& b, float lr, double* partials, const float* o_scale,
                                   cudaStream_t st);
 cudaError_t launch_hyperball_finalize(const DescBatch& b, const double* partials, const double* upart,
@@ -183,7 +184,7 @@ struct Plan {
     std::vector<int> bucket_of;   // bucket-order position -> bucket index
     std::vector<int> chunk0;      // bucket-order position -> first chunk
     int total_chunks = 0;
-    size_t off_nu2, off_rho2, off_inv, off_inv2, off_fac, off_flags, off_partials, off_io, off_upart;
+    size_t off_nu2, off_rho2, off_inv, off_inv2, off_fac, off_oscale, off_flags, off_partials, off_io, off_upart;
     long long n_upart = 0;        // ||U||^2 partials of the last apply GEMM, all buckets
     size_t bytes = 0;
 };
@@ -217,6 +218,7 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
     P.off_inv = take(sizeof(float) * n);
     P.off_inv2 = take(sizeof(float) * n);
     P.off_fac = take(sizeof(float) * n);
+    P.off_oscale = take(sizeof(float) * n);
     P.off_flags = take(sizeof(uint32_t) * n);
     P.off_io = take(sizeof(NsIO) * n);
     // s-groups with the most Newton-Schulz work first, and within one the
@@ -346,6 +348,7 @@ Scalars scalars_of(const Plan& P, uint8_t* ws) {
     sc.inv_nu = reinterpret_cast<float*>(ws + P.off_inv);
     sc.inv_nu2 = reinterpret_cast<float*>(ws + P.off_inv2);
     sc.factor = reinterpret_cast<float*>(ws + P.off_fac);
+    sc.oscale = reinterpret_cast<float*>(ws + P.off_oscale);
     sc.flags = reinterpret_cast<uint32_t*>(ws + P.off_flags);
     return sc;
 }
@@ -363,6 +366,7 @@ struct NsFuse {
     bool out_w = false;   // plain Muon: the last apply writes the new weight
     bool pair = true;
     bool check = false;   // fp32 check mode: every bucket on CUDA cores
+    int scale_mode = kScaleNone;   // update scale of O (UpdateScale)
     float lr = 0.f;
     float wdecay = 1.f;   // out_w: 1 - lr*weight_decay
 };
@@ -584,7 +588,7 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         a.io = reinterpret_cast<const NsIO*>(ws + P.off_io) + B.first;
         a.upart = reinterpret_cast<double*>(ws + P.off_upart) + B.upart0;
         a.mflags = sc.flags + B.first;
-        a.nlr = -fuse.lr;
+        a.nlr = -fuse.lr * update_scale(B.R, B.C, fuse.scale_mode);
         a.wdecay = fuse.wdecay;
         const double G = B.G, S = B.s, L = B.l;
         cudaError_t e;
@@ -627,9 +631,18 @@ int check_scalars(int ns_steps, const float* coeffs, float eps, uint32_t flags) 
     for (int i = 0; i < 3; ++i)
         if (!std::isfinite(coeffs[i])) return fail(MUONH_ERR_INVALID_ARG, "ns_coeffs must be finite");
     if (!std::isfinite(eps) || eps < 0.f) return fail(MUONH_ERR_INVALID_ARG, "eps must be finite and >= 0");
-    if (flags & ~(uint32_t)(MUONH_FLAG_FP32_CHECK | MUONH_FLAG_SYNC_DEBUG | MUONH_FLAG_GEMM_1SM))
+    if (flags & ~(uint32_t)(MUONH_FLAG_FP32_CHECK | MUONH_FLAG_SYNC_DEBUG | MUONH_FLAG_GEMM_1SM |
+                            MUONH_FLAG_NESTEROV | MUONH_FLAG_SCALE_SHAPE | MUONH_FLAG_SCALE_RMS))
         return fail(MUONH_ERR_UNSUPPORTED, "unknown flag bits");
+    if ((flags & MUONH_FLAG_SCALE_SHAPE) && (flags & MUONH_FLAG_SCALE_RMS))
+        return fail(MUONH_ERR_UNSUPPORTED, "MUONH_FLAG_SCALE_SHAPE and MUONH_FLAG_SCALE_RMS exclude each other");
     return MUONH_OK;
+}
+
+int scale_mode_of(uint32_t flags) {
+    if (flags & MUONH_FLAG_SCALE_SHAPE) return kScaleShape;
+    if (flags & MUONH_FLAG_SCALE_RMS) return kScaleRms;
+    return kScaleNone;
 }
 
 int check_workspace(void* ws, size_t ws_bytes, size_t need) {
@@ -743,14 +756,19 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     // rescale.  Other matrices, the fp32 check mode and ns_steps = 0 keep the
     // separate norm and apply passes.
     const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
+    const bool nesterov = (flags & MUONH_FLAG_NESTEROV) != 0;
     NsFuse fuse;
-    fuse.in = fuse.out = !check && ns_steps >= 1;
+    // with Nesterov momentum the Newton-Schulz input is not M, so it is stored
+    fuse.in = !check && !nesterov && ns_steps >= 1;
+    fuse.out = !check && ns_steps >= 1;
     fuse.pair = (flags & MUONH_FLAG_GEMM_1SM) == 0;
     fuse.check = check;
+    fuse.scale_mode = scale_mode_of(flags);
     fuse.lr = lr;
     if (fuse.out && P.n_upart > INT32_MAX)
         return fail(MUONH_ERR_UNSUPPORTED, "too many matrices/tiles for one step: split the list");
-    NsIO* io = fuse.in ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
+    // the table of the matrices' own buffers, read by every fused apply variant
+    NsIO* io = (fuse.in || fuse.out) ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
     const double* upart = reinterpret_cast<const double*>(ws + P.off_upart);
 
     std::vector<DescBatch> batches = make_batches(P, mats, ws, false, true, fuse);
@@ -765,12 +783,13 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
         const double bytes = 14 * elems(B, kFusedIn, true) + 18 * elems(B, kFusedIn, false);
         {
             Trace tr(K_MOMENTUM, st);
-            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, st), 0, bytes), "momentum launch");
+            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, nesterov, st), 0, bytes), "momentum launch");
         }
         if (r) return r;
         {
             Trace tr(K_MOM_FIN, st);
-            r = sy.check(tr.done(launch_momentum_finalize(B, partials, sc, eps, st), 0, 0), "momentum finalize launch");
+            r = sy.check(tr.done(launch_momentum_finalize(B, partials, sc, eps, fuse.scale_mode, ns_steps == 0, st), 0, 0),
+                         "momentum finalize launch");
         }
         if (r) return r;
     }
@@ -778,7 +797,7 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
     if (r) return r;
     if (x_alt) batches = make_batches(P, mats, ws, true, true, fuse);
-    const float* o_scale = ns_steps == 0 ? sc.inv_nu : nullptr;
+    const float* o_scale = sc.oscale;
     for (const DescBatch& B : batches) {
         const double e_sep = elems(B, kFusedOut, false), e_fused = elems(B, kFusedOut, true);
         if (e_sep > 0) {
@@ -830,13 +849,17 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
     // fusable buckets the last apply writes the new weight itself, the rest
     // get it from muon_finish_kernel.
     const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
+    const bool nesterov = (flags & MUONH_FLAG_NESTEROV) != 0;
     NsFuse fuse;
-    fuse.in = fuse.out_w = !check && ns_steps >= 1;
+    fuse.in = !check && !nesterov && ns_steps >= 1;
+    fuse.out_w = !check && ns_steps >= 1;
     fuse.pair = (flags & MUONH_FLAG_GEMM_1SM) == 0;
     fuse.check = check;
+    fuse.scale_mode = scale_mode_of(flags);
     fuse.lr = lr;
     fuse.wdecay = 1.f - lr * weight_decay;
-    NsIO* io = fuse.in ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
+    // the table of the matrices' own buffers, read by every fused apply variant
+    NsIO* io = (fuse.in || fuse.out_w) ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
 
     std::vector<DescBatch> batches = make_batches(P, mats, ws, false, true, fuse);
     for (const DescBatch& B : batches) {
@@ -848,13 +871,15 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
         }
         {
             Trace tr(K_MOMENTUM, st);
-            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, st), 0, 14 * e_in + 18 * (e_all - e_in)),
+            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, nesterov, st), 0,
+                                 14 * e_in + 18 * (e_all - e_in)),
                          "momentum launch");
         }
         if (r) return r;
         {
             Trace tr(K_MOM_FIN, st);
-            r = sy.check(tr.done(launch_momentum_finalize(B, partials, sc, eps, st), 0, 0), "momentum finalize launch");
+            r = sy.check(tr.done(launch_momentum_finalize(B, partials, sc, eps, fuse.scale_mode, ns_steps == 0, st), 0, 0),
+                         "momentum finalize launch");
         }
         if (r) return r;
     }
@@ -862,7 +887,7 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
     r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
     if (r) return r;
     if (x_alt) batches = make_batches(P, mats, ws, true, true, fuse);
-    const float* o_scale = ns_steps == 0 ? sc.inv_nu : nullptr;
+    const float* o_scale = sc.oscale;
     for (const DescBatch& B : batches) {
         double e_sep = 0;
         for (int k = 0; k < B.n; ++k)
@@ -935,13 +960,13 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     const bool in_fused = (batches[0].d[0].fused & kFusedIn) != 0;
     {
         Trace tr(K_MOMENTUM, st);
-        r = sy.check(tr.done(launch_momentum(batches[0], 0.f, partials, io, st), 0, el * (in_fused ? 6 : 10)),
+        r = sy.check(tr.done(launch_momentum(batches[0], 0.f, partials, io, false, st), 0, el * (in_fused ? 6 : 10)),
                      "momentum launch");
     }
     if (r) return r;
     {
         Trace tr(K_MOM_FIN, st);
-        r = sy.check(tr.done(launch_momentum_finalize(batches[0], partials, sc, eps, st), 0, 0),
+        r = sy.check(tr.done(launch_momentum_finalize(batches[0], partials, sc, eps, kScaleNone, ns_steps == 0, st), 0, 0),
                      "momentum finalize launch");
     }
     if (r) return r;

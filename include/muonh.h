@@ -71,6 +71,13 @@ extern "C" {
 #define MUONH_FLAG_GEMM_1SM    0x8u  /* Newton-Schulz GEMMs on one SM per 128x256 tile instead of the
                                         default CTA pair per 256x256 tile (same results up to bf16
                                         rounding order; for comparison and small problems) */
+/* Step variants the pages do not name (muonh_step and muon_step; ignored by
+ * muonh_orthogonalize): */
+#define MUONH_FLAG_NESTEROV    0x2u  /* Newton-Schulz input G + beta*M_new (Nesterov look-ahead)
+                                        instead of M_new; the stored momentum is M_new either way */
+#define MUONH_FLAG_SCALE_SHAPE 0x10u /* O <- sqrt(max(1, rows/cols)) * O before the update */
+#define MUONH_FLAG_SCALE_RMS   0x20u /* O <- 0.2 * sqrt(max(rows, cols)) * O before the update
+                                        (not together with MUONH_FLAG_SCALE_SHAPE) */
 
 /* One weight matrix and its optimizer state.  All device pointers, fp32
  * row-major rows x cols (row stride = cols elements), 16-byte aligned.
