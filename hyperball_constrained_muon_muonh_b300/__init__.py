@@ -179,20 +179,26 @@ class MuonH:
         self.moms = [torch.zeros_like(w) for w in self.weights]
         self.bf16 = [torch.empty_like(w, dtype=torch.bfloat16) for w in self.weights] if bf16_copies else None
         self.r0 = capture_norms(self.weights)
-        self._grads_ptrs = None
-        self._arr = None
+        self._arrays = {}
         self.workspace = torch.empty(workspace_size([tuple(w.shape) for w in self.weights], self.flags),
                                      dtype=torch.uint8, device=self.weights[0].device)
 
     def step(self, grads=None, stream=None) -> None:
         if grads is None:
             grads = [w.grad for w in self.weights]
+        step(self._array_for(grads), self.r0, self.lr, self.beta, self.ns_steps, self.ns_coeffs, self.eps,
+             self.flags, self.workspace, stream)
+
+    def _array_for(self, grads):
+        # one matrix array per set of gradient buffers (a few at most): a
+        # training loop that alternates buffers rebuilds nothing
         ptrs = tuple(g.data_ptr() for g in grads)
-        if ptrs != self._grads_ptrs:
-            self._arr = matrix_array(self.weights, grads, self.moms, self.bf16)
-            self._grads_ptrs = ptrs
-        step(self._arr, self.r0, self.lr, self.beta, self.ns_steps, self.ns_coeffs, self.eps, self.flags,
-             self.workspace, stream)
+        arr = self._arrays.get(ptrs)
+        if arr is None:
+            if len(self._arrays) >= 4:
+                self._arrays.clear()
+            arr = self._arrays[ptrs] = matrix_array(self.weights, grads, self.moms, self.bf16)
+        return arr
 
     def state_dict(self):
         return {"moms": [m.clone() for m in self.moms], "r0": self.r0.clone()}
@@ -217,20 +223,24 @@ class Muon:
         self.flags = (FLAG_FP32_CHECK if fp32_check else 0) | int(flags)
         self.moms = [torch.zeros_like(w) for w in self.weights]
         self.bf16 = [torch.empty_like(w, dtype=torch.bfloat16) for w in self.weights] if bf16_copies else None
-        self._grads_ptrs = None
-        self._arr = None
+        self._arrays = {}
         self.workspace = torch.empty(workspace_size([tuple(w.shape) for w in self.weights], self.flags),
                                      dtype=torch.uint8, device=self.weights[0].device)
 
     def step(self, grads=None, stream=None) -> None:
         if grads is None:
             grads = [w.grad for w in self.weights]
+        muon_step(self._array_for(grads), self.lr, self.beta, self.weight_decay, self.ns_steps, self.ns_coeffs,
+                  self.eps, self.flags, self.workspace, stream)
+
+    def _array_for(self, grads):
         ptrs = tuple(g.data_ptr() for g in grads)
-        if ptrs != self._grads_ptrs:
-            self._arr = matrix_array(self.weights, grads, self.moms, self.bf16)
-            self._grads_ptrs = ptrs
-        muon_step(self._arr, self.lr, self.beta, self.weight_decay, self.ns_steps, self.ns_coeffs, self.eps,
-                  self.flags, self.workspace, stream)
+        arr = self._arrays.get(ptrs)
+        if arr is None:
+            if len(self._arrays) >= 4:
+                self._arrays.clear()
+            arr = self._arrays[ptrs] = matrix_array(self.weights, grads, self.moms, self.bf16)
+        return arr
 
 
 def adamw_array(params, grads, exp_avgs, exp_avg_sqs, bf16=None):
@@ -267,15 +277,16 @@ class AdamW:
         self.exp_avg_sqs = [torch.zeros_like(p) for p in self.params]
         self.bf16 = [torch.empty_like(p, dtype=torch.bfloat16) for p in self.params] if bf16_copies else None
         self.t = 0
-        self._grads_ptrs = None
-        self._arr = None
+        self._arrays = {}
 
     def step(self, grads=None, stream=None) -> None:
         if grads is None:
             grads = [p.grad for p in self.params]
         ptrs = tuple(g.data_ptr() for g in grads)
-        if ptrs != self._grads_ptrs:
-            self._arr = adamw_array(self.params, grads, self.exp_avgs, self.exp_avg_sqs, self.bf16)
-            self._grads_ptrs = ptrs
+        arr = self._arrays.get(ptrs)
+        if arr is None:
+            if len(self._arrays) >= 4:
+                self._arrays.clear()
+            arr = self._arrays[ptrs] = adamw_array(self.params, grads, self.exp_avgs, self.exp_avg_sqs, self.bf16)
         self.t += 1
-        adamw_step(self._arr, self.t, self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, stream)
+        adamw_step(arr, self.t, self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, stream)

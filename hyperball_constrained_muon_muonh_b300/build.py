@@ -12,8 +12,8 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmuonh.so")
-SOURCES = ["muonh_api.cu", "elementwise.cu", "ns_tcgen05.cu", "ns_simt.cu", "adamw.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "ns_gemm.h"]
+SOURCES = ["muonh_api.cu", "elementwise.cu", "ns_tcgen05.cu", "ns_small.cu", "ns_simt.cu", "adamw.cu", "noalloc.cu"]
+HEADERS = ["common.cuh", "ns_gemm.h", "tc_ptx.cuh"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
          "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "-shared"]

@@ -36,7 +36,9 @@ struct MatDesc {
 //              ||U||^2 (part0, npart), so the hyperball step only rescales
 //   kFusedOutW the last apply GEMM of a plain Muon step writes the new
 //              weight (1 - lr*wd)*W - lr*O and its bf16 copy itself
-constexpr int kFusedIn = 1, kFusedOut = 2, kFusedOutW = 4;
+//   kFusedAll  the whole step runs in the small-matrix kernel (both sides
+//              <= 256): every other kernel of the step skips the matrix
+constexpr int kFusedIn = 1, kFusedOut = 2, kFusedOutW = 4, kFusedAll = 8;
 static_assert(sizeof(MatDesc) == 80, "MatDesc layout");
 
 // Largest descriptor batch one launch carries in its parameter space

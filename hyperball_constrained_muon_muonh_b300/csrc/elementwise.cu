@@ -134,6 +134,7 @@ momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restr
     const int chunk = b.chunk_begin + blockIdx.x;
     const int mi = find_matrix(b, chunk);
     const MatDesc& D = b.d[mi];
+    if (D.fused & kFusedAll) return;
     const int cols = D.cols;
     if (io && chunk == D.chunk0 && threadIdx.x == 0) {
         NsIO r;
@@ -162,6 +163,7 @@ __global__ void momentum_finalize(const __grid_constant__ DescBatch b, const dou
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= b.n) return;
     const MatDesc& D = b.d[i];
+    if (D.fused & kFusedAll) return;
     const int p = b.first + i;
     const int nch = chunks_for(D.rows, D.cols);
     double s = 0.0;
@@ -268,7 +270,7 @@ hyperball_norm_kernel(const __grid_constant__ DescBatch b, float lr, double* __r
     const int chunk = b.chunk_begin + blockIdx.x;
     const int mi = find_matrix(b, chunk);
     const MatDesc& D = b.d[mi];
-    if (D.fused & kFusedOut) return;
+    if (D.fused & (kFusedOut | kFusedAll)) return;
     const int p = b.first + mi;
     const int cr = chunk_rows_for(D.rows, D.cols);
     const int r_begin = (chunk - D.chunk0) * cr;
@@ -291,7 +293,7 @@ hyperball_finish_kernel(const __grid_constant__ DescBatch b, float lr, const flo
     const int mi = find_matrix(b, chunk);
     const MatDesc& D = b.d[mi];
     const int p = b.first + mi;
-    if (flags[p] != 0) return;  // W stays as it was
+    if ((D.fused & kFusedAll) || flags[p] != 0) return;  // W stays as it was
     const int cr = chunk_rows_for(D.rows, D.cols);
     const int r_begin = (chunk - D.chunk0) * cr;
     const int r_end = min(D.rows, r_begin + cr);
@@ -314,7 +316,7 @@ muon_finish_kernel(const __grid_constant__ DescBatch b, float lr, float wdecay, 
     const int mi = find_matrix(b, chunk);
     const MatDesc& D = b.d[mi];
     const int p = b.first + mi;
-    if ((D.fused & kFusedOutW) || flags[p] != 0) return;
+    if ((D.fused & (kFusedOutW | kFusedAll)) || flags[p] != 0) return;
     const int cr = chunk_rows_for(D.rows, D.cols);
     const int r_begin = (chunk - D.chunk0) * cr;
     const int r_end = min(D.rows, r_begin + cr);
@@ -353,6 +355,7 @@ __global__ void hyperball_finalize(const __grid_constant__ DescBatch b, const do
     const int lane = threadIdx.x & 31;
     if (i >= b.n) return;
     const MatDesc& D = b.d[i];
+    if (D.fused & kFusedAll) return;
     const int p = b.first + i;
     const bool from_gemm = (D.fused & kFusedOut) != 0;
     const double* src = from_gemm ? upart + (size_t)D.part0 : partials + D.chunk0;

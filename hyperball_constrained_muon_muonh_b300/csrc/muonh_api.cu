@@ -46,6 +46,7 @@ cudaError_t status_word(uint32_t** ptr);
 int adamw_launch(const adamw_param_t* params, int n, int step, float lr, float beta1, float beta2, float eps,
                  float weight_decay, cudaStream_t st, int* launches, double* bytes);
 
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -69,12 +70,13 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // the new weight
 enum Kind { K_MOMENTUM, K_MOM_FIN, K_GRAM, K_POLY, K_APPLY, K_APPLY_IN, K_APPLY_OUT, K_APPLY_IN_OUT,
             K_APPLY_OUTW, K_APPLY_IN_OUTW, K_HB_NORM, K_HB_FIN, K_HB_APPLY, K_HB_SCALE, K_MUON_FIN, K_EMIT,
-            K_CAPTURE, K_SIMT_GRAM, K_SIMT_POLY, K_SIMT_APPLY, K_ADAMW, K_COUNT };
+            K_CAPTURE, K_SIMT_GRAM, K_SIMT_POLY, K_SIMT_APPLY, K_ADAMW, K_SMALL, K_COUNT };
 const char* const kKindName[K_COUNT] = {"momentum", "momentum_finalize", "ns_gram", "ns_poly", "ns_apply",
                                         "ns_apply_in", "ns_apply_out", "ns_apply_in_out", "ns_apply_outw",
                                         "ns_apply_in_outw", "hyperball_norm", "hyperball_finalize",
                                         "hyperball_apply", "hyperball_scale", "muon_finish", "emit",
-                                        "capture_norms", "fp32_gram", "fp32_poly", "fp32_apply", "adamw"};
+                                        "capture_norms", "fp32_gram", "fp32_poly", "fp32_apply", "adamw",
+                                        "small_step"};
 
 int apply_kind(int variant) {
     switch (variant) {
@@ -141,11 +143,17 @@ struct Trace {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Matrices whose short side is at most this run Newton-Schulz on fp32 CUDA
-// cores.  Their s x s Gram is smaller than one tensor-core tile, so the
-// tensor cores gain nothing, and with only a few singular values the bf16
-// rounding of B (|B| ~ 2.7 against a result ~0.7 per step) is not averaged
-// out: rank-1 inputs lose several percent in bf16, none in fp32.
-constexpr int kSmallSide = 32;
+// cores.  With few singular values the bf16 rounding of the tensor-core
+// operands is not averaged out (B ~ -2.7 against a per-step result ~0.7 is a
+// near-cancellation): emulating the bf16 path in NumPy on Gaussian inputs
+// gives a median error in O of 3.2 % at 36 x 100, 2.7 % at 64 x 200 and
+// 1.9 % at 96 x 256 (14 % worst case on rank-1 inputs), against 1e-6 in fp32.
+// These matrices are small, so fp32 costs little.
+constexpr int kSmallSide = 80;
+
+// Matrices with both sides at most this (and a short side above kSmallSide)
+// can take the whole step in one on-chip kernel (csrc/ns_small.cu).
+constexpr int kSmallStepSide = 256;
 
 struct Bucket {
     int R, C;             // matrix shape (rows, cols)
@@ -159,6 +167,7 @@ struct Bucket {
     size_t off_xs, off_xo;                    // byte offsets in the workspace
     size_t off_af, off_aop, off_bop;          // this bucket's slice of its s-group's s x s buffers
     size_t off_bf32;                          // fp32 check mode: its slice of the group's fp32 B
+    int sgroup;                               // index of its s-group
     long long upart0;                         // first ||U||^2 partial of this bucket (index into the
                                               // plan's partial region; written by the last apply GEMM)
     int tiles1, tiles2;                       // apply tiles per matrix: 1-SM and pair kernel
@@ -170,6 +179,8 @@ struct Bucket {
 // covers all of them.
 struct SGroup {
     int s, ld_s, G;
+    bool small_step;      // every matrix has both sides in (kSmallSide, kSmallStepSide]: the whole
+                          // step can run in the small-matrix kernel
     int b_begin, b_end;   // its buckets, contiguous in Plan::buckets
     size_t off_af, off_aop, off_bop;
     size_t elems() const { return (size_t)G * s * ld_s; }
@@ -248,7 +259,11 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
         S.ld_s = (int)align_up(S.s, 8);
         S.G = 0;
         S.b_begin = (int)P.buckets.size();
-        for (auto& sh : shapes) S.G += (int)sh.idx.size();
+        S.small_step = S.s > kSmallSide;
+        for (auto& sh : shapes) {
+            S.G += (int)sh.idx.size();
+            if (sh.R > kSmallStepSide || sh.C > kSmallStepSide) S.small_step = false;
+        }
         S.off_af = take(sizeof(float) * S.elems());
         S.off_aop = take(sizeof(__nv_bfloat16) * S.elems());
         // fp32 check mode keeps an fp32 B at off_aop, spanning A_op and B_op
@@ -274,6 +289,7 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
             B.off_aop = S.off_aop + sizeof(__nv_bfloat16) * so;
             B.off_bop = S.off_bop + sizeof(__nv_bfloat16) * so;
             B.off_bf32 = S.off_aop + sizeof(float) * so;
+            B.sgroup = (int)P.sgroups.size();
             g_in_group += B.G;
             B.tiles1 = tc::tiles_per_matrix(NS_APPLY, B.R, B.C);
             B.tiles2 = tc::pair_tiles_per_matrix(NS_APPLY, B.R, B.C);
@@ -366,6 +382,7 @@ struct NsFuse {
     bool out_w = false;   // plain Muon: the last apply writes the new weight
     bool pair = true;
     bool check = false;   // fp32 check mode: every bucket on CUDA cores
+    bool small = false;   // s-groups marked small_step take the whole step in the small-matrix kernel
     int scale_mode = kScaleNone;   // update scale of O (UpdateScale)
     float lr = 0.f;
     float wdecay = 1.f;   // out_w: 1 - lr*weight_decay
@@ -407,7 +424,9 @@ std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, u
             D.part0 = 0;
             D.npart = 0;
             D.fused = 0;
-            if (bk.fusable) {
+            if (fuse.small && P.sgroups[bk.sgroup].small_step) {
+                D.fused = kFusedAll;
+            } else if (bk.fusable) {
                 if (fuse.in) D.fused |= kFusedIn;
                 if (fuse.out_w) D.fused |= kFusedOutW;
                 if (fuse.out) {
@@ -607,6 +626,7 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
 
     for (int it = 0; it < ns_steps; ++it) {
         for (const SGroup& Q : P.sgroups) {
+            if (fuse.small && Q.small_step) continue;   // done by the small-matrix kernel
             // every bucket of an s-group has the same s, so the same path
             const bool simt = check || Q.s <= kSmallSide;
             for (int b = Q.b_begin; b < Q.b_end; ++b) {
@@ -637,6 +657,40 @@ int check_scalars(int ns_steps, const float* coeffs, float eps, uint32_t flags) 
     if ((flags & MUONH_FLAG_SCALE_SHAPE) && (flags & MUONH_FLAG_SCALE_RMS))
         return fail(MUONH_ERR_UNSUPPORTED, "MUONH_FLAG_SCALE_SHAPE and MUONH_FLAG_SCALE_RMS exclude each other");
     return MUONH_OK;
+}
+
+// True when every matrix of the batch takes its whole step in the
+// small-matrix kernel (the batch's other kernels would do nothing).
+bool all_small(const DescBatch& b) {
+    for (int k = 0; k < b.n; ++k)
+        if (!(b.d[k].fused & kFusedAll)) return false;
+    return true;
+}
+
+// The matrices of small-step s-groups (caller indices, bucket order).
+std::vector<int> small_step_matrices(const Plan& P) {
+    std::vector<int> idx;
+    for (int p = 0; p < P.n; ++p)
+        if (P.sgroups[P.buckets[P.bucket_of[p]].sgroup].small_step) idx.push_back(P.order[p]);
+    return idx;
+}
+
+// One launch sequence of the small-matrix kernel for a step (no-op if the
+// step has none of its matrices).
+int run_small_step(const Plan& P, const muonh_matrix_t* mats, const SmallStepArgs& a, Sync& sy) {
+    const std::vector<int> idx = small_step_matrices(P);
+    if (idx.empty()) return MUONH_OK;
+    double flops = 0, bytes = 0;
+    for (int u : idx) {
+        const double r = (double)mats[u].rows, c = (double)mats[u].cols, sd = std::min(r, c), ld = std::max(r, c);
+        flops += a.ns_steps * (3 * sd * sd * ld + sd * sd * sd);
+        bytes += r * c * (22 + (mats[u].w_bf16 ? 0 : -2));
+    }
+    Trace tr(K_SMALL, sy.st);
+    int launches = 0;
+    const cudaError_t e = launch_small_step(mats, idx.data(), (int)idx.size(), a, sy.st, &launches);
+    if (launches > 1) g_launches += launches - 1;
+    return sy.check(tr.done(e, flops, bytes), "small-matrix step launch");
 }
 
 int scale_mode_of(uint32_t flags) {
@@ -763,8 +817,14 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     fuse.out = !check && ns_steps >= 1;
     fuse.pair = (flags & MUONH_FLAG_GEMM_1SM) == 0;
     fuse.check = check;
+    fuse.small = !check && ns_steps >= 1;
     fuse.scale_mode = scale_mode_of(flags);
     fuse.lr = lr;
+    if (fuse.small) {
+        SmallStepArgs sa{lr, beta, eps, 1.f, ns_coeffs, ns_steps, false, nesterov, fuse.scale_mode, r0_dev, status};
+        r = run_small_step(P, mats, sa, sy);
+        if (r) return r;
+    }
     if (fuse.out && P.n_upart > INT32_MAX)
         return fail(MUONH_ERR_UNSUPPORTED, "too many matrices/tiles for one step: split the list");
     // the table of the matrices' own buffers, read by every fused apply variant
@@ -780,7 +840,9 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
         return e;
     };
     for (const DescBatch& B : batches) {
-        const double bytes = 14 * elems(B, kFusedIn, true) + 18 * elems(B, kFusedIn, false);
+        if (all_small(B)) continue;
+        const double bytes = 14 * elems(B, kFusedIn, true) +
+                             18 * (elems(B, kFusedIn, false) - elems(B, kFusedAll, true));
         {
             Trace tr(K_MOMENTUM, st);
             r = sy.check(tr.done(launch_momentum(B, beta, partials, io, nesterov, st), 0, bytes), "momentum launch");
@@ -799,7 +861,9 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     if (x_alt) batches = make_batches(P, mats, ws, true, true, fuse);
     const float* o_scale = sc.oscale;
     for (const DescBatch& B : batches) {
-        const double e_sep = elems(B, kFusedOut, false), e_fused = elems(B, kFusedOut, true);
+        if (all_small(B)) continue;
+        const double e_sep = elems(B, kFusedOut, false) - elems(B, kFusedAll, true);
+        const double e_fused = elems(B, kFusedOut, true);
         if (e_sep > 0) {
             Trace tr(K_HB_NORM, st);
             r = sy.check(tr.done(launch_hyperball_norm(B, lr, partials, o_scale, st), 0, e_sep * 8),
@@ -855,16 +919,25 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
     fuse.out_w = !check && ns_steps >= 1;
     fuse.pair = (flags & MUONH_FLAG_GEMM_1SM) == 0;
     fuse.check = check;
+    fuse.small = !check && ns_steps >= 1;
     fuse.scale_mode = scale_mode_of(flags);
     fuse.lr = lr;
     fuse.wdecay = 1.f - lr * weight_decay;
+    if (fuse.small) {
+        SmallStepArgs sa{lr, beta, eps, fuse.wdecay, ns_coeffs, ns_steps, true, nesterov, fuse.scale_mode, nullptr,
+                         status};
+        r = run_small_step(P, mats, sa, sy);
+        if (r) return r;
+    }
     // the table of the matrices' own buffers, read by every fused apply variant
     NsIO* io = (fuse.in || fuse.out_w) ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
 
     std::vector<DescBatch> batches = make_batches(P, mats, ws, false, true, fuse);
     for (const DescBatch& B : batches) {
+        if (all_small(B)) continue;
         double e_in = 0, e_all = 0;
         for (int k = 0; k < B.n; ++k) {
+            if (B.d[k].fused & kFusedAll) continue;
             const double e = (double)B.d[k].rows * B.d[k].cols;
             e_all += e;
             if (B.d[k].fused & kFusedIn) e_in += e;
@@ -891,7 +964,7 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
     for (const DescBatch& B : batches) {
         double e_sep = 0;
         for (int k = 0; k < B.n; ++k)
-            if (!(B.d[k].fused & kFusedOutW)) e_sep += (double)B.d[k].rows * B.d[k].cols;
+            if (!(B.d[k].fused & (kFusedOutW | kFusedAll))) e_sep += (double)B.d[k].rows * B.d[k].cols;
         if (e_sep == 0) continue;
         Trace tr(K_MUON_FIN, st);
         r = sy.check(tr.done(launch_muon_finish(B, lr, fuse.wdecay, sc, o_scale, st), 0, e_sep * 14),

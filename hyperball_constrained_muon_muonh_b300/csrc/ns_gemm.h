@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "../../include/muonh.h"
+
 namespace muonh {
 
 enum NsMode { NS_GRAM = 0, NS_POLY = 1, NS_APPLY = 2 };
@@ -67,6 +69,20 @@ int pair_tiles_per_matrix(int mode, int M, int N);
 // two CTAs per tile in the pair kernel).
 constexpr int kUPartsPerTile1 = 8, kUPartsPerTilePair = 16;
 }  // namespace tc
+
+// The whole step of matrices with both sides <= 256 in one on-chip kernel
+// per CTA pair (ns_small.cu): MuonH (muon = false, r0 read) or plain Muon.
+struct SmallStepArgs {
+    float lr, beta, eps, wdecay;   // wdecay: plain Muon's 1 - lr*weight_decay
+    const float* coeffs;           // host array {a, b, c}
+    int ns_steps;
+    bool muon, nesterov;
+    int scale_mode;                // UpdateScale
+    const float* r0;               // device, indexed by caller position (MuonH)
+    uint32_t* status;
+};
+cudaError_t launch_small_step(const muonh_matrix_t* mats, const int* idx, int n, const SmallStepArgs& a,
+                              cudaStream_t st, int* launches);
 
 // fp32 CUDA-core GEMM for the accuracy-check mode: out = epilogue(A B) with
 // A M x K and B K x N.  a stored [m][k] (or [k][m] with a_km), b stored
