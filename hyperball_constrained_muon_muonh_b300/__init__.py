@@ -26,7 +26,7 @@ from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_NESTEROV, FLAG_SCALE_RMS
 
 NS_COEFFS = (3.4445, -4.7750, 2.0315)
 
-__all__ = ["MuonH", "Muon", "AdamW", "adamw_step", "capture_norms", "workspace_size", "step", "muon_step", "orthogonalize",
+__all__ = ["MuonH", "Muon", "AdamW", "ShardedMuonH", "partition", "exchange_weights", "adamw_step", "capture_norms", "workspace_size", "step", "muon_step", "orthogonalize",
            "orthogonalize_workspace_size", "get_status", "profile_read", "MuonHError", "NS_COEFFS"]
 
 
@@ -290,3 +290,6 @@ class AdamW:
             arr = self._arrays[ptrs] = adamw_array(self.params, grads, self.exp_avgs, self.exp_avg_sqs, self.bf16)
         self.t += 1
         adamw_step(arr, self.t, self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, stream)
+
+
+from .sharded import ShardedMuonH, exchange_weights, partition  # noqa: E402

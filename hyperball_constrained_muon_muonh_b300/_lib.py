@@ -39,7 +39,7 @@ EXPORTS = (
     "muonh_orthogonalize_workspace_size", "muonh_orthogonalize", "muonh_get_status",
     "muonh_status_string", "muonh_last_error", "muonh_version",
     "muonh_profile_enable", "muonh_profile_read", "muonh_launch_count",
-    "muonh_orthogonalize_static", "muon_step", "adamw_step",
+    "muonh_orthogonalize_static", "muon_step", "adamw_step", "muonh_partition",
 )
 
 STATIC_SCRATCH_BYTES = 80 * 1024 * 1024
@@ -101,6 +101,7 @@ def _load():
     lib.muonh_step.argtypes = [mp, I, P, F, F, I, fp, F, U32, P, SZ, P]
     lib.muon_step.argtypes = [mp, I, F, F, F, I, fp, F, U32, P, SZ, P]
     lib.adamw_step.argtypes = [ctypes.POINTER(AdamParamT), I, I, F, F, F, F, F, P]
+    lib.muonh_partition.argtypes = [mp, I, I, ctypes.POINTER(I)]
     lib.muonh_orthogonalize_workspace_size.argtypes = [I64, I64, U32, ctypes.POINTER(SZ)]
     lib.muonh_orthogonalize.argtypes = [P, P, I64, I64, I, fp, F, U32, P, SZ, P]
     lib.muonh_orthogonalize_static.argtypes = [P, P, I64, I64, I, fp, F, U32, P]

@@ -1056,6 +1056,33 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     return r;
 }
 
+int muonh_partition(const muonh_matrix_t* mats, int n, int world_size, int* owner_out) {
+    g_last_error.clear();
+    std::vector<int64_t> rc;
+    int r = check_shapes(mats, n, rc, false);
+    if (r) return r;
+    if (world_size < 1 || world_size > 65536) return fail(MUONH_ERR_INVALID_ARG, "world_size must be in [1, 65536]");
+    if (!owner_out) return fail(MUONH_ERR_INVALID_ARG, "owner_out is NULL");
+    std::vector<std::pair<double, int>> cost(n);
+    for (int i = 0; i < n; ++i) {
+        const double a = (double)rc[2 * i], b = (double)rc[2 * i + 1];
+        const double sd = std::min(a, b), ld = std::max(a, b);
+        cost[i] = {3 * sd * sd * ld + sd * sd * sd, i};
+    }
+    std::stable_sort(cost.begin(), cost.end(), [](const std::pair<double, int>& x, const std::pair<double, int>& y) {
+        return x.first > y.first;
+    });
+    std::vector<double> load(world_size, 0.0);
+    for (const auto& c : cost) {
+        int best = 0;
+        for (int k = 1; k < world_size; ++k)
+            if (load[k] < load[best]) best = k;
+        load[best] += c.first;
+        owner_out[c.second] = best;
+    }
+    return MUONH_OK;
+}
+
 int muonh_get_status(uint32_t* status_out, void* stream) {
     g_last_error.clear();
     if (!status_out) return fail(MUONH_ERR_INVALID_ARG, "status_out is NULL");

@@ -216,6 +216,18 @@ int muonh_orthogonalize_static(const float* in, float* out, int64_t rows, int64_
                                void* stream);
 
 /*
+ * Data-parallel sharding of the step across ranks (each matrix is an
+ * independent unit): owner_out[i] (host array of n ints) = the rank in
+ * [0, world_size) that steps matrix i.  Greedy longest-processing-time
+ * assignment by the Newton-Schulz cost 3 s^2 l + s^3 (s, l the short and long
+ * side): matrices in decreasing cost (ties: lower index first) each go to the
+ * least-loaded rank (ties: lower rank).  Deterministic, host only, reads
+ * only the shapes of mats.  After their steps, ranks exchange the updated
+ * weights (each matrix from its owner).
+ */
+int muonh_partition(const muonh_matrix_t* mats, int n, int world_size, int* owner_out);
+
+/*
  * Synchronises `stream`, then copies the current device's status word to
  * *status_out (host) and clears it.  Blocking.
  */

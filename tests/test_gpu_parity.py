@@ -328,3 +328,41 @@ def test_many_matrices_step():
     w0, r0, hist, status = _run_steps(work, 1, False, indices=idx)
     assert status == 0
     _check_step(work, w0, r0, hist, False, idx=idx)
+
+
+def _sharded_world1(port, result):
+    import os
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
+    try:
+        import hyperball_constrained_muon_muonh_b300 as mh_
+        work = wl.ragged([(256, 384), (384, 256), (512, 512), (96, 100)])
+        wa, wb = work.weights("cuda"), work.weights("cuda")
+        a = mh_.ShardedMuonH(wa, lr=work.lr, beta=work.beta)
+        b = mh_.MuonH(wb, lr=work.lr, beta=work.beta)
+        for t in range(2):
+            gs = work.grads(t, "cuda")
+            a.step(gs)
+            b.step(gs)
+        torch.cuda.synchronize()
+        result[0] = int(all(torch.equal(x, y) for x, y in zip(wa, wb)) and set(a.owners) == {0})
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sharded_world_size_1_equals_unsharded():
+    # one rank owns every matrix: the sharded step is the plain step, bit for bit
+    # (several ranks on one GPU would wait on one another; the exchange across
+    # ranks is tested with gloo on CPU)
+    import socket
+    import torch.multiprocessing as tmp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = tmp.get_context("spawn")
+    result = ctx.Manager().dict()
+    tmp.start_processes(_sharded_world1, args=(port, result), nprocs=1, start_method="spawn", join=True)
+    assert result.get(0) == 1
