@@ -330,7 +330,7 @@ def test_many_matrices_step():
     _check_step(work, w0, r0, hist, False, idx=idx)
 
 
-def _sharded_world1(port, result):
+def _sharded_world1(rank, port, result):
     import os
     import torch.distributed as dist
     os.environ["MASTER_ADDR"] = "127.0.0.1"
