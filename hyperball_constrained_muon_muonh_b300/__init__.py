@@ -20,7 +20,8 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_NESTEROV, FLAG_SCALE_RMS, FLAG_SCALE_SHAPE,  # noqa: F401
+from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_GRAD_BF16, FLAG_NESTEROV, FLAG_SCALE_RMS,  # noqa: F401
+                   FLAG_SCALE_SHAPE,
                    FLAG_SYNC_DEBUG, STATUS_DEGENERATE_NORM, STATUS_KERNEL_TIMEOUT, STATUS_NONFINITE_INPUT,
                    MuonHError, check, lib)
 
@@ -44,8 +45,9 @@ def _check_tensor(t, name, dtype=torch.float32):
         raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
 
 
-def matrix_array(weights, grads=None, moms=None, bf16=None):
-    """Build the muonh_matrix_t array for a list of 2-D tensors."""
+def matrix_array(weights, grads=None, moms=None, bf16=None, grad_dtype=torch.float32):
+    """Build the muonh_matrix_t array for a list of 2-D tensors (gradients
+    bfloat16 when the step runs with MUONH_FLAG_GRAD_BF16)."""
     n = len(weights)
     arr = (_lib.MatrixT * n)()
     for i, w in enumerate(weights):
@@ -55,7 +57,7 @@ def matrix_array(weights, grads=None, moms=None, bf16=None):
         arr[i].w = w.data_ptr()
         arr[i].rows, arr[i].cols = w.shape
         if grads is not None:
-            _check_tensor(grads[i], f"grads[{i}]")
+            _check_tensor(grads[i], f"grads[{i}]", grad_dtype)
             arr[i].grad = grads[i].data_ptr()
         if moms is not None:
             _check_tensor(moms[i], f"moms[{i}]")
@@ -197,7 +199,9 @@ class MuonH:
         if arr is None:
             if len(self._arrays) >= 4:
                 self._arrays.clear()
-            arr = self._arrays[ptrs] = matrix_array(self.weights, grads, self.moms, self.bf16)
+            arr = self._arrays[ptrs] = matrix_array(
+                self.weights, grads, self.moms, self.bf16,
+                torch.bfloat16 if self.flags & FLAG_GRAD_BF16 else torch.float32)
         return arr
 
     def state_dict(self):
@@ -239,7 +243,9 @@ class Muon:
         if arr is None:
             if len(self._arrays) >= 4:
                 self._arrays.clear()
-            arr = self._arrays[ptrs] = matrix_array(self.weights, grads, self.moms, self.bf16)
+            arr = self._arrays[ptrs] = matrix_array(
+                self.weights, grads, self.moms, self.bf16,
+                torch.bfloat16 if self.flags & FLAG_GRAD_BF16 else torch.float32)
         return arr
 
 

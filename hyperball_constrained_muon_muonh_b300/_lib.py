@@ -30,6 +30,7 @@ FLAG_SYNC_DEBUG = 0x4
 FLAG_GEMM_1SM = 0x8
 FLAG_SCALE_SHAPE = 0x10
 FLAG_SCALE_RMS = 0x20
+FLAG_GRAD_BF16 = 0x40
 
 MAX_SIDE = 65536
 

@@ -54,6 +54,20 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, float4 v) {
 // With `io` set, the CTA of each matrix's first chunk records where the
 // matrix's input and weight are (NsIO, indexed by bucket-order position).
 // ---------------------------------------------------------------------------
+// Four gradient values at element e (a multiple of 4), fp32 or bf16 (the
+// bf16 values widen exactly to fp32).
+__device__ __forceinline__ float4 load_g4(const float* g, size_t e, bool bf16) {
+    if (!bf16) return __ldcs(reinterpret_cast<const float4*>(g + e));
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(g) + e));
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ float load_g1(const float* g, size_t e, bool bf16) {
+    if (!bf16) return g[e];
+    return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(g)[e] << 16);
+}
+
 // The Newton-Schulz input of one element: the new momentum v, or with
 // Nesterov momentum the look-ahead g + beta*v.
 __device__ __forceinline__ float ns_in(float v, float g, float beta, bool nesterov) {
@@ -62,7 +76,7 @@ __device__ __forceinline__ float ns_in(float v, float g, float beta, bool nester
 
 template <bool WRITE_XS>
 __device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, int r_end, float beta, bool nesterov,
-                                               float& acc) {
+                                               bool grad_bf16, float& acc) {
     const int cols = D.cols, ld = D.ld;
     if (ld == cols && (cols & 3) == 0) {
         // flat float4 stream; four vectors per thread in flight
@@ -72,7 +86,7 @@ __device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, in
         for (; e + 4 * kThreads * (U - 1) < e1; e += 4 * kThreads * U) {
             float4 g[U], m[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) g[u] = __ldcs(reinterpret_cast<const float4*>(D.g + e + 4 * kThreads * u));
+            for (int u = 0; u < U; ++u) g[u] = load_g4(D.g, e + 4 * kThreads * u, grad_bf16);
             if (D.m) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) m[u] = __ldcs(reinterpret_cast<const float4*>(D.m + e + 4 * kThreads * u));
@@ -95,7 +109,7 @@ __device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, in
             }
         }
         for (; e < e1; e += 4 * kThreads) {
-            const float4 g = __ldcs(reinterpret_cast<const float4*>(D.g + e));
+            const float4 g = load_g4(D.g, e, grad_bf16);
             float4 v = g;
             if (D.m) {
                 const float4 m = *reinterpret_cast<const float4*>(D.m + e);
@@ -116,7 +130,7 @@ __device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, in
         for (size_t e = threadIdx.x; e < n; e += kThreads) {
             const size_t r = r_begin + e / cols, c = e % cols;
             const size_t wi = r * cols + c, xi = r * ld + c;
-            const float g = D.g[wi];
+            const float g = load_g1(D.g, wi, grad_bf16);
             float m = g;
             if (D.m) { m = fmaf(beta, D.m[wi], m); D.m[wi] = m; }
             const float x = ns_in(m, g, beta, nesterov);
@@ -129,7 +143,7 @@ __device__ __forceinline__ void momentum_chunk(const MatDesc& D, int r_begin, in
 
 __global__ void __launch_bounds__(kThreads)
 momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restrict__ partials, NsIO* io,
-                bool nesterov) {
+                bool nesterov, bool grad_bf16) {
     __shared__ double red[kThreads / 32];
     const int chunk = b.chunk_begin + blockIdx.x;
     const int mi = find_matrix(b, chunk);
@@ -148,9 +162,9 @@ momentum_kernel(const __grid_constant__ DescBatch b, float beta, double* __restr
     const int r_end = min(D.rows, r_begin + cr);
     float acc = 0.f;
     if (D.fused & kFusedIn)
-        momentum_chunk<false>(D, r_begin, r_end, beta, nesterov, acc);
+        momentum_chunk<false>(D, r_begin, r_end, beta, nesterov, grad_bf16, acc);
     else
-        momentum_chunk<true>(D, r_begin, r_end, beta, nesterov, acc);
+        momentum_chunk<true>(D, r_begin, r_end, beta, nesterov, grad_bf16, acc);
     double s = block_sum<kThreads>((double)acc, red);
     if (threadIdx.x == 0) partials[chunk] = s;
 }
@@ -421,10 +435,10 @@ capture_norms_kernel(const __grid_constant__ DescBatch b, float* __restrict__ r0
 // host launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, NsIO* io, bool nesterov,
-                            cudaStream_t st) {
+                            bool grad_bf16, cudaStream_t st) {
     const int nblk = b.chunk_end - b.chunk_begin;
     if (nblk <= 0) return cudaSuccess;
-    momentum_kernel<<<nblk, kThreads, 0, st>>>(b, beta, partials, io, nesterov);
+    momentum_kernel<<<nblk, kThreads, 0, st>>>(b, beta, partials, io, nesterov, grad_bf16);
     return cudaGetLastError();
 }
 

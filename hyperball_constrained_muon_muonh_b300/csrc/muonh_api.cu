@@ -29,7 +29,7 @@
 namespace muonh {
 
 cudaError_t launch_momentum(const DescBatch& b, float beta, double* partials, NsIO* io, bool nesterov,
-                            cudaStream_t st);
+                            bool grad_bf16, cudaStream_t st);
 cudaError_t launch_momentum_finalize(const DescBatch& b, const double* partials, const Scalars& sc, float eps,
                                      int scale_mode, bool no_iterations, cudaStream_t st);
 cudaError_t launch_hyperball_norm(const DescBatch& b, float lr, double* partials, const float* o_scale,
@@ -652,7 +652,8 @@ int check_scalars(int ns_steps, const float* coeffs, float eps, uint32_t flags) 
         if (!std::isfinite(coeffs[i])) return fail(MUONH_ERR_INVALID_ARG, "ns_coeffs must be finite");
     if (!std::isfinite(eps) || eps < 0.f) return fail(MUONH_ERR_INVALID_ARG, "eps must be finite and >= 0");
     if (flags & ~(uint32_t)(MUONH_FLAG_FP32_CHECK | MUONH_FLAG_SYNC_DEBUG | MUONH_FLAG_GEMM_1SM |
-                            MUONH_FLAG_NESTEROV | MUONH_FLAG_SCALE_SHAPE | MUONH_FLAG_SCALE_RMS))
+                            MUONH_FLAG_NESTEROV | MUONH_FLAG_SCALE_SHAPE | MUONH_FLAG_SCALE_RMS |
+                            MUONH_FLAG_GRAD_BF16))
         return fail(MUONH_ERR_UNSUPPORTED, "unknown flag bits");
     if ((flags & MUONH_FLAG_SCALE_SHAPE) && (flags & MUONH_FLAG_SCALE_RMS))
         return fail(MUONH_ERR_UNSUPPORTED, "MUONH_FLAG_SCALE_SHAPE and MUONH_FLAG_SCALE_RMS exclude each other");
@@ -811,6 +812,7 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     // separate norm and apply passes.
     const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
     const bool nesterov = (flags & MUONH_FLAG_NESTEROV) != 0;
+    const bool grad_bf16 = (flags & MUONH_FLAG_GRAD_BF16) != 0;
     NsFuse fuse;
     // with Nesterov momentum the Newton-Schulz input is not M, so it is stored
     fuse.in = !check && !nesterov && ns_steps >= 1;
@@ -821,7 +823,8 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     fuse.scale_mode = scale_mode_of(flags);
     fuse.lr = lr;
     if (fuse.small) {
-        SmallStepArgs sa{lr, beta, eps, 1.f, ns_coeffs, ns_steps, false, nesterov, fuse.scale_mode, r0_dev, status};
+        SmallStepArgs sa{lr, beta, eps, 1.f, ns_coeffs, ns_steps, false, nesterov, grad_bf16, fuse.scale_mode, r0_dev,
+                         status};
         r = run_small_step(P, mats, sa, sy);
         if (r) return r;
     }
@@ -845,7 +848,9 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
                              18 * (elems(B, kFusedIn, false) - elems(B, kFusedAll, true));
         {
             Trace tr(K_MOMENTUM, st);
-            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, nesterov, st), 0, bytes), "momentum launch");
+            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, nesterov, grad_bf16, st), 0,
+                                 bytes - (grad_bf16 ? 2 * (elems(B, 0, false) - elems(B, kFusedAll, true)) : 0)),
+                         "momentum launch");
         }
         if (r) return r;
         {
@@ -914,6 +919,7 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
     // get it from muon_finish_kernel.
     const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
     const bool nesterov = (flags & MUONH_FLAG_NESTEROV) != 0;
+    const bool grad_bf16 = (flags & MUONH_FLAG_GRAD_BF16) != 0;
     NsFuse fuse;
     fuse.in = !check && !nesterov && ns_steps >= 1;
     fuse.out_w = !check && ns_steps >= 1;
@@ -924,8 +930,8 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
     fuse.lr = lr;
     fuse.wdecay = 1.f - lr * weight_decay;
     if (fuse.small) {
-        SmallStepArgs sa{lr, beta, eps, fuse.wdecay, ns_coeffs, ns_steps, true, nesterov, fuse.scale_mode, nullptr,
-                         status};
+        SmallStepArgs sa{lr, beta, eps, fuse.wdecay, ns_coeffs, ns_steps, true, nesterov, grad_bf16, fuse.scale_mode,
+                         nullptr, status};
         r = run_small_step(P, mats, sa, sy);
         if (r) return r;
     }
@@ -944,8 +950,8 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
         }
         {
             Trace tr(K_MOMENTUM, st);
-            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, nesterov, st), 0,
-                                 14 * e_in + 18 * (e_all - e_in)),
+            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, nesterov, grad_bf16, st), 0,
+                                 14 * e_in + 18 * (e_all - e_in) - (grad_bf16 ? 2 * e_all : 0)),
                          "momentum launch");
         }
         if (r) return r;
@@ -1033,7 +1039,8 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     const bool in_fused = (batches[0].d[0].fused & kFusedIn) != 0;
     {
         Trace tr(K_MOMENTUM, st);
-        r = sy.check(tr.done(launch_momentum(batches[0], 0.f, partials, io, false, st), 0, el * (in_fused ? 6 : 10)),
+        r = sy.check(tr.done(launch_momentum(batches[0], 0.f, partials, io, false, false, st), 0,
+                             el * (in_fused ? 6 : 10)),
                      "momentum launch");
     }
     if (r) return r;

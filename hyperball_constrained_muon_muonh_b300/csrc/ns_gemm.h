@@ -77,6 +77,7 @@ struct SmallStepArgs {
     const float* coeffs;           // host array {a, b, c}
     int ns_steps;
     bool muon, nesterov;
+    bool grad_bf16;                // gradients are bf16 bit patterns
     int scale_mode;                // UpdateScale
     const float* r0;               // device, indexed by caller position (MuonH)
     uint32_t* status;

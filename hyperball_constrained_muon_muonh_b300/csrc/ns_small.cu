@@ -71,7 +71,7 @@ struct SmallParams {
     int muon;                      // 1: plain Muon update, 0: MuonH (hyperball)
     int nesterov;
     int scale_mode;                // UpdateScale
-    int pad_;
+    int grad_bf16;                 // gradients are bf16 bit patterns
     const float* r0;
     uint32_t* status;
 };
@@ -300,7 +300,15 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
                 const size_t base = (size_t)i * C + j0;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const float4 g = __ldcs(reinterpret_cast<const float4*>(D.g + base) + c);
+                    float4 g;
+                    if (p.grad_bf16) {
+                        const uint2 u =
+                            __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(D.g) + base) + c);
+                        g = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+                    } else {
+                        g = __ldcs(reinterpret_cast<const float4*>(D.g + base) + c);
+                    }
                     const float4 mv = *reinterpret_cast<const float4*>(D.m + base + 4 * c);
                     gv[4 * c] = g.x; gv[4 * c + 1] = g.y; gv[4 * c + 2] = g.z; gv[4 * c + 3] = g.w;
                     x[4 * c] = mv.x; x[4 * c + 1] = mv.y; x[4 * c + 2] = mv.z; x[4 * c + 3] = mv.w;
@@ -317,7 +325,9 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
                     const int j = j0 + t;
                     const bool ok = row_ok && j < l;
                     const size_t e = widx(tall, C, i, ok ? j : 0);
-                    gv[t] = ok ? __ldcs(D.g + e) : 0.f;
+                    gv[t] = !ok ? 0.f
+                                : p.grad_bf16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(D.g)[e] << 16)
+                                              : __ldcs(D.g + e);
                     x[t] = ok ? D.m[e] : 0.f;
                 }
 #pragma unroll
@@ -524,6 +534,7 @@ cudaError_t launch_small_step(const muonh_matrix_t* mats, const int* idx, int n,
     p.muon = a.muon ? 1 : 0;
     p.nesterov = a.nesterov ? 1 : 0;
     p.scale_mode = a.scale_mode;
+    p.grad_bf16 = a.grad_bf16 ? 1 : 0;
     p.r0 = a.r0;
     p.status = a.status;
     for (int b0 = 0; b0 < n; b0 += kMaxPerLaunch) {

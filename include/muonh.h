@@ -78,6 +78,8 @@ extern "C" {
 #define MUONH_FLAG_SCALE_SHAPE 0x10u /* O <- sqrt(max(1, rows/cols)) * O before the update */
 #define MUONH_FLAG_SCALE_RMS   0x20u /* O <- 0.2 * sqrt(max(rows, cols)) * O before the update
                                         (not together with MUONH_FLAG_SCALE_SHAPE) */
+#define MUONH_FLAG_GRAD_BF16   0x40u /* each muonh_matrix_t.grad points to bfloat16 values (bit
+                                        patterns, same shape, 16-byte aligned) instead of fp32 */
 
 /* One weight matrix and its optimizer state.  All device pointers, fp32
  * row-major rows x cols (row stride = cols elements), 16-byte aligned.

@@ -113,3 +113,43 @@ def test_scale_flags_exclude_each_other():
     with pytest.raises(mh.MuonHError):
         opt = mh.MuonH(w, flags=SHAPE | RMS)
         opt.step([torch.ones(8, 8, device="cuda")])
+
+
+@pytest.mark.parametrize("optimizer", ["muonh", "muon"])
+def test_bf16_gradients(optimizer):
+    # gradients handed over as bf16 (MUONH_FLAG_GRAD_BF16); the oracle gets the same values widened
+    work = wl.ragged(SHAPES + [(256, 256), (250, 100)])
+    ws = work.weights("cuda")
+    flags = 0x40
+    if optimizer == "muonh":
+        opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, flags=flags)
+        r0 = opt.r0.cpu().numpy().astype(np.float64)
+    else:
+        opt = mh.Muon(ws, lr=work.lr, beta=work.beta, weight_decay=0.1, flags=flags)
+    lr, beta, eps = _f32(work.lr), _f32(work.beta), _f32(work.eps)
+    coeffs = tuple(_f32(c) for c in work.coeffs)
+    for t in range(2):
+        gb = [g.to(torch.bfloat16) for g in work.grads(t, "cuda")]
+        w0 = [w.cpu().numpy() for w in ws]
+        m0 = [m.cpu().numpy() for m in opt.moms]
+        opt.step(gb)
+        torch.cuda.synchronize()
+        g0 = [g.float().cpu().numpy() for g in gb]
+        if optimizer == "muonh":
+            out = om.muonh_step(w0, g0, m0, r0, lr, beta, work.ns_steps, coeffs, eps)
+        else:
+            out = om.muon_step(w0, g0, m0, lr, beta, _f32(0.1), work.ns_steps, coeffs, eps)
+        for i in range(len(ws)):
+            m_or = out["m"][i]
+            assert np.all(np.abs(opt.moms[i].cpu().numpy() - m_or) <= 2 * np.spacing(np.abs(m_or).astype(np.float32)))
+            w = ws[i].cpu().numpy().astype(np.float64)
+            o = out["o"][i]
+            if optimizer == "muonh":
+                u = w0[i].astype(np.float64) - lr * o
+                bound = 2 * lr * 3e-2 * np.linalg.norm(o) / np.linalg.norm(u) + 1e-6
+                err = np.linalg.norm(w - out["w"][i]) / np.linalg.norm(out["w"][i])
+            else:
+                bound = lr * 3e-2 * np.linalg.norm(o) + 1e-6 * np.linalg.norm(out["w"][i])
+                err = np.linalg.norm(w - out["w"][i])
+            assert err <= bound, f"{optimizer} step {t} matrix {i}: {err:.3e} > {bound:.3e}"
+    assert mh.get_status() == 0
