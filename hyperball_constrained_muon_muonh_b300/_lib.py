@@ -28,6 +28,7 @@ FLAG_FP32_CHECK = 0x1
 FLAG_NESTEROV = 0x2
 FLAG_SYNC_DEBUG = 0x4
 FLAG_GEMM_1SM = 0x8
+FLAG_GEMM_QUAD = 0x80
 FLAG_SCALE_SHAPE = 0x10
 FLAG_SCALE_RMS = 0x20
 FLAG_GRAD_BF16 = 0x40

@@ -130,11 +130,12 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint6
         : "memory");
 }
 
-// arrive once on the barrier at the same offset in both CTAs of the pair
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+// arrive once on the barrier at the same offset in every CTA of `mask`
+// (default: both CTAs of the pair 0/1)
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask = 3) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"((uint16_t)3)
+        "h"(mask)
         : "memory");
 }
 

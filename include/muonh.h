@@ -71,6 +71,9 @@ extern "C" {
 #define MUONH_FLAG_GEMM_1SM    0x8u  /* Newton-Schulz GEMMs on one SM per 128x256 tile instead of the
                                         default CTA pair per 256x256 tile (same results up to bf16
                                         rounding order; for comparison and small problems) */
+#define MUONH_FLAG_GEMM_QUAD   0x80u /* Newton-Schulz GEMMs on clusters of two CTA pairs that fetch the
+                                        operand rows both pairs' tiles share once, multicast to both
+                                        (same results bit for bit as the CTA-pair kernel) */
 /* Step variants the pages do not name (muonh_step and muon_step; ignored by
  * muonh_orthogonalize): */
 #define MUONH_FLAG_NESTEROV    0x2u  /* Newton-Schulz input G + beta*M_new (Nesterov look-ahead)

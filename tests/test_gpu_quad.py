@@ -1,0 +1,101 @@
+"""The 4-SM Newton-Schulz GEMM (MUONH_FLAG_GEMM_QUAD) against the CTA-pair
+kernel, bit for bit.
+
+Both kernels walk the same list of 256 x 256 pair tiles and issue the same
+tcgen05 MMAs over the same shared-memory layout in the same K order; the
+4-SM kernel only changes who fetches an operand (one TMA multicast for the
+rows two tiles share).  So every output -- O, the momentum, W, the bf16
+copy -- must equal the pair kernel's exactly.  The shapes cover: symmetric
+Gram/polynomial tile lists with even and odd counts (odd: pair 1 recomputes
+a tile and writes nothing), the wide apply (tiles that share B), the tall
+apply (tiles that share A), super-tiles that straddle a row, a column or a
+matrix boundary (no sharing), and buckets of several matrices.  The oracle
+parity of the 4-SM path itself runs in test_gpu_parity.py and
+test_gpu_muon.py (mode "quad").
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import muonh_workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import hyperball_constrained_muon_muonh_b300 as mh
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mh.get_status()
+    yield
+    assert mh.get_status() & mh.STATUS_KERNEL_TIMEOUT == 0
+
+
+# (rows, cols): short side s -> s/256 pair tiles per side
+#   2048^2: 36 Gram tiles (even), wide apply 8 x 8
+#   640x384: 3 Gram tiles (odd), apply 2 x 3 over a ragged 128-row tail
+#   768x1280, 1280x768: apply 3 x 5, super-tiles across column / row ends
+#   129x520, 520x129: one tile per launch (only a stand-in partner)
+#   6144x2048, 2048x6144: the tall and wide MLP shapes
+SHAPES = [(2048, 2048), (640, 384), (384, 640), (768, 1280), (1280, 768), (129, 520), (520, 129),
+          (6144, 2048), (2048, 6144), (1000, 1000)]
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int32).numpy()
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_orthogonalize_quad_equals_pair(shape):
+    g = wl.ragged([shape]).grad(0, 0, "cuda")
+    o_pair = mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7, flags=0)
+    o_quad = mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7, flags=mh.FLAG_GEMM_QUAD)
+    torch.cuda.synchronize()
+    assert mh.get_status() == 0
+    assert np.array_equal(_bits(o_pair), _bits(o_quad)), f"{shape}"
+
+
+def _step_states(work, steps, flags, optimizer="muonh", wd=0.0):
+    ws = work.weights("cuda")
+    if optimizer == "muonh":
+        opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps, ns_coeffs=work.coeffs,
+                       eps=work.eps, bf16_copies=True, flags=flags)
+    else:
+        opt = mh.Muon(ws, lr=work.lr, beta=work.beta, weight_decay=wd, ns_steps=work.ns_steps,
+                      ns_coeffs=work.coeffs, eps=work.eps, bf16_copies=True, flags=flags)
+    for t in range(steps):
+        opt.step(work.grads(t, "cuda"))
+    torch.cuda.synchronize()
+    return ([_bits(w) for w in ws], [_bits(m) for m in opt.moms],
+            [opt.bf16[i].detach().cpu().view(torch.int16).numpy() for i in range(len(ws))])
+
+
+# several matrices per bucket: super-tiles that pair the last tile of one
+# matrix with the first of the next
+BUCKETS = [(512, 512)] * 3 + [(384, 1024)] * 5 + [(1024, 384)] * 3 + [(2048, 768)] * 2 + [(300, 200), (77, 77)]
+
+
+@pytest.mark.parametrize("optimizer", ["muonh", "muon"])
+@pytest.mark.parametrize("extra", [0, 1 << 1])   # plain, Nesterov (the first apply reads its own input)
+def test_step_quad_equals_pair(optimizer, extra):
+    work = wl.ragged(BUCKETS)
+    a = _step_states(work, 2, extra, optimizer, wd=0.1)
+    b = _step_states(work, 2, extra | mh.FLAG_GEMM_QUAD, optimizer, wd=0.1)
+    assert mh.get_status() == 0
+    for k in range(len(BUCKETS)):
+        for part in range(3):
+            assert np.array_equal(a[part][k], b[part][k]), f"matrix {k} {BUCKETS[k]} part {part}"
+
+
+def test_step_quad_equals_pair_qwen3_layer():
+    work = wl.qwen3_layer()
+    a = _step_states(work, 2, 0)
+    b = _step_states(work, 2, mh.FLAG_GEMM_QUAD)
+    assert mh.get_status() == 0
+    for k in range(len(work.shapes)):
+        for part in range(3):
+            assert np.array_equal(a[part][k], b[part][k]), f"matrix {k} part {part}"
