@@ -243,8 +243,9 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--gemm", default="pair", choices=["pair", "quad", "1sm"],
-                    help="Newton-Schulz GEMM kernel: CTA pair per 256x256 tile, clusters of two pairs "
+    ap.add_argument("--gemm", default="pair", choices=["pair", "pair_one_step", "quad", "1sm"],
+                    help="Newton-Schulz GEMM kernel: CTA pair per 256x256 tile (two K steps per pipeline "
+                         "stage where the shape allows; pair_one_step: always one), clusters of two pairs "
                          "sharing an operand fetch, or one SM per 128x256 tile")
     ap.add_argument("--optimizer", default="muonh", choices=["muonh", "muon", "adamw"],
                     help="muon: plain Muon (decoupled weight decay 0.1, no hyperball), the baseline MuonH is "
@@ -283,7 +284,8 @@ def main():
 
     ws = work.weights(dev)
     grads = [work.grads(t, dev) for t in range(2)]   # two gradient sets, alternated
-    gemm_flags = {"pair": 0, "quad": mh.FLAG_GEMM_QUAD, "1sm": mh.FLAG_GEMM_1SM}[args.gemm]
+    gemm_flags = {"pair": 0, "pair_one_step": mh.FLAG_GEMM_ONE_STEP, "quad": mh.FLAG_GEMM_QUAD,
+                  "1sm": mh.FLAG_GEMM_1SM}[args.gemm]
     if args.optimizer == "adamw":
         ws = [w.reshape(-1) for w in ws]
         grads = [[g.reshape(-1) for g in gs] for gs in grads]
@@ -428,7 +430,9 @@ def main():
                    "eps": work.eps, "state": "fp32 W/M/G + bf16 W copy; NS bf16 operands, fp32 state",
                    "l2": "inputs larger than L2 (about 20 GB of optimizer state touched per step)",
                    "parallelism": f"replica x{world}",
-                   "ns_gemm": {"pair": "2-SM pair 256x256 tiles", "quad": "4-SM clusters: two pair tiles, shared operand multicast",
+                   "ns_gemm": {"pair": "2-SM pair 256x256 tiles, two K steps (32 KB TMA boxes) per stage",
+                               "pair_one_step": "2-SM pair 256x256 tiles, one K step (16 KB TMA boxes) per stage",
+                               "quad": "4-SM clusters: two pair tiles, shared operand multicast",
                                "1sm": "1-SM 128x256 tiles"}[args.gemm],
                    "optimizer": {"muon": "muon (weight decay 0.1)",
                                  "adamw": f"adamw (betas {ADAMW_BETAS}, eps {ADAMW_EPS}, weight decay {ADAMW_WD})"

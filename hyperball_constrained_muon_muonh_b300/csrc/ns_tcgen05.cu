@@ -509,6 +509,32 @@ constexpr int B2_BYTES = (BN / 2) * BK * 2;           // 16 KB: this CTA's 128 r
 constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
 constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + 1024 + 256 + EPI_WARPS * ST_FLOATS * 4;
 
+// Pipeline shape of the pair kernel: KPS K steps of BK per stage.  Alone,
+// TMA moves about 56 bytes per SM clock into shared memory with 16 KB boxes
+// and about 80 with 32 KB boxes (8 KB boxes: about 40), while a 256 x 256
+// pair tile consumes 64 bytes per clock per SM at the full MMA rate.  A
+// two-step stage is loaded by one 32 KB box per operand (4-D view of a
+// K-major operand, 5-D view of an MN-major one); within it, K step j sits at
+// +j * 16 KB in the layout of a one-step stage, so the MMA descriptors are
+// those of the one-step pipeline plus that offset.  Inside the GEMM the two
+// shapes deliver about the same bytes per clock (the MMA's own shared-memory
+// reads share the SM's bandwidth), and the three-stage ring holds less in
+// flight, so the host takes two steps only where that measured faster.
+template <int KPS>
+struct PairPipe {
+    static constexpr int STAGES = 6 / KPS;
+    static constexpr int A_STEP = BM * BK * 2;          // 16 KB: one K step of this CTA's A rows
+    static constexpr int B_STEP = (BN / 2) * BK * 2;    // 16 KB: one K step of this CTA's B rows
+    static constexpr int A_BYTES = KPS * A_STEP;
+    static constexpr int B_BYTES = KPS * B_STEP;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+};
+static_assert(PairPipe<1>::STAGES * PairPipe<1>::STAGE_BYTES == STAGES2 * STAGE2_BYTES, "pipelines share smem size");
+static_assert(PairPipe<2>::STAGES * PairPipe<2>::STAGE_BYTES == STAGES2 * STAGE2_BYTES, "pipelines share smem size");
+static_assert(PairPipe<1>::A_BYTES == PairPipe<1>::B_BYTES && PairPipe<2>::A_BYTES == PairPipe<2>::B_BYTES &&
+                  PairPipe<1>::A_STEP == PairPipe<1>::B_STEP,
+              "a diagonal tile reads B from A's buffer");
+
 // TMA load into this CTA's shared memory, completing on a barrier that may
 // belong to the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int x,
@@ -517,6 +543,22 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int c0,
+                                                 int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int c0,
+                                                 int c1, int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
 }
 __host__ __device__ constexpr uint32_t idesc_pair(bool a_mn_major, bool b_mn_major) {
@@ -547,10 +589,18 @@ __device__ __forceinline__ void pair_coords(const GemmParams& p, int local, int&
     nj = m + local;
 }
 
-template <int MODE, int VAR>
+// KPS = 1: 3-D maps, K-major box 64 x 128, MN-major box 64 x 64 (two per
+// operand and step).  KPS = 2: K-major 4-D map {64 k, rows, K/64, G}, box
+// {64, 128, 2, 1}; MN-major 5-D map {64 m, 64 k, M/64, K/64, G}, box
+// {64, 64, 2, 2, 1}.  Both give, per K step, 128 rows of 128 bytes in the
+// 128B-swizzled layout (MN-major: two 64-wide chunks 8 KB apart).
+template <int MODE, int VAR, int KPS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ GemmParams p) {
+    using Pipe = PairPipe<KPS>;
+    constexpr int STAGES2 = Pipe::STAGES, A2_BYTES = Pipe::A_BYTES, B2_BYTES = Pipe::B_BYTES;
+    constexpr int STAGE2_BYTES = Pipe::STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* smem_a = smem;
@@ -595,6 +645,7 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
 
     const int total = p.G * p.tiles_per_mat;
     const int num_kb = (p.K + BK - 1) / BK;
+    const int num_ks = (num_kb + KPS - 1) / KPS;
     const int cid = (int)cluster_id(), ncl = (int)cluster_count();
 
     if (warp == 0 && lane == 0) {
@@ -608,13 +659,31 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             pair_coords(p, t - g * p.tiles_per_mat, mp, nj);
             const int row_a = mp * 2 * BM + (int)rank * BM;       // this CTA's 128 rows of A
             const int row_b = nj * BN + (int)rank * (BN / 2);     // this CTA's 128 rows (N) of B
-            for (int kb = 0; kb < num_kb; ++kb) {
+            // diagonal tile of a symmetric product: this CTA's B rows are its A
+            // rows (same operand tensor), so B is not fetched
+            const bool diag = MODE != NS_APPLY && mp == nj;
+            for (int ks = 0; ks < num_ks; ++ks) {
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
                 const uint32_t fb_local = full0 + 8 * stage;
                 const uint32_t fb = map_to_rank(fb_local, 0);
-                if (leader) mbar_expect_tx(fb_local, 2 * STAGE2_BYTES);
+                if (leader) mbar_expect_tx(fb_local, diag ? 2 * A2_BYTES : 2 * STAGE2_BYTES);
                 const uint32_t sa = smem_u32(smem_a + stage * A2_BYTES);
                 const uint32_t sb = smem_u32(smem_b + stage * B2_BYTES);
+                if (KPS == 2) {
+                    // K steps 2ks and 2ks+1 (the second is zero-filled past K)
+                    if (!p.a_mn)
+                        tma_load_4d_pair(sa, &tm_a, fb, 0, row_a, 2 * ks, g);
+                    else
+                        tma_load_5d_pair(sa, &tm_a, fb, 0, 0, row_a / 64, 2 * ks, g);
+                    if (diag) {
+                    } else if (!p.b_mn)
+                        tma_load_4d_pair(sb, &tm_b, fb, 0, row_b, 2 * ks, g);
+                    else
+                        tma_load_5d_pair(sb, &tm_b, fb, 0, 0, row_b / 64, 2 * ks, g);
+                    if (++stage == STAGES2) { stage = 0; phase ^= 1; }
+                    continue;
+                }
+                const int kb = ks;
                 if (!p.a_mn) {
                     tma_load_3d_pair(sa, &tm_a, fb, kb * BK, row_a, g);
                 } else {
@@ -622,7 +691,8 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
                     for (int c = 0; c < BM / 64; ++c)
                         tma_load_3d_pair(sa + c * (64 * BK * 2), &tm_a, fb, row_a + c * 64, kb * BK, g);
                 }
-                if (!p.b_mn) {
+                if (diag) {
+                } else if (!p.b_mn) {
                     tma_load_3d_pair(sb, &tm_b, fb, kb * BK, row_b, g);
                 } else {
 #pragma unroll
@@ -652,17 +722,32 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int t = cid; t < total && ok; t += ncl) {
+            bool diag = false;
+            if (MODE != NS_APPLY) {
+                const int g = t / p.tiles_per_mat;
+                int mp, nj;
+                pair_coords(p, t - g * p.tiles_per_mat, mp, nj);
+                diag = mp == nj;
+            }
+            // B of a diagonal tile is read from A's buffer (same layout and size)
+            const uint64_t b_base = diag ? a_desc0 : b_desc0;
+            const int b_stage = diag ? A2_BYTES : B2_BYTES;
             if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int ks = 0; ks < num_ks; ++ks) {
                 if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t ad = a_desc0 + (uint64_t)(stage * (A2_BYTES >> 4));
-                const uint64_t bd = b_desc0 + (uint64_t)(stage * (B2_BYTES >> 4));
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_bf16_pair(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc, (kb | kk) ? 1u : 0u);
+                for (int j = 0; j < KPS; ++j) {
+                    const int kb = ks * KPS + j;
+                    if (KPS > 1 && kb >= num_kb) break;
+                    const uint64_t ad = a_desc0 + (uint64_t)((stage * A2_BYTES + j * Pipe::A_STEP) >> 4);
+                    const uint64_t bd = b_base + (uint64_t)((stage * b_stage + j * Pipe::B_STEP) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_bf16_pair(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc, (kb | kk) ? 1u : 0u);
+                }
                 mma_commit_pair(empty0 + 8 * stage);
                 if (++stage == STAGES2) { stage = 0; phase ^= 1; }
             }
@@ -993,6 +1078,36 @@ static bool encode_bf16_3d(CUtensorMap* map, const void* base, int cols, int row
     return r == CUDA_SUCCESS;
 }
 
+// Two-K-step boxes (pair kernel, KPS = 2).  K-major operand [G][rows][ld],
+// K valid columns (K % 64 == 0): {64 k, rows, K/64, G}, box {64, 128, 2, 1}.
+// MN-major operand [G][K][ld], `cols` valid columns (cols % 64 == 0, K % 64
+// == 0): {64 m, 64 k, cols/64, K/64, G}, box {64, 64, 2, 2, 1}.  Every
+// coordinate past an extent reads zeros.
+static bool encode_bf16_kmajor_2step(CUtensorMap* map, const void* base, int K, int rows, int G, int ld) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(K / 64), (cuuint64_t)G};
+    cuuint64_t strides[3] = {(cuuint64_t)ld * 2, 128, (cuuint64_t)ld * 2 * (cuuint64_t)rows};
+    cuuint32_t box[4] = {64, (cuuint32_t)BM, 2, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+static bool encode_bf16_mnmajor_2step(CUtensorMap* map, const void* base, int cols, int K, int G, int ld) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[5] = {64, 64, (cuuint64_t)(cols / 64), (cuuint64_t)(K / 64), (cuuint64_t)G};
+    cuuint64_t strides[4] = {(cuuint64_t)ld * 2, 128, (cuuint64_t)ld * 2 * 64, (cuuint64_t)ld * 2 * (cuuint64_t)K};
+    cuuint32_t box[5] = {64, 64, 2, 2, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 static int sm_count() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -1016,7 +1131,7 @@ int pair_tiles_per_matrix(int mode, int M, int N) {
     return cnt;
 }
 
-template <int MODE, int VAR>
+template <int MODE, int VAR, int KPS>
 static int max_pair_clusters() {
     static int cached = 0;
     if (cached) return cached;
@@ -1032,7 +1147,7 @@ static int max_pair_clusters() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair::ns_gemm_pair_kernel<MODE, VAR>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, pair::ns_gemm_pair_kernel<MODE, VAR, KPS>, &cfg) != cudaSuccess || n <= 0) {
         (void)cudaGetLastError();
         n = sm_count() / 2;
     }
@@ -1040,19 +1155,19 @@ static int max_pair_clusters() {
     return n;
 }
 
-template <int MODE, int VAR>
+template <int MODE, int VAR, int KPS>
 static cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, long long total,
                                cudaStream_t st) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(pair::ns_gemm_pair_kernel<MODE, VAR>,
+        cudaError_t e = cudaFuncSetAttribute(pair::ns_gemm_pair_kernel<MODE, VAR, KPS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM2_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int maxc = max_pair_clusters<MODE, VAR>();
+    const int maxc = max_pair_clusters<MODE, VAR, KPS>();
     const long long clusters = total < maxc ? total : maxc;
-    pair::ns_gemm_pair_kernel<MODE, VAR><<<(int)(2 * clusters), NUM_THREADS, pair::SMEM2_BYTES, st>>>(ta, tb, p);
+    pair::ns_gemm_pair_kernel<MODE, VAR, KPS><<<(int)(2 * clusters), NUM_THREADS, pair::SMEM2_BYTES, st>>>(ta, tb, p);
     return cudaGetLastError();
 }
 
@@ -1113,15 +1228,16 @@ static cudaError_t launch_quad(const CUtensorMap& ta, const CUtensorMap& tb, con
 }
 
 int quad_cluster_capacity() { return max_quad_clusters<NS_GRAM, 0>(); }
-int pair_cluster_capacity() { return max_pair_clusters<NS_GRAM, 0>(); }
+int pair_cluster_capacity() { return max_pair_clusters<NS_GRAM, 0, 2>(); }
 
 template <int KIND>
 static cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, long long total,
                             cudaStream_t st) {
 #define MUONH_LAUNCH(M_, V_)                                                                      \
-    (KIND == kGemmQuad   ? launch_quad<M_, V_>(ta, tb, p, total, st)                               \
-     : KIND == kGemmPair ? launch_pair<M_, V_>(ta, tb, p, total, st)                               \
-                         : launch_single<M_, V_>(ta, tb, p, total, st))
+    (KIND == kGemmQuad         ? launch_quad<M_, V_>(ta, tb, p, total, st)                         \
+     : KIND == kGemmPair       ? launch_pair<M_, V_, 2>(ta, tb, p, total, st)                      \
+     : KIND == kGemmPairStep1  ? launch_pair<M_, V_, 1>(ta, tb, p, total, st)                      \
+                               : launch_single<M_, V_>(ta, tb, p, total, st))
     if (p.mode == NS_GRAM) return MUONH_LAUNCH(NS_GRAM, 0);
     if (p.mode == NS_POLY) return MUONH_LAUNCH(NS_POLY, 0);
     switch (p.variant) {
@@ -1154,16 +1270,38 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
     if ((p.variant & NS_OUT_W) && !p.mflags) { *why = "apply variant without status flags"; return cudaErrorInvalidValue; }
     if ((p.variant & NS_OUT_U) && (p.variant & NS_OUT_W)) { *why = "conflicting apply variants"; return cudaErrorInvalidValue; }
     if (p.variant != 0 && (p.N & 3) != 0) { *why = "apply variant needs a row length that is a multiple of 4"; return cudaErrorInvalidValue; }
-    if (kind != kGemmSingle && kind != kGemmPair && kind != kGemmQuad) { *why = "unknown GEMM kernel"; return cudaErrorInvalidValue; }
+    if (kind != kGemmSingle && kind != kGemmPair && kind != kGemmPairStep1 && kind != kGemmQuad) {
+        *why = "unknown GEMM kernel";
+        return cudaErrorInvalidValue;
+    }
+    // two-K-step stages need every box coordinate past the data to be an
+    // extent of the view: K, and the contiguous extent of an MN-major operand,
+    // multiples of 64
+    // Measured on the 2B set (cycles per K step, two-step vs one-step
+    // stages): tall Gram 595 vs 653, wide Gram 660 vs 663, polynomial 801
+    // vs 745, apply 635-675 vs 636-669.  Three 64 KB stages keep less data
+    // in flight than six 32 KB ones, which only the tall Gram's four 8 KB
+    // MN-major boxes per step outweigh; the other launches keep one step.
+    if (kind == kGemmPair &&
+        !(p.mode == NS_GRAM && p.a_mn && (p.K % 64) == 0 && (p.M % 64) == 0 && (p.N % 64) == 0))
+        kind = kGemmPairStep1;
     const bool multi = kind != kGemmSingle;
     const int a_box = kind == kGemmQuad ? 64 : BM;
-    const int b_box = kind == kGemmQuad ? 64 : kind == kGemmPair ? BN / 2 : BN;
+    const int b_box = kind == kGemmQuad ? 64 : kind == kGemmPairStep1 ? BN / 2 : BN;
     CUtensorMap ta, tb;
-    const bool oka = p.a_mn ? encode_bf16_3d(&ta, a_op, p.M, p.K, p.G, a_ld, 64)
-                            : encode_bf16_3d(&ta, a_op, p.K, p.M, p.G, a_ld, a_box);
+    bool oka, okb;
+    if (kind == kGemmPair) {
+        oka = p.a_mn ? encode_bf16_mnmajor_2step(&ta, a_op, p.M, p.K, p.G, a_ld)
+                     : encode_bf16_kmajor_2step(&ta, a_op, p.K, p.M, p.G, a_ld);
+        okb = p.b_mn ? encode_bf16_mnmajor_2step(&tb, b_op, p.N, p.K, p.G, b_ld)
+                     : encode_bf16_kmajor_2step(&tb, b_op, p.K, p.N, p.G, b_ld);
+    } else {
+        oka = p.a_mn ? encode_bf16_3d(&ta, a_op, p.M, p.K, p.G, a_ld, 64)
+                     : encode_bf16_3d(&ta, a_op, p.K, p.M, p.G, a_ld, a_box);
+        okb = p.b_mn ? encode_bf16_3d(&tb, b_op, p.N, p.K, p.G, b_ld, 64)
+                     : encode_bf16_3d(&tb, b_op, p.K, p.N, p.G, b_ld, b_box);
+    }
     if (!oka) { *why = "cuTensorMapEncodeTiled (A) failed"; return cudaErrorInvalidValue; }
-    const bool okb = p.b_mn ? encode_bf16_3d(&tb, b_op, p.N, p.K, p.G, b_ld, 64)
-                            : encode_bf16_3d(&tb, b_op, p.K, p.N, p.G, b_ld, b_box);
     if (!okb) { *why = "cuTensorMapEncodeTiled (B) failed"; return cudaErrorInvalidValue; }
     if (multi) {
         p.tiles_m = (p.M + 2 * BM - 1) / (2 * BM);
@@ -1176,11 +1314,12 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
     }
     const long long total = (long long)p.G * p.tiles_per_mat;
     if (total <= 0) return cudaSuccess;
-    cudaError_t e = kind == kGemmQuad   ? dispatch<kGemmQuad>(ta, tb, p, total, st)
-                    : kind == kGemmPair ? dispatch<kGemmPair>(ta, tb, p, total, st)
-                                        : dispatch<kGemmSingle>(ta, tb, p, total, st);
+    cudaError_t e = kind == kGemmQuad        ? dispatch<kGemmQuad>(ta, tb, p, total, st)
+                    : kind == kGemmPair      ? dispatch<kGemmPair>(ta, tb, p, total, st)
+                    : kind == kGemmPairStep1 ? dispatch<kGemmPairStep1>(ta, tb, p, total, st)
+                                             : dispatch<kGemmSingle>(ta, tb, p, total, st);
     if (e != cudaSuccess)
-        *why = kind == kGemmQuad ? "4-SM GEMM launch failed" : kind == kGemmPair ? "2-SM GEMM launch failed" : "GEMM launch failed";
+        *why = kind == kGemmQuad ? "4-SM GEMM launch failed" : kind == kGemmSingle ? "GEMM launch failed" : "2-SM GEMM launch failed";
     return e;
 }
 

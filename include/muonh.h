@@ -74,6 +74,10 @@ extern "C" {
 #define MUONH_FLAG_GEMM_QUAD   0x80u /* Newton-Schulz GEMMs on clusters of two CTA pairs that fetch the
                                         operand rows both pairs' tiles share once, multicast to both
                                         (same results bit for bit as the CTA-pair kernel) */
+#define MUONH_FLAG_GEMM_ONE_STEP 0x100u /* CTA-pair GEMMs with one 64-wide K step per pipeline stage
+                                        (16 KB TMA boxes) instead of two (32 KB boxes, used when K and
+                                        the contiguous extent of MN-major operands are multiples of
+                                        64); same results bit for bit */
 /* Step variants the pages do not name (muonh_step and muon_step; ignored by
  * muonh_orthogonalize): */
 #define MUONH_FLAG_NESTEROV    0x2u  /* Newton-Schulz input G + beta*M_new (Nesterov look-ahead)
