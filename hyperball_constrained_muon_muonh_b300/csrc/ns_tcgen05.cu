@@ -194,13 +194,15 @@ __device__ __forceinline__ void apply_slice(const GemmParams& p, const NsIO& io,
                     u.z = fmaf(p.nlr, y.z, p.wdecay * wp[k].z);
                     u.w = fmaf(p.nlr, y.w, p.wdecay * wp[k].w);
                     const size_t woff = (size_t)row * p.N + col;
-                    *reinterpret_cast<float4*>(io.w + woff) = u;
+                    __stcs(reinterpret_cast<float4*>(io.w + woff), u);
                     if (io.wb) store_bf16x4(reinterpret_cast<__nv_bfloat16*>(io.wb) + woff, u);
                 }
                 continue;
             }
+            // the fp32 state is read again only by the next apply's epilogue:
+            // streaming store, so it does not push the GEMM operands out of L2
             const size_t off = (size_t)row * p.ld_x + col;
-            *reinterpret_cast<float4*>(xs + off) = y;
+            __stcs(reinterpret_cast<float4*>(xs + off), y);
             if (xo) store_bf16x4(xo + off, y);
         }
     }
