@@ -380,6 +380,35 @@ def main():
         e2e = {"value": world * e_steps / dt, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": 4, "copy": "next step's gradients copied on a side stream during the step"}
 
+        # The same loop with bf16 gradients (MUONH_FLAG_GRAD_BF16): half the
+        # host->device bytes.  A second optimizer on the same weights; reported
+        # beside the fp32-gradient line, which stays the headline.
+        if args.optimizer != "adamw":
+            host_f32 = host
+            host = [h.to(torch.bfloat16).pin_memory() for h in host_f32]
+            del host_f32
+            grads = [[g.to(torch.bfloat16) for g in gs] for gs in grads]
+            flags16 = gemm_flags | mh.FLAG_GRAD_BF16
+            if args.optimizer == "muon":
+                opt = mh.Muon(ws, lr=work.lr, beta=work.beta, weight_decay=MUON_WD, ns_steps=work.ns_steps,
+                              ns_coeffs=work.coeffs, eps=work.eps, bf16_copies=True, flags=flags16)
+            else:
+                opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps, ns_coeffs=work.coeffs,
+                               eps=work.eps, bf16_copies=True, flags=flags16)
+            h2d16 = sum(h.numel() * h.element_size() for h in host)
+            run(2)
+            barrier()
+            t0 = time.perf_counter()
+            run(e_steps)
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            if world > 1:
+                t_ = torch.tensor([dt], device=dev)
+                dist.all_reduce(t_, op=dist.ReduceOp.MAX)
+                dt = t_.item()
+            e2e["grad_bf16"] = {"value": world * e_steps / dt, "unit": "steps/s", "h2d_bytes_per_step": h2d16,
+                                "d2h_bytes_per_step": 4, "flags": "MUONH_FLAG_GRAD_BF16"}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
