@@ -247,6 +247,9 @@ def main():
                     help="Newton-Schulz GEMM kernel: CTA pair per 256x256 tile (two K steps per pipeline "
                          "stage where the shape allows; pair_one_step: always one), clusters of two pairs "
                          "sharing an operand fetch, or one SM per 128x256 tile")
+    ap.add_argument("--one-stream", action="store_true",
+                    help="every Newton-Schulz launch on the caller's stream (no side streams for independent "
+                         "buckets)")
     ap.add_argument("--optimizer", default="muonh", choices=["muonh", "muon", "adamw"],
                     help="muon: plain Muon (decoupled weight decay 0.1, no hyperball), the baseline MuonH is "
                          "compared with; adamw: AdamW on the non-matrix group (workload qwen3_2b_adamw_group)")
@@ -285,7 +288,7 @@ def main():
     ws = work.weights(dev)
     grads = [work.grads(t, dev) for t in range(2)]   # two gradient sets, alternated
     gemm_flags = {"pair": 0, "pair_one_step": mh.FLAG_GEMM_ONE_STEP, "quad": mh.FLAG_GEMM_QUAD,
-                  "1sm": mh.FLAG_GEMM_1SM}[args.gemm]
+                  "1sm": mh.FLAG_GEMM_1SM}[args.gemm] | (mh.FLAG_ONE_STREAM if args.one_stream else 0)
     if args.optimizer == "adamw":
         ws = [w.reshape(-1) for w in ws]
         grads = [[g.reshape(-1) for g in gs] for gs in grads]
@@ -418,8 +421,12 @@ def main():
     ns_kinds = ("ns_gram", "ns_poly", "ns_apply", "ns_apply_in", "ns_apply_out", "ns_apply_in_out", "ns_apply_outw",
                 "ns_apply_in_outw")
     ns_ms = sum(prof[k]["ms"] for k in ns_kinds if k in prof)
+    ns_sum_ms = ns_ms
     ns_flops = sum(prof[k]["flops"] for k in ns_kinds if k in prof)
     ns_launches = sum(prof[k]["launches"] for k in ns_kinds if k in prof)
+    if "ns_busy" in prof and ns_launches == prof["ns_busy"]["launches"]:
+        # launches on the side streams overlap: time = union of their intervals
+        ns_ms = prof["ns_busy"]["ms"]
     achieved = ns_flops / (ns_ms / 1000.0) / 1e12 if ns_ms > 0 else 0.0
     tr = _ns_traffic_from_profiles()
     if args.optimizer == "adamw":
@@ -441,6 +448,9 @@ def main():
             "traffic": tr["bytes_per_launch"] if tr and tr.get("current") else None,
             "launches": ns_launches, "flops_per_launch": ns_flops / max(ns_launches, 1),
             "ms_per_launch": ns_ms / max(ns_launches, 1),
+            "ns_ms_per_step": ns_ms / args.steps,
+            "ns_launch_ms_sum_per_step": ns_sum_ms / args.steps,
+            "timing": "per-launch CUDA events on each launch's stream; time = union of the launch intervals",
             "ns_share_of_step": ns_ms / max(ms_total, 1e-9),
         }
     hbm = {}
@@ -459,6 +469,8 @@ def main():
                    "eps": work.eps, "state": "fp32 W/M/G + bf16 W copy; NS bf16 operands, fp32 state",
                    "l2": "inputs larger than L2 (about 20 GB of optimizer state touched per step)",
                    "parallelism": f"replica x{world}",
+                   "ns_streams": "caller's stream only" if args.one_stream else
+                                 "independent buckets on up to 4 streams (caller's + 3 side streams)",
                    "ns_gemm": {"pair": "2-SM pair 256x256 tiles, two K steps (32 KB TMA boxes) per stage",
                                "pair_one_step": "2-SM pair 256x256 tiles, one K step (16 KB TMA boxes) per stage",
                                "quad": "4-SM clusters: two pair tiles, shared operand multicast",

@@ -19,6 +19,7 @@
 #include <cstring>
 #include <atomic>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -70,13 +71,19 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // the new weight
 enum Kind { K_MOMENTUM, K_MOM_FIN, K_GRAM, K_POLY, K_APPLY, K_APPLY_IN, K_APPLY_OUT, K_APPLY_IN_OUT,
             K_APPLY_OUTW, K_APPLY_IN_OUTW, K_HB_NORM, K_HB_FIN, K_HB_APPLY, K_HB_SCALE, K_MUON_FIN, K_EMIT,
-            K_CAPTURE, K_SIMT_GRAM, K_SIMT_POLY, K_SIMT_APPLY, K_ADAMW, K_SMALL, K_COUNT };
+            K_CAPTURE, K_SIMT_GRAM, K_SIMT_POLY, K_SIMT_APPLY, K_ADAMW, K_SMALL, K_NS_BUSY, K_COUNT };
 const char* const kKindName[K_COUNT] = {"momentum", "momentum_finalize", "ns_gram", "ns_poly", "ns_apply",
                                         "ns_apply_in", "ns_apply_out", "ns_apply_in_out", "ns_apply_outw",
                                         "ns_apply_in_outw", "hyperball_norm", "hyperball_finalize",
                                         "hyperball_apply", "hyperball_scale", "muon_finish", "emit",
                                         "capture_norms", "fp32_gram", "fp32_poly", "fp32_apply", "adamw",
-                                        "small_step"};
+                                        "small_step", "ns_busy"};
+// ns_busy: all Newton-Schulz GEMM launches (tensor-core and fp32), with ms =
+// the length of the union of their event intervals, so launches that
+// overlap on the side streams are not counted twice
+inline bool is_ns_kind(int k) {
+    return (k >= K_GRAM && k <= K_APPLY_IN_OUTW) || (k >= K_SIMT_GRAM && k <= K_SIMT_APPLY);
+}
 
 int apply_kind(int variant) {
     switch (variant) {
@@ -452,15 +459,71 @@ double batch_elems(const DescBatch& b) {
 struct Sync {
     bool on;
     cudaStream_t st;
-    int check(cudaError_t e, const char* where) {
+    int check(cudaError_t e, const char* where) { return check_on(st, e, where); }
+    int check_on(cudaStream_t s, cudaError_t e, const char* where) {
         if (e != cudaSuccess) return cuda_fail(e, where);
         if (on) {
-            e = cudaStreamSynchronize(st);
+            e = cudaStreamSynchronize(s);
             if (e != cudaSuccess) return cuda_fail(e, where);
         }
         return MUONH_OK;
     }
 };
+
+// Side streams for Newton-Schulz.  The buckets of a step are independent
+// until the polynomial of their s-group, and s-groups are independent
+// throughout, so their launches go to up to kNsStreams streams (the
+// caller's first): a launch's tail of partly filled waves overlaps the next
+// bucket's launch instead of idling SMs.  Events fork the side streams from
+// the caller's stream and join them back; events are handed out in order
+// within a call, under a per-device lock so that concurrent calls cannot
+// re-record an event another call has yet to wait on.
+constexpr int kNsStreams = 4;
+struct NsStreams {
+    std::mutex mu;
+    cudaStream_t side[kNsStreams - 1] = {};
+    std::vector<cudaEvent_t> events;
+    size_t next = 0;
+    bool ready = false;
+    cudaError_t init() {
+        if (ready) return cudaSuccess;
+        for (auto& st : side) {
+            cudaError_t e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+            if (e != cudaSuccess) return e;
+        }
+        ready = true;
+        return cudaSuccess;
+    }
+    cudaError_t event(cudaEvent_t* out) {
+        if (next == events.size()) {
+            cudaEvent_t e = nullptr;
+            cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+            if (r != cudaSuccess) return r;
+            events.push_back(e);
+        }
+        *out = events[next++];
+        return cudaSuccess;
+    }
+};
+NsStreams& ns_streams_for_device() {
+    static std::mutex mu;
+    static std::map<int, std::unique_ptr<NsStreams>> by_dev;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    auto& p = by_dev[dev];
+    if (!p) p.reset(new NsStreams);
+    return *p;
+}
+// `to` waits for the work enqueued so far on `from`
+cudaError_t stream_after(NsStreams& ns, cudaStream_t to, cudaStream_t from) {
+    if (to == from) return cudaSuccess;
+    cudaEvent_t ev;
+    cudaError_t e = ns.event(&ev);
+    if (e == cudaSuccess) e = cudaEventRecord(ev, from);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(to, ev, 0);
+    return e;
+}
 
 // Newton-Schulz over every bucket: per iteration and s-group, the Gram of
 // each bucket, one polynomial launch for the group, the apply of each bucket.
@@ -474,6 +537,7 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                      : (flags & MUONH_FLAG_GEMM_ONE_STEP) ? tc::kGemmPairStep1
                                                           : tc::kGemmPair;
     *x_in_alt = false;
+    cudaStream_t cur = sy.st;   // stream of the launch being enqueued
 
     // ---- fp32 check mode (CUDA cores) ----
     auto simt_gram = [&](const Bucket& B, int it) {
@@ -490,8 +554,8 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         g.out = reinterpret_cast<float*>(ws + B.off_af); g.ldo = B.ld_s; g.out_bstride = sstr;
         g.scale = it == 0 ? sc.inv_nu2 + B.first : nullptr;
         const double G = B.G, S = B.s, L = B.l;
-        Trace tr(K_SIMT_GRAM, sy.st);
-        return sy.check(tr.done(launch_simt_gemm(g, sy.st), G * S * S * L, G * S * L * 4 + G * S * S * 4),
+        Trace tr(K_SIMT_GRAM, cur);
+        return sy.check_on(cur, tr.done(launch_simt_gemm(g, cur), G * S * S * L, G * S * L * 4 + G * S * S * 4),
                         "fp32 Gram launch");
     };
     auto simt_poly = [&](const SGroup& Q) {
@@ -505,8 +569,8 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         q.out = reinterpret_cast<float*>(ws + Q.off_aop); q.ldo = Q.ld_s; q.out_bstride = sstr;
         q.cb = coeffs[1]; q.cc = coeffs[2];
         const double G = Q.G, S = Q.s;
-        Trace tr(K_SIMT_POLY, sy.st);
-        return sy.check(tr.done(launch_simt_gemm(q, sy.st), G * S * S * S, G * S * S * 12), "fp32 polynomial launch");
+        Trace tr(K_SIMT_POLY, cur);
+        return sy.check_on(cur, tr.done(launch_simt_gemm(q, cur), G * S * S * S, G * S * S * 12), "fp32 polynomial launch");
     };
     auto simt_apply = [&](const Bucket& B, int it) {
         float* xs = reinterpret_cast<float*>(ws + B.off_xs);
@@ -532,8 +596,8 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         a.scale = it == 0 ? sc.inv_nu + B.first : nullptr;
         a.ca = coeffs[0];
         const double G = B.G, S = B.s, L = B.l;
-        Trace tr(K_SIMT_APPLY, sy.st);
-        return sy.check(tr.done(launch_simt_gemm(a, sy.st), 2 * G * S * S * L, G * S * S * 4 + G * S * L * 12),
+        Trace tr(K_SIMT_APPLY, cur);
+        return sy.check_on(cur, tr.done(launch_simt_gemm(a, cur), 2 * G * S * S * L, G * S * S * 4 + G * S * L * 12),
                         "fp32 apply launch");
     };
 
@@ -560,11 +624,11 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         const double G = B.G, S = B.s, L = B.l;
         cudaError_t e;
         {
-            Trace tr(K_GRAM, sy.st);
-            e = tr.done(tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, pair, sy.st, &why), G * S * S * L,
+            Trace tr(K_GRAM, cur);
+            e = tr.done(tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, pair, cur, &why), G * S * S * L,
                         G * S * L * 2 + G * S * S * 6);
         }
-        return sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 Gram launch");
+        return sy.check_on(cur, e, e == cudaErrorInvalidValue ? why : "tcgen05 Gram launch");
     };
     auto tc_poly = [&](const SGroup& Q) {
         const char* why = "";
@@ -579,11 +643,11 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         const double G = Q.G, S = Q.s;
         cudaError_t e;
         {
-            Trace tr(K_POLY, sy.st);
-            e = tr.done(tc::launch_ns_gemm(q, aop, Q.ld_s, aop, Q.ld_s, pair, sy.st, &why), G * S * S * S,
+            Trace tr(K_POLY, cur);
+            e = tr.done(tc::launch_ns_gemm(q, aop, Q.ld_s, aop, Q.ld_s, pair, cur, &why), G * S * S * S,
                         G * S * S * 8);
         }
-        return sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 polynomial launch");
+        return sy.check_on(cur, e, e == cudaErrorInvalidValue ? why : "tcgen05 polynomial launch");
     };
     auto tc_apply = [&](const Bucket& B, int it) {
         __nv_bfloat16 *xc, *xn;
@@ -619,12 +683,61 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
             // NS_OUT_W writes the weight (fp32 and bf16) in place of X
             double per_el = 8.0 + (a.x_op_out ? 2.0 : 0.0) + ((a.variant & NS_OUT_U) ? 4.0 : 0.0);
             if (a.variant & NS_OUT_W) per_el = 4.0 + 4.0 + 4.0 + 2.0;
-            Trace tr(apply_kind(a.variant), sy.st);
-            e = tr.done(B.tall ? tc::launch_ns_gemm(a, xc, B.ld_x, bop, B.ld_s, pair, sy.st, &why)
-                               : tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, pair, sy.st, &why),
+            Trace tr(apply_kind(a.variant), cur);
+            e = tr.done(B.tall ? tc::launch_ns_gemm(a, xc, B.ld_x, bop, B.ld_s, pair, cur, &why)
+                               : tc::launch_ns_gemm(a, bop, B.ld_s, xc, B.ld_x, pair, cur, &why),
                         2 * G * S * S * L, G * S * S * 2 + G * S * L * per_el);
         }
-        return sy.check(e, e == cudaErrorInvalidValue ? why : "tcgen05 apply launch");
+        return sy.check_on(cur, e, e == cudaErrorInvalidValue ? why : "tcgen05 apply launch");
+    };
+
+    // Streams: bucket k of the step (in plan order, small-step groups left
+    // out) runs on stream k % kNsStreams, the caller's stream first; an
+    // s-group's polynomial runs on its first bucket's stream, after every
+    // Gram of the group, and the group's applies run after it.  The next
+    // iteration's Gram of a bucket follows its apply on the same stream, so
+    // the polynomial of iteration it+1 (which rewrites the group's A and B
+    // buffers) comes after every apply of iteration it.
+    const int nb = (int)P.buckets.size();
+    std::vector<cudaStream_t> bst(nb, sy.st);
+    std::vector<cudaStream_t> used{sy.st};
+    NsStreams* ns = nullptr;
+    std::unique_lock<std::mutex> ns_lock;
+    {
+        int active = 0;
+        for (const SGroup& Q : P.sgroups)
+            if (!(fuse.small && Q.small_step)) active += Q.b_end - Q.b_begin;
+        if (active > 1 && ns_steps > 0 && !(flags & MUONH_FLAG_ONE_STREAM)) {
+            ns = &ns_streams_for_device();
+            ns_lock = std::unique_lock<std::mutex>(ns->mu);
+            ns->next = 0;
+            cudaError_t e = ns->init();
+            if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz side streams");
+            int k = 0;
+            for (const SGroup& Q : P.sgroups) {
+                if (fuse.small && Q.small_step) continue;
+                for (int b = Q.b_begin; b < Q.b_end; ++b, ++k) {
+                    const int slot = k % kNsStreams;
+                    bst[b] = slot == 0 ? sy.st : ns->side[slot - 1];
+                    if (std::find(used.begin(), used.end(), bst[b]) == used.end()) used.push_back(bst[b]);
+                }
+            }
+            for (size_t u = 1; u < used.size(); ++u) {
+                e = stream_after(*ns, used[u], sy.st);
+                if (e != cudaSuccess) return cuda_fail(e, "fork of the Newton-Schulz streams");
+            }
+        }
+    }
+    // group stream waits for / releases the streams of the group's buckets
+    auto join_group = [&](const SGroup& Q, cudaStream_t gs, bool to_group) {
+        std::vector<cudaStream_t> seen;
+        for (int b = Q.b_begin; b < Q.b_end; ++b) {
+            if (bst[b] == gs || std::find(seen.begin(), seen.end(), bst[b]) != seen.end()) continue;
+            seen.push_back(bst[b]);
+            cudaError_t e = to_group ? stream_after(*ns, gs, bst[b]) : stream_after(*ns, bst[b], gs);
+            if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz stream ordering");
+        }
+        return (int)MUONH_OK;
     };
 
     for (int it = 0; it < ns_steps; ++it) {
@@ -633,15 +746,29 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
             // every bucket of an s-group has the same s, so the same path
             const bool simt = check || Q.s <= kSmallSide;
             for (int b = Q.b_begin; b < Q.b_end; ++b) {
+                cur = bst[b];
                 const int r = simt ? simt_gram(P.buckets[b], it) : tc_gram(P.buckets[b], it);
                 if (r) return r;
             }
-            int r = simt ? simt_poly(Q) : tc_poly(Q);
+            const cudaStream_t gs = bst[Q.b_begin];
+            int r = ns ? join_group(Q, gs, true) : MUONH_OK;
+            if (r) return r;
+            cur = gs;
+            r = simt ? simt_poly(Q) : tc_poly(Q);
+            if (r) return r;
+            r = ns ? join_group(Q, gs, false) : MUONH_OK;
             if (r) return r;
             for (int b = Q.b_begin; b < Q.b_end; ++b) {
+                cur = bst[b];
                 r = simt ? simt_apply(P.buckets[b], it) : tc_apply(P.buckets[b], it);
                 if (r) return r;
             }
+        }
+    }
+    if (ns) {
+        for (size_t u = 1; u < used.size(); ++u) {
+            cudaError_t e = stream_after(*ns, sy.st, used[u]);
+            if (e != cudaSuccess) return cuda_fail(e, "join of the Newton-Schulz streams");
         }
     }
     *x_in_alt = (ns_steps & 1) != 0;
@@ -655,7 +782,7 @@ int check_scalars(int ns_steps, const float* coeffs, float eps, uint32_t flags) 
         if (!std::isfinite(coeffs[i])) return fail(MUONH_ERR_INVALID_ARG, "ns_coeffs must be finite");
     if (!std::isfinite(eps) || eps < 0.f) return fail(MUONH_ERR_INVALID_ARG, "eps must be finite and >= 0");
     if (flags & ~(uint32_t)(MUONH_FLAG_FP32_CHECK | MUONH_FLAG_SYNC_DEBUG | MUONH_FLAG_GEMM_1SM |
-                            MUONH_FLAG_GEMM_QUAD | MUONH_FLAG_GEMM_ONE_STEP | MUONH_FLAG_NESTEROV | MUONH_FLAG_SCALE_SHAPE | MUONH_FLAG_SCALE_RMS |
+                            MUONH_FLAG_GEMM_QUAD | MUONH_FLAG_GEMM_ONE_STEP | MUONH_FLAG_ONE_STREAM | MUONH_FLAG_NESTEROV | MUONH_FLAG_SCALE_SHAPE | MUONH_FLAG_SCALE_RMS |
                             MUONH_FLAG_GRAD_BF16))
         return fail(MUONH_ERR_UNSUPPORTED, "unknown flag bits");
     if ((flags & MUONH_FLAG_SCALE_SHAPE) && (flags & MUONH_FLAG_SCALE_RMS))
@@ -1138,6 +1265,8 @@ int muonh_profile_read(muonh_profile_entry_t* out, int max_entries, int* n_out) 
     g_last_error.clear();
     if (!out || !n_out || max_entries < 0) return fail(MUONH_ERR_INVALID_ARG, "out/n_out NULL");
     std::lock_guard<std::mutex> lk(g_prof.mu);
+    std::vector<std::pair<float, float>> ns_iv;   // Newton-Schulz intervals, ms from the first start
+    const cudaEvent_t ref = g_prof.pending.empty() ? nullptr : g_prof.pending.front().a;
     for (Pending& q : g_prof.pending) {
         cudaError_t e = cudaEventSynchronize(q.b);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
@@ -1148,10 +1277,31 @@ int muonh_profile_read(muonh_profile_entry_t* out, int max_entries, int* n_out) 
         g_prof.ms[q.kind] += ms;
         g_prof.flops[q.kind] += q.flops;
         g_prof.bytes[q.kind] += q.bytes;
+        if (is_ns_kind(q.kind)) {
+            float t0 = 0.f;
+            e = cudaEventElapsedTime(&t0, ref, q.a);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+            ns_iv.push_back({t0, t0 + ms});
+            g_prof.launches[K_NS_BUSY] += 1;
+            g_prof.flops[K_NS_BUSY] += q.flops;
+            g_prof.bytes[K_NS_BUSY] += q.bytes;
+        }
+    }
+    for (Pending& q : g_prof.pending) {
         g_prof.pool.push_back(q.a);
         g_prof.pool.push_back(q.b);
     }
     g_prof.pending.clear();
+    std::sort(ns_iv.begin(), ns_iv.end());
+    double busy = 0.0;
+    for (size_t i = 0; i < ns_iv.size();) {
+        float lo = ns_iv[i].first, hi = ns_iv[i].second;
+        size_t j = i + 1;
+        for (; j < ns_iv.size() && ns_iv[j].first <= hi; ++j) hi = std::max(hi, ns_iv[j].second);
+        busy += hi - lo;
+        i = j;
+    }
+    g_prof.ms[K_NS_BUSY] += busy;
     int n = 0;
     for (int k = 0; k < K_COUNT && n < max_entries; ++k) {
         if (g_prof.launches[k] == 0) continue;

@@ -74,6 +74,10 @@ extern "C" {
 #define MUONH_FLAG_GEMM_QUAD   0x80u /* Newton-Schulz GEMMs on clusters of two CTA pairs that fetch the
                                         operand rows both pairs' tiles share once, multicast to both
                                         (same results bit for bit as the CTA-pair kernel) */
+#define MUONH_FLAG_ONE_STREAM  0x200u /* enqueue every Newton-Schulz launch on the caller's stream
+                                        (default: independent buckets also use up to three
+                                        library-owned side streams, forked from and joined back
+                                        to the caller's stream with events) */
 #define MUONH_FLAG_GEMM_ONE_STEP 0x100u /* CTA-pair GEMMs with one 64-wide K step per pipeline stage
                                         (16 KB TMA boxes) instead of two (32 KB boxes, used when K and
                                         the contiguous extent of MN-major operands are multiples of
@@ -269,7 +273,10 @@ int muonh_profile_enable(int on);
 
 /* Waits for the recorded events, adds their durations into the per-kind
  * totals, and writes up to max_entries kinds with launches > 0 to out (host
- * array); *n_out = number written.  Blocking. */
+ * array); *n_out = number written.  Blocking.  The kind "ns_busy" covers
+ * every Newton-Schulz GEMM launch: its ms is the length of the union of
+ * their intervals (launches on the side streams may overlap), its flops
+ * and bytes the sums. */
 int muonh_profile_read(muonh_profile_entry_t* out, int max_entries, int* n_out);
 
 /* Number of kernels this library has launched in this process (all devices). */

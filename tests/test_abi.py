@@ -67,7 +67,7 @@ def test_step_rejects_bad_arguments_before_launch():
     assert _step(good, steps=65) == _lib.ERR_INVALID_ARG
     assert _step(good, coeffs=(ctypes.c_float * 3)(1.0, float("inf"), 0.0)) == _lib.ERR_INVALID_ARG
     assert _step(good, eps=-1.0) == _lib.ERR_INVALID_ARG
-    assert _step(good, flags=0x200) == _lib.ERR_UNSUPPORTED
+    assert _step(good, flags=0x400) == _lib.ERR_UNSUPPORTED
     assert _step(good, ws=0) == _lib.ERR_WORKSPACE
     assert _step(good, ws=512 + 16) == _lib.ERR_WORKSPACE
     assert _step(good, ws_bytes=16) == _lib.ERR_WORKSPACE
@@ -125,7 +125,7 @@ def test_muon_step_rejects_bad_arguments_before_launch():
     assert call(wd=float("inf")) == _lib.ERR_INVALID_ARG
     assert call(lr=float("nan")) == _lib.ERR_INVALID_ARG
     assert call(steps=65) == _lib.ERR_INVALID_ARG
-    assert call(flags=0x200) == _lib.ERR_UNSUPPORTED
+    assert call(flags=0x400) == _lib.ERR_UNSUPPORTED
     assert call(ws=0) == _lib.ERR_WORKSPACE
     assert call(ws_bytes=16) == _lib.ERR_WORKSPACE
 

@@ -6,7 +6,9 @@ The default pair kernel stages two 64-wide K steps per pipeline stage (one
 MN-major operand are multiples of 64, else one.  MUONH_FLAG_GEMM_ONE_STEP
 forces one K step per stage (16 KB boxes); MUONH_FLAG_GEMM_QUAD runs
 clusters of two pairs that fetch an operand two tiles share once, by TMA
-multicast.  All three walk the same list of 256 x 256 pair tiles and issue
+multicast; MUONH_FLAG_ONE_STREAM keeps every launch on the caller's stream
+instead of spreading independent buckets over side streams (same kernels,
+same dependencies).  All GEMM kernels walk the same list of 256 x 256 pair tiles and issue
 the same tcgen05 MMAs on the same shared-memory layout in the same K order,
 so every output -- O, the momentum, W, the bf16 copy -- must be identical.
 The shapes cover: symmetric Gram/polynomial tile lists with even and odd
@@ -51,11 +53,12 @@ def _cuda():
 SHAPES = [(2048, 2048), (640, 384), (384, 640), (768, 1280), (1280, 768), (129, 520), (520, 129),
           (1280, 320), (320, 1280), (384, 650), (650, 384), (6144, 2048), (2048, 6144), (1000, 1000)]
 
-VARIANTS = ["quad", "one_step"]
+VARIANTS = ["quad", "one_step", "one_stream"]
 
 
 def _flag(variant):
-    return {"quad": mh.FLAG_GEMM_QUAD, "one_step": mh.FLAG_GEMM_ONE_STEP}[variant]
+    return {"quad": mh.FLAG_GEMM_QUAD, "one_step": mh.FLAG_GEMM_ONE_STEP,
+            "one_stream": mh.FLAG_ONE_STREAM}[variant]
 
 
 def _bits(t):
