@@ -68,6 +68,7 @@ struct DescBatch {
     int first;            // global (bucket-order) index of d[0]
     int chunk_begin;      // first chunk of this batch
     int chunk_end;        // one past the last chunk of this batch
+    int bucket;           // plan bucket of every matrix in this batch (host side)
     MatDesc d[kMaxDescPerLaunch];
 };
 static_assert(sizeof(DescBatch) <= 32000, "descriptor batch exceeds kernel parameter space");

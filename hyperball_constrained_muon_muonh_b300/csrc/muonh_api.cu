@@ -403,13 +403,19 @@ std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, u
                                     bool with_momentum, const NsFuse& fuse = NsFuse()) {
     std::vector<DescBatch> out;
     const int n = P.n;
-    for (int b0 = 0; b0 < n; b0 += kMaxDescPerLaunch) {
+    // a batch never spans two buckets, so each bucket's elementwise passes
+    // can go to that bucket's stream
+    for (int b0 = 0; b0 < n;) {
+        int len = 1;
+        while (len < kMaxDescPerLaunch && b0 + len < n && P.bucket_of[b0 + len] == P.bucket_of[b0]) ++len;
         out.emplace_back();
         DescBatch& B = out.back();
-        B.n = std::min(kMaxDescPerLaunch, n - b0);
+        B.n = len;
         B.first = b0;
+        B.bucket = P.bucket_of[b0];
+        b0 += len;
         for (int k = 0; k < B.n; ++k) {
-            const int p = b0 + k;
+            const int p = B.first + k;
             const int u = P.order[p];
             const Bucket& bk = P.buckets[P.bucket_of[p]];
             const muonh_matrix_t& m = mats[u];
@@ -444,8 +450,8 @@ std::vector<DescBatch> make_batches(const Plan& P, const muonh_matrix_t* mats, u
                 }
             }
         }
-        B.chunk_begin = P.chunk0[b0];
-        B.chunk_end = (b0 + B.n < n) ? P.chunk0[b0 + B.n] : P.total_chunks;
+        B.chunk_begin = P.chunk0[B.first];
+        B.chunk_end = (B.first + B.n < n) ? P.chunk0[B.first + B.n] : P.total_chunks;
     }
     return out;
 }
@@ -525,12 +531,67 @@ cudaError_t stream_after(NsStreams& ns, cudaStream_t to, cudaStream_t from) {
     return e;
 }
 
+// The stream of every bucket for one call.  Bucket k of the step (plan
+// order, small-step groups left out) goes to stream k % kNsStreams, the
+// caller's stream first.  open() forks the side streams from the caller's
+// stream; close() (or the destructor, on an error path) joins them back.
+struct Schedule {
+    cudaStream_t st = nullptr;
+    std::vector<cudaStream_t> bst;    // per bucket
+    std::vector<cudaStream_t> used;   // used[0] = the caller's stream
+    NsStreams* ns = nullptr;
+    std::unique_lock<std::mutex> lock;
+    bool joined = false;
+
+    int open(const Plan& P, uint32_t flags, bool skip_small_groups, cudaStream_t caller) {
+        st = caller;
+        bst.assign(P.buckets.size(), caller);
+        used.assign(1, caller);
+        int active = 0;
+        for (const SGroup& Q : P.sgroups)
+            if (!(skip_small_groups && Q.small_step)) active += Q.b_end - Q.b_begin;
+        if (active <= 1 || (flags & MUONH_FLAG_ONE_STREAM)) return MUONH_OK;
+        ns = &ns_streams_for_device();
+        lock = std::unique_lock<std::mutex>(ns->mu);
+        ns->next = 0;
+        cudaError_t e = ns->init();
+        if (e != cudaSuccess) return cuda_fail(e, "side streams");
+        int k = 0;
+        for (const SGroup& Q : P.sgroups) {
+            if (skip_small_groups && Q.small_step) continue;
+            for (int b = Q.b_begin; b < Q.b_end; ++b, ++k) {
+                const int slot = k % kNsStreams;
+                bst[b] = slot == 0 ? caller : ns->side[slot - 1];
+                if (std::find(used.begin(), used.end(), bst[b]) == used.end()) used.push_back(bst[b]);
+            }
+        }
+        for (size_t u = 1; u < used.size(); ++u) {
+            e = stream_after(*ns, used[u], caller);
+            if (e != cudaSuccess) return cuda_fail(e, "fork of the side streams");
+        }
+        return MUONH_OK;
+    }
+    int close() {
+        joined = true;
+        if (!ns) return MUONH_OK;
+        for (size_t u = 1; u < used.size(); ++u) {
+            cudaError_t e = stream_after(*ns, st, used[u]);
+            if (e != cudaSuccess) return cuda_fail(e, "join of the side streams");
+        }
+        return MUONH_OK;
+    }
+    ~Schedule() {
+        if (!joined) (void)close();
+    }
+};
+
 // Newton-Schulz over every bucket: per iteration and s-group, the Gram of
 // each bucket, one polynomial launch for the group, the apply of each bucket.
 // Returns MUONH_OK or an error code; *x_in_alt tells whether the buckets
 // that ran on CUDA cores left their result in the second fp32 buffer.
 int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_steps, const float* coeffs,
-                      uint32_t flags, uint32_t* status, Sync& sy, bool* x_in_alt, const NsFuse& fuse) {
+                      uint32_t flags, uint32_t* status, Sync& sy, bool* x_in_alt, const NsFuse& fuse,
+                      const Schedule& S) {
     const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
     const int pair = (flags & MUONH_FLAG_GEMM_1SM)        ? tc::kGemmSingle
                      : (flags & MUONH_FLAG_GEMM_QUAD)     ? tc::kGemmQuad
@@ -691,43 +752,13 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         return sy.check_on(cur, e, e == cudaErrorInvalidValue ? why : "tcgen05 apply launch");
     };
 
-    // Streams: bucket k of the step (in plan order, small-step groups left
-    // out) runs on stream k % kNsStreams, the caller's stream first; an
-    // s-group's polynomial runs on its first bucket's stream, after every
-    // Gram of the group, and the group's applies run after it.  The next
-    // iteration's Gram of a bucket follows its apply on the same stream, so
-    // the polynomial of iteration it+1 (which rewrites the group's A and B
-    // buffers) comes after every apply of iteration it.
-    const int nb = (int)P.buckets.size();
-    std::vector<cudaStream_t> bst(nb, sy.st);
-    std::vector<cudaStream_t> used{sy.st};
-    NsStreams* ns = nullptr;
-    std::unique_lock<std::mutex> ns_lock;
-    {
-        int active = 0;
-        for (const SGroup& Q : P.sgroups)
-            if (!(fuse.small && Q.small_step)) active += Q.b_end - Q.b_begin;
-        if (active > 1 && ns_steps > 0 && !(flags & MUONH_FLAG_ONE_STREAM)) {
-            ns = &ns_streams_for_device();
-            ns_lock = std::unique_lock<std::mutex>(ns->mu);
-            ns->next = 0;
-            cudaError_t e = ns->init();
-            if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz side streams");
-            int k = 0;
-            for (const SGroup& Q : P.sgroups) {
-                if (fuse.small && Q.small_step) continue;
-                for (int b = Q.b_begin; b < Q.b_end; ++b, ++k) {
-                    const int slot = k % kNsStreams;
-                    bst[b] = slot == 0 ? sy.st : ns->side[slot - 1];
-                    if (std::find(used.begin(), used.end(), bst[b]) == used.end()) used.push_back(bst[b]);
-                }
-            }
-            for (size_t u = 1; u < used.size(); ++u) {
-                e = stream_after(*ns, used[u], sy.st);
-                if (e != cudaSuccess) return cuda_fail(e, "fork of the Newton-Schulz streams");
-            }
-        }
-    }
+    // Streams (Schedule): an s-group's polynomial runs on its first
+    // bucket's stream, after every Gram of the group, and the group's applies
+    // run after it.  The next iteration's Gram of a bucket follows its apply
+    // on the same stream, so the polynomial of iteration it+1 (which rewrites
+    // the group's A and B buffers) comes after every apply of iteration it.
+    const std::vector<cudaStream_t>& bst = S.bst;
+    NsStreams* ns = S.ns;
     // group stream waits for / releases the streams of the group's buckets
     auto join_group = [&](const SGroup& Q, cudaStream_t gs, bool to_group) {
         std::vector<cudaStream_t> seen;
@@ -763,12 +794,6 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                 r = simt ? simt_apply(P.buckets[b], it) : tc_apply(P.buckets[b], it);
                 if (r) return r;
             }
-        }
-    }
-    if (ns) {
-        for (size_t u = 1; u < used.size(); ++u) {
-            cudaError_t e = stream_after(*ns, sy.st, used[u]);
-            if (e != cudaSuccess) return cuda_fail(e, "join of the Newton-Schulz streams");
         }
     }
     *x_in_alt = (ns_steps & 1) != 0;
@@ -952,6 +977,11 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
     fuse.small = !check && ns_steps >= 1;
     fuse.scale_mode = scale_mode_of(flags);
     fuse.lr = lr;
+    // every bucket's momentum, Newton-Schulz and hyperball passes run on its
+    // stream (Schedule); the small-matrix kernel runs on the caller's stream
+    Schedule S;
+    r = S.open(P, flags, fuse.small, st);
+    if (r) return r;
     if (fuse.small) {
         SmallStepArgs sa{lr, beta, eps, 1.f, ns_coeffs, ns_steps, false, nesterov, grad_bf16, fuse.scale_mode, r0_dev,
                          status};
@@ -976,22 +1006,24 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
         if (all_small(B)) continue;
         const double bytes = 14 * elems(B, kFusedIn, true) +
                              18 * (elems(B, kFusedIn, false) - elems(B, kFusedAll, true));
+        const cudaStream_t bs = S.bst[B.bucket];
         {
-            Trace tr(K_MOMENTUM, st);
-            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, nesterov, grad_bf16, st), 0,
-                                 bytes - (grad_bf16 ? 2 * (elems(B, 0, false) - elems(B, kFusedAll, true)) : 0)),
-                         "momentum launch");
+            Trace tr(K_MOMENTUM, bs);
+            r = sy.check_on(bs, tr.done(launch_momentum(B, beta, partials, io, nesterov, grad_bf16, bs), 0,
+                                        bytes - (grad_bf16 ? 2 * (elems(B, 0, false) - elems(B, kFusedAll, true)) : 0)),
+                            "momentum launch");
         }
         if (r) return r;
         {
-            Trace tr(K_MOM_FIN, st);
-            r = sy.check(tr.done(launch_momentum_finalize(B, partials, sc, eps, fuse.scale_mode, ns_steps == 0, st), 0, 0),
-                         "momentum finalize launch");
+            Trace tr(K_MOM_FIN, bs);
+            r = sy.check_on(bs, tr.done(launch_momentum_finalize(B, partials, sc, eps, fuse.scale_mode, ns_steps == 0, bs),
+                                        0, 0),
+                            "momentum finalize launch");
         }
         if (r) return r;
     }
     bool x_alt = false;
-    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
+    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse, S);
     if (r) return r;
     if (x_alt) batches = make_batches(P, mats, ws, true, true, fuse);
     const float* o_scale = sc.oscale;
@@ -999,26 +1031,27 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev, float lr,
         if (all_small(B)) continue;
         const double e_sep = elems(B, kFusedOut, false) - elems(B, kFusedAll, true);
         const double e_fused = elems(B, kFusedOut, true);
+        const cudaStream_t bs = S.bst[B.bucket];
         if (e_sep > 0) {
-            Trace tr(K_HB_NORM, st);
-            r = sy.check(tr.done(launch_hyperball_norm(B, lr, partials, o_scale, st), 0, e_sep * 8),
-                         "hyperball norm launch");
+            Trace tr(K_HB_NORM, bs);
+            r = sy.check_on(bs, tr.done(launch_hyperball_norm(B, lr, partials, o_scale, bs), 0, e_sep * 8),
+                            "hyperball norm launch");
             if (r) return r;
         }
         {
-            Trace tr(K_HB_FIN, st);
-            r = sy.check(tr.done(launch_hyperball_finalize(B, partials, upart, sc, r0_dev, st), 0, 0),
-                         "hyperball finalize launch");
+            Trace tr(K_HB_FIN, bs);
+            r = sy.check_on(bs, tr.done(launch_hyperball_finalize(B, partials, upart, sc, r0_dev, bs), 0, 0),
+                            "hyperball finalize launch");
         }
         if (r) return r;
         {
-            Trace tr(e_sep > 0 ? K_HB_APPLY : K_HB_SCALE, st);
-            r = sy.check(tr.done(launch_hyperball_finish(B, lr, sc, o_scale, st), 0, e_sep * 14 + e_fused * 10),
-                         "hyperball finish launch");
+            Trace tr(e_sep > 0 ? K_HB_APPLY : K_HB_SCALE, bs);
+            r = sy.check_on(bs, tr.done(launch_hyperball_finish(B, lr, sc, o_scale, bs), 0, e_sep * 14 + e_fused * 10),
+                            "hyperball finish launch");
         }
         if (r) return r;
     }
-    return MUONH_OK;
+    return S.close();
 }
 
 int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float weight_decay, int ns_steps,
@@ -1059,6 +1092,9 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
     fuse.scale_mode = scale_mode_of(flags);
     fuse.lr = lr;
     fuse.wdecay = 1.f - lr * weight_decay;
+    Schedule S;
+    r = S.open(P, flags, fuse.small, st);
+    if (r) return r;
     if (fuse.small) {
         SmallStepArgs sa{lr, beta, eps, fuse.wdecay, ns_coeffs, ns_steps, true, nesterov, grad_bf16, fuse.scale_mode,
                          nullptr, status};
@@ -1078,22 +1114,24 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
             e_all += e;
             if (B.d[k].fused & kFusedIn) e_in += e;
         }
+        const cudaStream_t bs = S.bst[B.bucket];
         {
-            Trace tr(K_MOMENTUM, st);
-            r = sy.check(tr.done(launch_momentum(B, beta, partials, io, nesterov, grad_bf16, st), 0,
-                                 14 * e_in + 18 * (e_all - e_in) - (grad_bf16 ? 2 * e_all : 0)),
-                         "momentum launch");
+            Trace tr(K_MOMENTUM, bs);
+            r = sy.check_on(bs, tr.done(launch_momentum(B, beta, partials, io, nesterov, grad_bf16, bs), 0,
+                                        14 * e_in + 18 * (e_all - e_in) - (grad_bf16 ? 2 * e_all : 0)),
+                            "momentum launch");
         }
         if (r) return r;
         {
-            Trace tr(K_MOM_FIN, st);
-            r = sy.check(tr.done(launch_momentum_finalize(B, partials, sc, eps, fuse.scale_mode, ns_steps == 0, st), 0, 0),
-                         "momentum finalize launch");
+            Trace tr(K_MOM_FIN, bs);
+            r = sy.check_on(bs, tr.done(launch_momentum_finalize(B, partials, sc, eps, fuse.scale_mode, ns_steps == 0, bs),
+                                        0, 0),
+                            "momentum finalize launch");
         }
         if (r) return r;
     }
     bool x_alt = false;
-    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
+    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse, S);
     if (r) return r;
     if (x_alt) batches = make_batches(P, mats, ws, true, true, fuse);
     const float* o_scale = sc.oscale;
@@ -1102,12 +1140,13 @@ int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float wei
         for (int k = 0; k < B.n; ++k)
             if (!(B.d[k].fused & (kFusedOutW | kFusedAll))) e_sep += (double)B.d[k].rows * B.d[k].cols;
         if (e_sep == 0) continue;
-        Trace tr(K_MUON_FIN, st);
-        r = sy.check(tr.done(launch_muon_finish(B, lr, fuse.wdecay, sc, o_scale, st), 0, e_sep * 14),
-                     "muon finish launch");
+        const cudaStream_t bs = S.bst[B.bucket];
+        Trace tr(K_MUON_FIN, bs);
+        r = sy.check_on(bs, tr.done(launch_muon_finish(B, lr, fuse.wdecay, sc, o_scale, bs), 0, e_sep * 14),
+                        "muon finish launch");
         if (r) return r;
     }
-    return MUONH_OK;
+    return S.close();
 }
 
 int adamw_step(const adamw_param_t* params, int n, int step, float lr, float beta1, float beta2, float eps,
@@ -1181,7 +1220,12 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     }
     if (r) return r;
     bool x_alt = false;
-    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse);
+    Schedule S;   // one matrix, one bucket: the caller's stream only
+    r = S.open(P, flags, fuse.small, st);
+    if (r) return r;
+    r = run_newton_schulz(P, ws, sc, ns_steps, ns_coeffs, flags, status, sy, &x_alt, fuse, S);
+    if (r) return r;
+    r = S.close();
     if (r) return r;
     m.w = out;
     batches = make_batches(P, &m, ws, x_alt, false, fuse);
