@@ -449,8 +449,9 @@ def main():
             "launches": ns_launches, "flops_per_launch": ns_flops / max(ns_launches, 1),
             "ms_per_launch": ns_ms / max(ns_launches, 1),
             "ns_ms_per_step": ns_ms / args.steps,
-            "ns_launch_ms_sum_per_step": ns_sum_ms / args.steps,
-            "timing": "per-launch CUDA events on each launch's stream; time = union of the launch intervals",
+            "ns_kind_busy_sum_per_step": ns_sum_ms / args.steps,
+            "timing": "per-launch CUDA events on each launch's stream; time = union of the launch intervals "
+                      "(per kind in 'kernels', over all Newton-Schulz kinds here)",
             "ns_share_of_step": ns_ms / max(ms_total, 1e-9),
         }
     hbm = {}

@@ -78,9 +78,9 @@ const char* const kKindName[K_COUNT] = {"momentum", "momentum_finalize", "ns_gra
                                         "hyperball_apply", "hyperball_scale", "muon_finish", "emit",
                                         "capture_norms", "fp32_gram", "fp32_poly", "fp32_apply", "adamw",
                                         "small_step", "ns_busy"};
-// ns_busy: all Newton-Schulz GEMM launches (tensor-core and fp32), with ms =
-// the length of the union of their event intervals, so launches that
-// overlap on the side streams are not counted twice
+// A kind's ms is the length of the union of its launches' event intervals,
+// so launches that overlap on the side streams are not counted twice.
+// ns_busy: all Newton-Schulz GEMM launches (tensor-core and fp32) together.
 inline bool is_ns_kind(int k) {
     return (k >= K_GRAM && k <= K_APPLY_IN_OUTW) || (k >= K_SIMT_GRAM && k <= K_SIMT_APPLY);
 }
@@ -1309,23 +1309,24 @@ int muonh_profile_read(muonh_profile_entry_t* out, int max_entries, int* n_out) 
     g_last_error.clear();
     if (!out || !n_out || max_entries < 0) return fail(MUONH_ERR_INVALID_ARG, "out/n_out NULL");
     std::lock_guard<std::mutex> lk(g_prof.mu);
-    std::vector<std::pair<float, float>> ns_iv;   // Newton-Schulz intervals, ms from the first start
+    // per kind, the launch intervals in ms from the first recorded start;
+    // a kind's time is the length of their union (launches of one kind on
+    // different streams may overlap)
+    std::vector<std::vector<std::pair<float, float>>> iv(K_COUNT);
     const cudaEvent_t ref = g_prof.pending.empty() ? nullptr : g_prof.pending.front().a;
     for (Pending& q : g_prof.pending) {
         cudaError_t e = cudaEventSynchronize(q.b);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
-        float ms = 0.f;
+        float ms = 0.f, t0 = 0.f;
         e = cudaEventElapsedTime(&ms, q.a, q.b);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t0, ref, q.a);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+        iv[q.kind].push_back({t0, t0 + ms});
         g_prof.launches[q.kind] += 1;
-        g_prof.ms[q.kind] += ms;
         g_prof.flops[q.kind] += q.flops;
         g_prof.bytes[q.kind] += q.bytes;
         if (is_ns_kind(q.kind)) {
-            float t0 = 0.f;
-            e = cudaEventElapsedTime(&t0, ref, q.a);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
-            ns_iv.push_back({t0, t0 + ms});
+            iv[K_NS_BUSY].push_back({t0, t0 + ms});
             g_prof.launches[K_NS_BUSY] += 1;
             g_prof.flops[K_NS_BUSY] += q.flops;
             g_prof.bytes[K_NS_BUSY] += q.bytes;
@@ -1336,16 +1337,19 @@ int muonh_profile_read(muonh_profile_entry_t* out, int max_entries, int* n_out) 
         g_prof.pool.push_back(q.b);
     }
     g_prof.pending.clear();
-    std::sort(ns_iv.begin(), ns_iv.end());
-    double busy = 0.0;
-    for (size_t i = 0; i < ns_iv.size();) {
-        float lo = ns_iv[i].first, hi = ns_iv[i].second;
-        size_t j = i + 1;
-        for (; j < ns_iv.size() && ns_iv[j].first <= hi; ++j) hi = std::max(hi, ns_iv[j].second);
-        busy += hi - lo;
-        i = j;
+    for (int k = 0; k < K_COUNT; ++k) {
+        std::vector<std::pair<float, float>>& v = iv[k];
+        std::sort(v.begin(), v.end());
+        double busy = 0.0;
+        for (size_t i = 0; i < v.size();) {
+            float lo = v[i].first, hi = v[i].second;
+            size_t j = i + 1;
+            for (; j < v.size() && v[j].first <= hi; ++j) hi = std::max(hi, v[j].second);
+            busy += hi - lo;
+            i = j;
+        }
+        g_prof.ms[k] += busy;
     }
-    g_prof.ms[K_NS_BUSY] += busy;
     int n = 0;
     for (int k = 0; k < K_COUNT && n < max_entries; ++k) {
         if (g_prof.launches[k] == 0) continue;

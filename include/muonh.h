@@ -263,7 +263,8 @@ int muonh_version(void);
 typedef struct muonh_profile_entry {
     const char* name;   /* kernel kind: "momentum", "ns_gram", ...  (static string) */
     int64_t launches;   /* launches recorded */
-    double  ms;         /* summed event-measured duration, milliseconds */
+    double  ms;         /* event-measured busy time, milliseconds: the length of the union of
+                           the launches' intervals (launches on different streams may overlap) */
     double  flops;      /* summed algorithmic floating-point operations */
     double  bytes;      /* summed algorithmic HBM bytes */
 } muonh_profile_entry_t;
@@ -274,9 +275,8 @@ int muonh_profile_enable(int on);
 /* Waits for the recorded events, adds their durations into the per-kind
  * totals, and writes up to max_entries kinds with launches > 0 to out (host
  * array); *n_out = number written.  Blocking.  The kind "ns_busy" covers
- * every Newton-Schulz GEMM launch: its ms is the length of the union of
- * their intervals (launches on the side streams may overlap), its flops
- * and bytes the sums. */
+ * every Newton-Schulz GEMM launch together: the union of their intervals,
+ * the sums of their flops and bytes. */
 int muonh_profile_read(muonh_profile_entry_t* out, int max_entries, int* n_out);
 
 /* Number of kernels this library has launched in this process (all devices). */
