@@ -4,7 +4,8 @@ TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
 module.  The CUDA library never calls it, and it shares no code with the CUDA
 library (no kernels, headers, helpers or constants): it is written from the
-pages alone so that it can judge the CUDA path.
+cited descriptions of the method alone, so that it is an independent check
+of the CUDA path.
 
 What the pages fix
 ------------------
