@@ -31,6 +31,23 @@ def test_header_declarations_are_exported():
         assert hasattr(_lib.lib, name), name
 
 
+def test_binding_constants_match_header():
+    # every MUONH_FLAG_* / _STATUS_* / _ERR_* value the header defines is the
+    # binding's constant of the same name, and every binding flag is declared
+    text = open(os.path.join(ROOT, "include", "muonh.h")).read()
+    defs = {m.group(1): int(m.group(2), 0)
+            for m in re.finditer(r"#define\s+MUONH_((?:FLAG|STATUS|ERR)_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", text)}
+    assert len(defs) >= 17   # 4 error codes, 3 status bits, 10 flags
+    for name, value in defs.items():
+        assert getattr(_lib, name) == value, name
+    for name in dir(_lib):
+        if name.startswith("FLAG_"):
+            assert name in defs, name
+    flags = [v for k, v in defs.items() if k.startswith("FLAG_")]
+    assert len(set(flags)) == len(flags)                      # distinct bits
+    assert all(v and (v & (v - 1)) == 0 for v in flags)       # one bit each
+
+
 def test_version_and_strings():
     assert _lib.lib.muonh_version() >= 100
     assert _lib.lib.muonh_status_string(0) == b"ok"
