@@ -206,6 +206,18 @@ def test_step_aspect_low_rank():
     _check_step(work, w0, r0, hist, False, idx=idx)
 
 
+@pytest.mark.parametrize("mode", ["pair", "one_stream"])
+def test_step_maximum_side_lengths(mode):
+    # the longest side the ABI accepts (MUONH_MAX_SIDE = 65536), tall and wide,
+    # with a short side on fp32 CUDA cores (8) and on the tensor cores (96:
+    # one ragged pair tile, 1024 K steps in the Gram)
+    work = wl.ragged([(65536, 8), (8, 65536), (65536, 96), (96, 65536)])
+    flags = {"pair": 0, "one_stream": mh.FLAG_ONE_STREAM}[mode]
+    w0, r0, hist, status = _run_steps(work, 2, False, flags=flags)
+    assert status == 0
+    _check_step(work, w0, r0, hist, False)
+
+
 def test_step_golden_fixture():
     import json, os
     with open(os.path.join(os.path.dirname(__file__), "golden", "step_small.json")) as f:
