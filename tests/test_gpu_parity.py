@@ -106,7 +106,7 @@ def _check_step(work, w0, r0_gpu, hist, fp32_check, idx=None):
 # Newton-Schulz alone (muonh_orthogonalize) against the oracle
 # ---------------------------------------------------------------------------
 
-NS_SHAPES = [(256, 128), (128, 256), (300, 200), (200, 300), (129, 520), (520, 129), (1, 8), (8, 1),
+NS_SHAPES = [(256, 128), (128, 256), (300, 200), (200, 300), (129, 520), (520, 129), (1, 1), (1, 8), (8, 1),
              (77, 77), (640, 384), (2048, 2048), (1024, 2048), (6144, 2048), (2048, 6144)]
 
 
@@ -163,7 +163,7 @@ def test_step_single_256x128(fp32_check):
 @pytest.mark.parametrize("mode", list(MODES))
 def test_step_ragged_shapes_three_steps(mode):
     fp32_check = mode == "fp32"
-    work = wl.ragged([(300, 200), (200, 300), (129, 520), (1, 8), (8, 1), (77, 77), (5, 3), (640, 384)])
+    work = wl.ragged([(300, 200), (200, 300), (129, 520), (1, 8), (8, 1), (77, 77), (5, 3), (1, 1), (640, 384)])
     w0, r0, hist, status = _run_steps(work, 3, fp32_check, flags=MODES[mode])
     assert status == 0
     _check_step(work, w0, r0, hist, fp32_check)
