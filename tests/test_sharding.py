@@ -5,8 +5,8 @@ the weight exchange, on CPU.
   time assignment keeps the largest load within Graham's bound
   (4/3 - 1/(3m)) x the optimal makespan, checked against brute force on small
   inputs, and the loads within one item's cost of each other;
-* exchange: a world_size-2 gloo job where each rank steps only the matrices
-  it owns (the float64 oracle stands in for the GPU step) and the exchange
+* exchange: gloo jobs of 2, 3 and 8 ranks (with 8, one rank owns no
+  matrix) where each rank steps only the matrices it owns (the float64 oracle stands in for the GPU step) and the exchange
   makes every rank hold the weights of the unsharded step, bit for bit.
 """
 
@@ -78,19 +78,21 @@ def _worker(rank, world, port, result):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         from oracle import muonh as om
-        work = wl.ragged([(48, 32), (32, 48), (64, 64), (16, 40), (40, 16), (24, 24), (96, 8)])
+        work = wl.ragged(EXCHANGE_SHAPES)
         ws = [w for w in work.weights("cpu")]
         gs = [g for g in work.grads(0, "cpu")]
         w0 = [w.numpy().copy() for w in ws]
         r0 = om.capture_norms(w0)
         owners = partition(work.shapes, world)
         mine = [i for i, o in enumerate(owners) if o == rank]
-        # this rank's share of the step (the oracle stands in for the GPU step)
-        out = om.muonh_step([w0[i] for i in mine], [gs[i].numpy() for i in mine],
-                            [np.zeros_like(w0[i]) for i in mine], r0[mine], work.lr, work.beta, work.ns_steps,
-                            work.coeffs, work.eps)
-        for k, i in enumerate(mine):
-            ws[i].copy_(torch.from_numpy(out["w"][k]))
+        # this rank's share of the step (the oracle stands in for the GPU step);
+        # with more ranks than matrices a rank may own none
+        if mine:
+            out = om.muonh_step([w0[i] for i in mine], [gs[i].numpy() for i in mine],
+                                [np.zeros_like(w0[i]) for i in mine], r0[mine], work.lr, work.beta, work.ns_steps,
+                                work.coeffs, work.eps)
+            for k, i in enumerate(mine):
+                ws[i].copy_(torch.from_numpy(out["w"][k]))
         for i in range(len(ws)):
             if owners[i] != rank:
                 ws[i].fill_(float("nan"))                   # must be overwritten by the exchange
@@ -106,9 +108,15 @@ def _worker(rank, world, port, result):
         dist.destroy_process_group()
 
 
-def test_exchange_world_size_2_gloo():
-    world = 2
+EXCHANGE_SHAPES = [(48, 32), (32, 48), (64, 64), (16, 40), (40, 16), (24, 24), (96, 8)]
+
+
+@pytest.mark.parametrize("world", [2, 3, 8])
+def test_exchange_gloo(world):
+    owners = partition(EXCHANGE_SHAPES, world)
+    if world > len(EXCHANGE_SHAPES):
+        assert len(set(owners)) < world          # some rank owns nothing and still takes part
     ctx = mp.get_context("spawn")
     result = ctx.Manager().dict()
     mp.start_processes(_worker, args=(world, _free_port(), result), nprocs=world, start_method="spawn", join=True)
-    assert dict(result) == {0: 1, 1: 1}
+    assert dict(result) == {r: 1 for r in range(world)}
