@@ -24,7 +24,7 @@ if torch.cuda.is_available():
 SHAPES = [(300, 200), (200, 300), (13, 37), (37, 13), (77, 77), (520, 129), (640, 384), (8, 1)]
 NEST, SHAPE, RMS = 0x2, 0x10, 0x20
 VARIANTS = {"nesterov": (NEST, True, "none"), "shape": (SHAPE, False, "shape"), "rms": (RMS, False, "rms"),
-            "nesterov+shape": (NEST | SHAPE, True, "shape")}
+            "nesterov+shape": (NEST | SHAPE, True, "shape"), "nesterov+rms": (NEST | RMS, True, "rms")}
 
 
 @pytest.fixture(scope="module", autouse=True)
