@@ -243,10 +243,9 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--gemm", default="pair", choices=["pair", "pair_one_step", "quad", "1sm"],
+    ap.add_argument("--gemm", default="pair", choices=["pair", "pair_one_step", "1sm"],
                     help="Newton-Schulz GEMM kernel: CTA pair per 256x256 tile (two K steps per pipeline "
-                         "stage where the shape allows; pair_one_step: always one), clusters of two pairs "
-                         "sharing an operand fetch, or one SM per 128x256 tile")
+                         "stage where the shape allows; pair_one_step: always one), or one SM per 128x256 tile")
     ap.add_argument("--one-stream", action="store_true",
                     help="every Newton-Schulz launch on the caller's stream (no side streams for independent "
                          "buckets)")
@@ -287,7 +286,7 @@ def main():
 
     ws = work.weights(dev)
     grads = [work.grads(t, dev) for t in range(2)]   # two gradient sets, alternated
-    gemm_flags = {"pair": 0, "pair_one_step": mh.FLAG_GEMM_ONE_STEP, "quad": mh.FLAG_GEMM_QUAD,
+    gemm_flags = {"pair": 0, "pair_one_step": mh.FLAG_GEMM_ONE_STEP,
                   "1sm": mh.FLAG_GEMM_1SM}[args.gemm] | (mh.FLAG_ONE_STREAM if args.one_stream else 0)
     if args.optimizer == "adamw":
         ws = [w.reshape(-1) for w in ws]
@@ -502,7 +501,6 @@ def main():
                                  "independent buckets on up to 4 streams (caller's + 3 side streams)",
                    "ns_gemm": {"pair": "2-SM pair 256x256 tiles, two K steps (32 KB TMA boxes) per stage",
                                "pair_one_step": "2-SM pair 256x256 tiles, one K step (16 KB TMA boxes) per stage",
-                               "quad": "4-SM clusters: two pair tiles, shared operand multicast",
                                "1sm": "1-SM 128x256 tiles"}[args.gemm],
                    "optimizer": {"muon": "muon (weight decay 0.1)",
                                  "adamw": f"adamw (betas {ADAMW_BETAS}, eps {ADAMW_EPS}, weight decay {ADAMW_WD})"

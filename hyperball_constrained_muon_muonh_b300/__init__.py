@@ -20,7 +20,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_GEMM_ONE_STEP, FLAG_GEMM_QUAD, FLAG_ONE_STREAM, FLAG_GRAD_BF16, FLAG_NESTEROV, FLAG_SCALE_RMS,  # noqa: F401
+from ._lib import (FLAG_FP32_CHECK, FLAG_GEMM_1SM, FLAG_GEMM_ONE_STEP, FLAG_ONE_STREAM, FLAG_GRAD_BF16, FLAG_NESTEROV, FLAG_SCALE_RMS,  # noqa: F401
                    FLAG_SCALE_SHAPE,
                    FLAG_SYNC_DEBUG, STATUS_DEGENERATE_NORM, STATUS_KERNEL_TIMEOUT, STATUS_NONFINITE_INPUT,
                    MuonHError, check, lib)

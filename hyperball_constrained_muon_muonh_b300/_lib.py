@@ -28,7 +28,6 @@ FLAG_FP32_CHECK = 0x1
 FLAG_NESTEROV = 0x2
 FLAG_SYNC_DEBUG = 0x4
 FLAG_GEMM_1SM = 0x8
-FLAG_GEMM_QUAD = 0x80
 FLAG_GEMM_ONE_STEP = 0x100
 FLAG_ONE_STREAM = 0x200
 FLAG_SCALE_SHAPE = 0x10

@@ -594,7 +594,6 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
                       const Schedule& S) {
     const bool check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
     const int pair = (flags & MUONH_FLAG_GEMM_1SM)        ? tc::kGemmSingle
-                     : (flags & MUONH_FLAG_GEMM_QUAD)     ? tc::kGemmQuad
                      : (flags & MUONH_FLAG_GEMM_ONE_STEP) ? tc::kGemmPairStep1
                                                           : tc::kGemmPair;
     *x_in_alt = false;
@@ -807,7 +806,7 @@ int check_scalars(int ns_steps, const float* coeffs, float eps, uint32_t flags) 
         if (!std::isfinite(coeffs[i])) return fail(MUONH_ERR_INVALID_ARG, "ns_coeffs must be finite");
     if (!std::isfinite(eps) || eps < 0.f) return fail(MUONH_ERR_INVALID_ARG, "eps must be finite and >= 0");
     if (flags & ~(uint32_t)(MUONH_FLAG_FP32_CHECK | MUONH_FLAG_SYNC_DEBUG | MUONH_FLAG_GEMM_1SM |
-                            MUONH_FLAG_GEMM_QUAD | MUONH_FLAG_GEMM_ONE_STEP | MUONH_FLAG_ONE_STREAM | MUONH_FLAG_NESTEROV | MUONH_FLAG_SCALE_SHAPE | MUONH_FLAG_SCALE_RMS |
+                            MUONH_FLAG_GEMM_ONE_STEP | MUONH_FLAG_ONE_STREAM | MUONH_FLAG_NESTEROV | MUONH_FLAG_SCALE_SHAPE | MUONH_FLAG_SCALE_RMS |
                             MUONH_FLAG_GRAD_BF16))
         return fail(MUONH_ERR_UNSUPPORTED, "unknown flag bits");
     if ((flags & MUONH_FLAG_SCALE_SHAPE) && (flags & MUONH_FLAG_SCALE_RMS))

@@ -63,14 +63,12 @@ struct GemmParams {
 namespace tc {
 // GEMM kernels: one SM per 128 x 256 tile; one CTA pair per 256 x 256
 // tile, with two K steps per pipeline stage where the shape allows (else
-// one) or always one (kGemmPairStep1); or a cluster of two pairs that
-// fetches an operand both tiles share once.
-enum GemmKind { kGemmSingle = 0, kGemmPair = 1, kGemmQuad = 2, kGemmPairStep1 = 3 };
+// one) or always one (kGemmPairStep1).
+enum GemmKind { kGemmSingle = 0, kGemmPair = 1, kGemmPairStep1 = 3 };
 cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld, int kind,
                            cudaStream_t st, const char** why);
-// clusters of each multi-SM kernel that fit on the device at once
+// CTA pairs of the pair kernel that fit on the device at once
 int pair_cluster_capacity();
-int quad_cluster_capacity();
 int tiles_per_matrix(int mode, int M, int N);
 int pair_tiles_per_matrix(int mode, int M, int N);
 // ||U||^2 partials one apply tile writes: one per epilogue warp (8 per CTA,

@@ -799,253 +799,6 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
 
 }  // namespace pair
 
-// ---- 4-SM variant: two CTA pairs (cluster of 4) on consecutive pair tiles -------------
-// Pair P (CTAs 2P and 2P+1) computes pair tile t = 2u + P of the list the
-// pair kernel walks.  When the two tiles of super-tile u read the same 256
-// rows of an operand (same matrix and the same mp for A, or the same nj for
-// B), that operand is fetched once: CTA 2P+h loads 64 of the 128 rows CTA h
-// of either pair holds and multicasts them to CTAs h and 2+h, so each SM
-// issues 24 KB of TMA per K step instead of 32 KB.  Every TMA completion
-// lands on the full barrier of the destination's pair leader (the
-// cta_group::2 form signals the barrier at the same offset in the even CTA
-// of each destination pair).  A stage is refilled only after both pairs'
-// MMAs have released it: each leader's commit is multicast to the empty
-// barriers of all four CTAs, which count two arrivals.  When the tile count
-// is odd, pair 1 recomputes pair 0's last tile and writes nothing, so both
-// pairs walk the same stage sequence.
-namespace quad {
-
-using pair::A2_BYTES;
-using pair::B2_BYTES;
-using pair::SMEM2_BYTES;
-using pair::STAGE2_BYTES;
-using pair::STAGES2;
-
-constexpr int CHUNK_BYTES = 64 * BK * 2;   // 8 KB: 64 operand rows of one K step
-
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar,
-                                               uint16_t mask, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%4, %5, %6}], [%2], %3;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "h"(mask), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-
-// Operand rows row0 .. row0+127 of K step k0 into dst as two 64-row chunks
-// (dst, dst + 8 KB).  K-major maps take coordinates (k, row), MN-major maps
-// (row, k); both use a 64 x 64 box.  `shared`: this CTA loads only chunk P
-// and multicasts it to CTAs h and 2+h.
-__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, bool mn, int row0, int k0, int g,
-                                             uint32_t bar, bool shared, int P, int h) {
-    if (shared) {
-        const uint16_t mask = (uint16_t)((1u << h) | (1u << (2 + h)));
-        const int r = row0 + P * 64;
-        if (mn)
-            tma_load_3d_mc(dst + P * CHUNK_BYTES, map, bar, mask, r, k0, g);
-        else
-            tma_load_3d_mc(dst + P * CHUNK_BYTES, map, bar, mask, k0, r, g);
-        return;
-    }
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        if (mn)
-            pair::tma_load_3d_pair(dst + c * CHUNK_BYTES, map, bar, row0 + c * 64, k0, g);
-        else
-            pair::tma_load_3d_pair(dst + c * CHUNK_BYTES, map, bar, k0, row0 + c * 64, g);
-    }
-}
-
-// Super-tile u: this pair's tile (g, mp, nj), whether it is a stand-in
-// (odd tile count, pair 1 of the last super-tile), and which operand the
-// two tiles share.
-struct SuperTile {
-    int g, mp, nj;
-    bool dummy, share_a, share_b;
-};
-
-__device__ __forceinline__ SuperTile super_tile(const GemmParams& p, int u, int P, int total) {
-    const int t0 = 2 * u, t1 = 2 * u + 1;
-    SuperTile s;
-    const int g0 = t0 / p.tiles_per_mat;
-    int mp0, nj0;
-    pair::pair_coords(p, t0 - g0 * p.tiles_per_mat, mp0, nj0);
-    s.share_a = s.share_b = false;
-    s.dummy = t1 >= total;
-    s.g = g0;
-    s.mp = mp0;
-    s.nj = nj0;
-    if (s.dummy) return s;
-    const int g1 = t1 / p.tiles_per_mat;
-    int mp1, nj1;
-    pair::pair_coords(p, t1 - g1 * p.tiles_per_mat, mp1, nj1);
-    s.share_a = g0 == g1 && mp0 == mp1;
-    s.share_b = g0 == g1 && nj0 == nj1;
-    if (P == 1) {
-        s.g = g1;
-        s.mp = mp1;
-        s.nj = nj1;
-    }
-    s.dummy = false;
-    return s;
-}
-
-template <int MODE, int VAR>
-__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-ns_gemm_quad_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                    const __grid_constant__ GemmParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t* smem_a = smem;
-    uint8_t* smem_b = smem + STAGES2 * A2_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES2 * STAGE2_BYTES);
-    // bars: full[STAGES2], empty[STAGES2], tfull[2], tempty[2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 4);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* stage_base = reinterpret_cast<float*>(smem + STAGES2 * STAGE2_BYTES + 256);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_rank();
-    const int P = (int)(rank >> 1), h = (int)(rank & 1);
-    const bool leader = h == 0;
-    const uint32_t lead_rank = rank & ~1u;
-    const uint16_t pair_mask = (uint16_t)(3u << (2 * P));
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES2);
-    const uint32_t tfull0 = smem_u32(bars + 2 * STAGES2), tempty0 = smem_u32(bars + 2 * STAGES2 + 2);
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES2; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 2);   // one commit from each pair
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(tfull0 + 8 * s, 1);
-            mbar_init(tempty0 + 8 * s, 2 * EPI_WARPS);
-        }
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        prefetch_tmap(&tm_a);
-        prefetch_tmap(&tm_b);
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();   // all four CTAs' barriers initialised before any cross-CTA signal
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-
-    const int total = p.G * p.tiles_per_mat;
-    const int nsuper = (total + 1) / 2;
-    const int num_kb = (p.K + BK - 1) / BK;
-    const int cid = (int)cluster_id(), ncl = (int)cluster_count();
-
-    if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer (all four CTAs) ----------------
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        for (int u = cid; u < nsuper && ok; u += ncl) {
-            const SuperTile s = super_tile(p, u, P, total);
-            const int row_a = s.mp * 2 * BM + h * BM;
-            const int row_b = s.nj * BN + h * (BN / 2);
-            for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
-                const uint32_t fb_local = full0 + 8 * stage;
-                const uint32_t fb = map_to_rank(fb_local, lead_rank);
-                if (leader) mbar_expect_tx(fb_local, 2 * STAGE2_BYTES);
-                load_operand(smem_u32(smem_a + stage * A2_BYTES), &tm_a, p.a_mn != 0, row_a, kb * BK, s.g, fb,
-                             s.share_a, P, h);
-                load_operand(smem_u32(smem_b + stage * B2_BYTES), &tm_b, p.b_mn != 0, row_b, kb * BK, s.g, fb,
-                             s.share_b, P, h);
-                if (++stage == STAGES2) { stage = 0; phase ^= 1; }
-            }
-        }
-        if (!ok && leader) {
-            for (int s = 0; s < STAGES2; ++s) {
-                const unsigned long long t0 = global_ns();
-                while (global_ns() - t0 < 20000000ull) {
-                    if (mbar_try_wait(full0 + 8 * s, 0) || mbar_try_wait(full0 + 8 * s, 1)) break;
-                }
-            }
-        }
-    } else if (warp == 1 && lane == 0 && leader) {
-        // ---------------- MMA issuer (even CTA of each pair) ----------------
-        const uint32_t idesc = pair::idesc_pair(p.a_mn != 0, p.b_mn != 0);
-        const uint64_t a_desc0 = operand_desc(smem_u32(smem_a), 0, p.a_mn != 0);
-        const uint64_t b_desc0 = operand_desc(smem_u32(smem_b), 0, p.b_mn != 0);
-        const uint64_t a_step = operand_desc_step(p.a_mn != 0), b_step = operand_desc_step(p.b_mn != 0);
-        int stage = 0;
-        uint32_t phase = 0;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        bool ok = true;
-        for (int u = cid; u < nsuper && ok; u += ncl) {
-            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status)) break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t ad = a_desc0 + (uint64_t)(stage * (A2_BYTES >> 4));
-                const uint64_t bd = b_desc0 + (uint64_t)(stage * (B2_BYTES >> 4));
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_bf16_pair(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc, (kb | kk) ? 1u : 0u);
-                mma_commit_pair(empty0 + 8 * stage, (uint16_t)0xF);
-                if (++stage == STAGES2) { stage = 0; phase ^= 1; }
-            }
-            if (!ok) break;
-            mma_commit_pair(tfull0 + 8 * acc, pair_mask);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
-        }
-    } else if (warp >= 2) {
-        // ---------------- epilogue (all four CTAs: 128 rows each) ----------------
-        const int e = warp - 2;
-        const int q = warp & 3;
-        const int hc = e >> 2;
-        float* st = stage_base + e * ST_FLOATS;
-        const uint32_t tempty_leader = map_to_rank(tempty0, lead_rank);
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int u = cid; u < nsuper; u += ncl) {
-            const SuperTile s = super_tile(p, u, P, total);
-            const bool stand_in = s.dummy && P == 1;
-            const int t = 2 * u + P;
-            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + hc * (BN / 2));
-            const uint32_t te = tempty_leader + 8 * acc;
-            double* slot = ((VAR & NS_OUT_U) && !stand_in)
-                               ? p.upart + ((size_t)t * 2 + h) * (kUPartsPerTilePair / 2) + e
-                               : nullptr;
-            // a stand-in tile starts at column N: the epilogue writes nothing
-            const int jb = stand_in ? p.N : s.nj * BN + hc * (BN / 2);
-            if (!epilogue_tile<MODE, VAR>(p, s.g, s.mp * 2 * BM + h * BM + q * 32, jb, tfull0 + 8 * acc, acc_phase,
-                                          trow, st, lane, abort_flag, slot, [&]() {
-                                              __syncwarp();
-                                              if (lane == 0) remote_arrive(te);
-                                          }))
-                break;
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
-        }
-    }
-
-    tc_fence_before();
-    __syncwarp();
-    __syncthreads();
-    cluster_sync();   // no CTA leaves while another may still signal or write it
-    if (warp == 0) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                     : "memory");
-    }
-}
-
-}  // namespace quad
-
 // ---- host side -------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1188,56 +941,13 @@ static cudaError_t launch_single(const CUtensorMap& ta, const CUtensorMap& tb, c
     return cudaGetLastError();
 }
 
-template <int MODE, int VAR>
-static int max_quad_clusters() {
-    static int cached = 0;
-    if (cached) return cached;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(4 * 37, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = pair::SMEM2_BYTES;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 4;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, quad::ns_gemm_quad_kernel<MODE, VAR>, &cfg) != cudaSuccess || n <= 0) {
-        (void)cudaGetLastError();
-        n = sm_count() / 4;
-    }
-    cached = n;
-    return n;
-}
-
-template <int MODE, int VAR>
-static cudaError_t launch_quad(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, long long total,
-                               cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(quad::ns_gemm_quad_kernel<MODE, VAR>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, pair::SMEM2_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    const int maxc = max_quad_clusters<MODE, VAR>();
-    const long long nsuper = (total + 1) / 2;
-    const long long clusters = nsuper < maxc ? nsuper : maxc;
-    quad::ns_gemm_quad_kernel<MODE, VAR><<<(int)(4 * clusters), NUM_THREADS, pair::SMEM2_BYTES, st>>>(ta, tb, p);
-    return cudaGetLastError();
-}
-
-int quad_cluster_capacity() { return max_quad_clusters<NS_GRAM, 0>(); }
 int pair_cluster_capacity() { return max_pair_clusters<NS_GRAM, 0, 2>(); }
 
 template <int KIND>
 static cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, long long total,
                             cudaStream_t st) {
 #define MUONH_LAUNCH(M_, V_)                                                                      \
-    (KIND == kGemmQuad         ? launch_quad<M_, V_>(ta, tb, p, total, st)                         \
-     : KIND == kGemmPair       ? launch_pair<M_, V_, 2>(ta, tb, p, total, st)                      \
+    (KIND == kGemmPair         ? launch_pair<M_, V_, 2>(ta, tb, p, total, st)                      \
      : KIND == kGemmPairStep1  ? launch_pair<M_, V_, 1>(ta, tb, p, total, st)                      \
                                : launch_single<M_, V_>(ta, tb, p, total, st))
     if (p.mode == NS_GRAM) return MUONH_LAUNCH(NS_GRAM, 0);
@@ -1256,14 +966,13 @@ static cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const 
 
 // Operand tensors ([G][rows][ld] bf16, ld = a_ld / b_ld):
 //   K-major operand:  rows = M (or N), cols = K; box 64 x 128 (A, and B in
-//                     the pair kernel: 128 rows per CTA), 64 x 256 (B in the
-//                     1-SM kernel) or 64 x 64 (both in the 4-SM kernel)
+//                     the pair kernel: 128 rows per CTA) or 64 x 256 (B in the
+//                     1-SM kernel)
 //   MN-major operand: rows = K, cols = M (or N); box 64 x 64
 // GRAM wide: A = B = X_op (K-major);  GRAM tall: A = B = X_op (MN-major);
 // POLY: A = B = A_op (K-major);  APPLY wide: A = B_op (K-major), B = X_op
 // (MN-major);  APPLY tall: A = X_op, B = B_op (both K-major).
-// `kind` selects the 1-SM, 2-SM or 4-SM kernel; the 2-SM and 4-SM kernels
-// share the tile list and the ||U||^2 partial layout.
+// `kind` selects the 1-SM or the 2-SM kernel.
 cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void* b_op, int b_ld, int kind,
                            cudaStream_t st, const char** why) {
     if (p.mode != NS_APPLY) p.variant = 0;
@@ -1272,7 +981,7 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
     if ((p.variant & NS_OUT_W) && !p.mflags) { *why = "apply variant without status flags"; return cudaErrorInvalidValue; }
     if ((p.variant & NS_OUT_U) && (p.variant & NS_OUT_W)) { *why = "conflicting apply variants"; return cudaErrorInvalidValue; }
     if (p.variant != 0 && (p.N & 3) != 0) { *why = "apply variant needs a row length that is a multiple of 4"; return cudaErrorInvalidValue; }
-    if (kind != kGemmSingle && kind != kGemmPair && kind != kGemmPairStep1 && kind != kGemmQuad) {
+    if (kind != kGemmSingle && kind != kGemmPair && kind != kGemmPairStep1) {
         *why = "unknown GEMM kernel";
         return cudaErrorInvalidValue;
     }
@@ -1288,8 +997,8 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
         !(p.mode == NS_GRAM && p.a_mn && (p.K % 64) == 0 && (p.M % 64) == 0 && (p.N % 64) == 0))
         kind = kGemmPairStep1;
     const bool multi = kind != kGemmSingle;
-    const int a_box = kind == kGemmQuad ? 64 : BM;
-    const int b_box = kind == kGemmQuad ? 64 : kind == kGemmPairStep1 ? BN / 2 : BN;
+    const int a_box = BM;
+    const int b_box = kind == kGemmPairStep1 ? BN / 2 : BN;
     CUtensorMap ta, tb;
     bool oka, okb;
     if (kind == kGemmPair) {
@@ -1316,12 +1025,11 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
     }
     const long long total = (long long)p.G * p.tiles_per_mat;
     if (total <= 0) return cudaSuccess;
-    cudaError_t e = kind == kGemmQuad        ? dispatch<kGemmQuad>(ta, tb, p, total, st)
-                    : kind == kGemmPair      ? dispatch<kGemmPair>(ta, tb, p, total, st)
+    cudaError_t e = kind == kGemmPair        ? dispatch<kGemmPair>(ta, tb, p, total, st)
                     : kind == kGemmPairStep1 ? dispatch<kGemmPairStep1>(ta, tb, p, total, st)
                                              : dispatch<kGemmSingle>(ta, tb, p, total, st);
     if (e != cudaSuccess)
-        *why = kind == kGemmQuad ? "4-SM GEMM launch failed" : kind == kGemmSingle ? "GEMM launch failed" : "2-SM GEMM launch failed";
+        *why = kind == kGemmSingle ? "GEMM launch failed" : "2-SM GEMM launch failed";
     return e;
 }
 

@@ -71,9 +71,6 @@ extern "C" {
 #define MUONH_FLAG_GEMM_1SM    0x8u  /* Newton-Schulz GEMMs on one SM per 128x256 tile instead of the
                                         default CTA pair per 256x256 tile (same results up to bf16
                                         rounding order; for comparison and small problems) */
-#define MUONH_FLAG_GEMM_QUAD   0x80u /* Newton-Schulz GEMMs on clusters of two CTA pairs that fetch the
-                                        operand rows both pairs' tiles share once, multicast to both
-                                        (same results bit for bit as the CTA-pair kernel) */
 #define MUONH_FLAG_ONE_STREAM  0x200u /* enqueue every Newton-Schulz launch on the caller's stream
                                         (default: independent buckets also use up to three
                                         library-owned side streams, forked from and joined back

@@ -37,7 +37,7 @@ def test_binding_constants_match_header():
     text = open(os.path.join(ROOT, "include", "muonh.h")).read()
     defs = {m.group(1): int(m.group(2), 0)
             for m in re.finditer(r"#define\s+MUONH_((?:FLAG|STATUS|ERR)_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", text)}
-    assert len(defs) >= 17   # 4 error codes, 3 status bits, 10 flags
+    assert len(defs) >= 16   # 4 error codes, 3 status bits, 9 flags
     for name, value in defs.items():
         assert getattr(_lib, name) == value, name
     for name in dir(_lib):
@@ -85,6 +85,7 @@ def test_step_rejects_bad_arguments_before_launch():
     assert _step(good, coeffs=(ctypes.c_float * 3)(1.0, float("inf"), 0.0)) == _lib.ERR_INVALID_ARG
     assert _step(good, eps=-1.0) == _lib.ERR_INVALID_ARG
     assert _step(good, flags=0x400) == _lib.ERR_UNSUPPORTED
+    assert _step(good, flags=0x80) == _lib.ERR_UNSUPPORTED     # no flag has this bit
     assert _step(good, ws=0) == _lib.ERR_WORKSPACE
     assert _step(good, ws=512 + 16) == _lib.ERR_WORKSPACE
     assert _step(good, ws_bytes=16) == _lib.ERR_WORKSPACE

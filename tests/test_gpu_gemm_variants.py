@@ -4,18 +4,15 @@ bit.
 The default pair kernel stages two 64-wide K steps per pipeline stage (one
 32 KB TMA box per operand) when K and the contiguous extent of every
 MN-major operand are multiples of 64, else one.  MUONH_FLAG_GEMM_ONE_STEP
-forces one K step per stage (16 KB boxes); MUONH_FLAG_GEMM_QUAD runs
-clusters of two pairs that fetch an operand two tiles share once, by TMA
-multicast; MUONH_FLAG_ONE_STREAM keeps every launch on the caller's stream
+forces one K step per stage (16 KB boxes); MUONH_FLAG_ONE_STREAM keeps every launch on the caller's stream
 instead of spreading independent buckets over side streams (same kernels,
 same dependencies).  All GEMM kernels walk the same list of 256 x 256 pair tiles and issue
 the same tcgen05 MMAs on the same shared-memory layout in the same K order,
 so every output -- O, the momentum, W, the bf16 copy -- must be identical.
 The shapes cover: symmetric Gram/polynomial tile lists with even and odd
-counts (odd: the 4-SM kernel's pair 1 recomputes a tile and writes
-nothing), the wide apply (tiles that share B; B is MN-major), the tall
+counts, the wide apply (tiles that share B; B is MN-major), the tall
 apply and tall Gram (A shared; the tall Gram's operands are MN-major), an
-odd number of K steps, super-tiles that straddle a row, a column or a
+odd number of K steps, consecutive tiles that straddle a row, a column or a
 matrix boundary, buckets of several matrices, and shapes that fall back to
 one K step (K or an MN-major extent not a multiple of 64).  The oracle
 parity of each variant runs in test_gpu_parity.py and test_gpu_muon.py.
@@ -53,11 +50,11 @@ def _cuda():
 SHAPES = [(2048, 2048), (640, 384), (384, 640), (768, 1280), (1280, 768), (129, 520), (520, 129),
           (1280, 320), (320, 1280), (384, 650), (650, 384), (6144, 2048), (2048, 6144), (1000, 1000)]
 
-VARIANTS = ["quad", "one_step", "one_stream"]
+VARIANTS = ["one_step", "one_stream"]
 
 
 def _flag(variant):
-    return {"quad": mh.FLAG_GEMM_QUAD, "one_step": mh.FLAG_GEMM_ONE_STEP,
+    return {"one_step": mh.FLAG_GEMM_ONE_STEP,
             "one_stream": mh.FLAG_ONE_STREAM}[variant]
 
 

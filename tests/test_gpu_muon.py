@@ -23,7 +23,7 @@ if torch.cuda.is_available():
     import hyperball_constrained_muon_muonh_b300 as mh
 
 TOL_O = {False: 3e-2, True: 1e-4}
-MODES = {"pair": 0, "one_step": 1 << 8, "quad": 1 << 7, "1sm": 1 << 3, "fp32": 1}
+MODES = {"pair": 0, "one_step": 1 << 8, "1sm": 1 << 3, "fp32": 1}
 RAGGED = [(300, 200), (200, 300), (13, 37), (37, 13), (77, 77), (520, 129), (8, 1), (1, 1), (640, 384)]
 
 

@@ -111,7 +111,7 @@ NS_SHAPES = [(256, 128), (128, 256), (300, 200), (200, 300), (129, 520), (520, 1
 
 
 # flag sets: the default 2-SM pair GEMM, the 1-SM GEMM, the fp32 check mode
-MODES = {"pair": 0, "one_step": 1 << 8, "quad": 1 << 7, "1sm": 1 << 3, "fp32": 1}
+MODES = {"pair": 0, "one_step": 1 << 8, "1sm": 1 << 3, "fp32": 1}
 
 
 @pytest.mark.parametrize("mode", list(MODES))
