@@ -58,6 +58,9 @@ struct GemmParams {
     float wdecay;           // NS_OUT_W: 1 - lr*weight_decay
     float ca, cb, cc;
     uint32_t* status;       // device status word
+    unsigned long long timeout_ns;   // limit of every pipeline wait (0: the default, 4 s)
+    int test_no_loads;      // test hook: the TMA producer issues nothing, so the first wait of the
+                            // MMA issuer runs out (nothing is in flight when the kernel gives up)
 };
 
 namespace tc {

@@ -28,7 +28,8 @@
 //
 // Every wait is bounded; after a timeout the CTA raises
 // MUONH_STATUS_KERNEL_TIMEOUT and runs on through the same barrier sequence
-// (with invalid results) so that the peer CTA is never left waiting.
+// (with invalid results) so that the peer CTA is never left waiting, and
+// before TMEM is freed the issuer waits (bounded) for its last MMAs.
 
 #include "common.cuh"
 #include "ns_gemm.h"
@@ -206,6 +207,7 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
     double* peer = red + 8;                                                  // [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(peer + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t drain_bar = smem_u32(tmem_slot + 2);                     // 8-byte aligned
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, h = warp >> 2;
@@ -214,6 +216,7 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         mbar_init(mbar, 1);
+        mbar_init(drain_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -462,6 +465,12 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
         }
     }
 
+    // after a wait gave up, MMAs may still be running: every MMA the issuer
+    // started has completed before either CTA frees TMEM or exits
+    if (issuer) {
+        mma_commit_pair(drain_bar, 1);
+        mbar_drain_wait(drain_bar, 0, p.status, kTimeoutNs);
+    }
     tc_fence_before();
     __syncthreads();
     cluster_sync();

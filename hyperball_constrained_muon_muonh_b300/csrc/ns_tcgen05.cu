@@ -25,7 +25,9 @@
 // Shared memory: 4-stage ring of (A 128x64, B 256x64) bf16 tiles, 128-byte
 // swizzle.  TMEM: two 256-column fp32 accumulators so the epilogue of one
 // tile overlaps the main loop of the next.  Every mbarrier wait gives up
-// after a time limit, sets MUONH_STATUS_KERNEL_TIMEOUT and unwinds.
+// after a time limit, sets MUONH_STATUS_KERNEL_TIMEOUT and unwinds: copies
+// and MMAs already issued are waited for (bounded) before the CTA frees its
+// TMEM and exits (ExitState).
 
 #include <cuda.h>
 
@@ -57,6 +59,27 @@ __device__ __forceinline__ uint64_t operand_desc_step(bool mn_major) { return mn
 // 64-element MN chunks of 64 K-rows each (8 KB apart), K rows 128 B apart.
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk, bool mn_major) {
     return mn_major ? sdesc(base + kk * 2048, 64 * BK * 2, 1024) : sdesc(base + kk * 32, 16, 1024);
+}
+
+// Bookkeeping for leaving the kernel after a wait gave up, kept after the
+// pipeline barriers.  Copies and MMAs already issued must finish before the
+// CTA gives up the shared memory they write or read and the TMEM they
+// write: the producer counts the stage fills it issued (and the bytes of
+// each stage's last fill), the MMA issuer the fills it consumed, and on the
+// way out the fills issued but never consumed are waited for.
+struct ExitState {
+    uint64_t drain_bar;      // one MMA commit after the issuer's last MMA
+    uint32_t tmem_slot;
+    int abort_flag;
+    int fills;               // stage fills this CTA's producer issued
+    int consumed;            // stage fills the MMA issuer waited for
+    uint32_t fill_bytes[8];  // per stage, its last fill: bytes this CTA loaded (the pair
+                             // kernel's leader: the bytes it expected from both CTAs)
+};
+static_assert(sizeof(ExitState) == 56, "ExitState layout");
+
+__device__ __forceinline__ unsigned long long wait_limit(const GemmParams& p) {
+    return p.timeout_ns ? p.timeout_ns : kTimeoutNs;
 }
 
 __host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn_major, bool b_mn_major) {
@@ -298,7 +321,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
         if (reads_w) prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, jb, wc);
         if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, jb, ac);
     }
-    if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status)) return false;
+    if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, wait_limit(p))) return false;
     tc_fence_after();
     if (nsl == 0) release();
     float hacc = 0.f;
@@ -353,14 +376,18 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     uint8_t* smem_a = smem;
     uint8_t* smem_b = smem + STAGES * A_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2]; then the exit state
+    ExitState* ex = reinterpret_cast<ExitState*>(bars + 2 * STAGES + 4);
+    static_assert((2 * STAGES + 4) * 8 + sizeof(ExitState) <= 256, "barrier region");
+    uint32_t* tmem_slot = &ex->tmem_slot;
+    volatile int* abort_flag = &ex->abort_flag;
     float* stage_base = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t drain_bar = smem_u32(&ex->drain_bar);
+    const unsigned long long tlimit = wait_limit(p);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -371,7 +398,10 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             mbar_init(tfull0 + 8 * s, 1);
             mbar_init(tempty0 + 8 * s, 32 * EPI_WARPS);
         }
+        mbar_init(drain_bar, 1);
         *abort_flag = 0;
+        ex->fills = 0;
+        ex->consumed = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tm_a);
         prefetch_tmap(&tm_b);
@@ -394,13 +424,14 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         // ---------------- TMA producer ----------------
         int stage = 0;
         uint32_t phase = 0;
-        bool ok = true;
+        bool ok = !p.test_no_loads;
+        int fills = 0;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const int g = t / p.tiles_per_mat;
             int mi, nj;
             tile_coords(p, t - g * p.tiles_per_mat, mi, nj);
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, tlimit)) { ok = false; break; }
                 const uint32_t fb = full0 + 8 * stage;
                 mbar_expect_tx(fb, STAGE_BYTES);
                 const uint32_t sa = smem_u32(smem_a + stage * A_BYTES);
@@ -417,18 +448,11 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
                     for (int c = 0; c < BN / 64; ++c) tma_load_3d(sb + c * (64 * BK * 2), &tm_b, fb, nj * BN + c * 64, kb * BK, g);
                 }
+                ++fills;
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }
             }
         }
-        if (!ok) {
-            // let copies already in flight land before the CTA exits
-            for (int s = 0; s < STAGES; ++s) {
-                const unsigned long long t0 = global_ns();
-                while (global_ns() - t0 < 20000000ull) {
-                    if (mbar_try_wait(full0 + 8 * s, 0) || mbar_try_wait(full0 + 8 * s, 1)) break;
-                }
-            }
-        }
+        ex->fills = fills;
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer ----------------
         const uint32_t idesc = idesc_bf16(p.a_mn != 0, p.b_mn != 0);
@@ -440,12 +464,14 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
+        int consumed = 0;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status)) break;
+            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status, tlimit)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, tlimit)) { ok = false; break; }
+                ++consumed;
                 tc_fence_after();
                 // descriptors: stage base plus add-only steps along K
                 const uint64_t ad = a_desc0 + (uint64_t)(stage * (A_BYTES >> 4));
@@ -460,6 +486,10 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             mma_commit(tfull0 + 8 * acc);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        ex->consumed = consumed;
+        // every MMA this thread issued has completed before TMEM is freed
+        mma_commit(drain_bar);
+        mbar_drain_wait(drain_bar, 0, p.status, tlimit);
     } else if (warp >= 2) {
         // ---------------- epilogue ----------------
         // warp w reads TMEM lane quarter w%4; warps 2..5 take accumulator
@@ -486,6 +516,13 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
 
     tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // stage fills issued but never consumed (a wait gave up): their
+        // copies land in this CTA's shared memory, so wait for them here
+        for (int i = ex->consumed; i < ex->fills; ++i)
+            mbar_drain_wait(full0 + 8 * (i % STAGES), (uint32_t)(i / STAGES) & 1u, p.status, tlimit);
+    }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
@@ -608,9 +645,11 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     uint8_t* smem_a = smem;
     uint8_t* smem_b = smem + STAGES2 * A2_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES2 * STAGE2_BYTES);
-    // bars: full[STAGES2], empty[STAGES2], tfull[2], tempty[2]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 4);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // bars: full[STAGES2], empty[STAGES2], tfull[2], tempty[2]; then the exit state
+    ExitState* ex = reinterpret_cast<ExitState*>(bars + 2 * STAGES2 + 4);
+    static_assert((2 * STAGES2 + 4) * 8 + sizeof(ExitState) <= 256 && STAGES2 <= 8, "barrier region");
+    uint32_t* tmem_slot = &ex->tmem_slot;
+    volatile int* abort_flag = &ex->abort_flag;
     float* stage_base = reinterpret_cast<float*>(smem + STAGES2 * STAGE2_BYTES + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -618,6 +657,8 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     const bool leader = rank == 0;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES2);
     const uint32_t tfull0 = smem_u32(bars + 2 * STAGES2), tempty0 = smem_u32(bars + 2 * STAGES2 + 2);
+    const uint32_t drain_bar = smem_u32(&ex->drain_bar);
+    const unsigned long long tlimit = wait_limit(p);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES2; ++s) {
@@ -628,7 +669,10 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             mbar_init(tfull0 + 8 * s, 1);
             mbar_init(tempty0 + 8 * s, 2 * EPI_WARPS);
         }
+        mbar_init(drain_bar, 1);
         *abort_flag = 0;
+        ex->fills = 0;
+        ex->consumed = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tm_a);
         prefetch_tmap(&tm_b);
@@ -654,7 +698,8 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         // ---------------- TMA producer (both CTAs) ----------------
         int stage = 0;
         uint32_t phase = 0;
-        bool ok = true;
+        bool ok = !p.test_no_loads;
+        int fills = 0;
         for (int t = cid; t < total && ok; t += ncl) {
             const int g = t / p.tiles_per_mat;
             int mp, nj;
@@ -665,10 +710,14 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             // rows (same operand tensor), so B is not fetched
             const bool diag = MODE != NS_APPLY && mp == nj;
             for (int ks = 0; ks < num_ks; ++ks) {
-                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, tlimit)) { ok = false; break; }
                 const uint32_t fb_local = full0 + 8 * stage;
                 const uint32_t fb = map_to_rank(fb_local, 0);
-                if (leader) mbar_expect_tx(fb_local, diag ? 2 * A2_BYTES : 2 * STAGE2_BYTES);
+                // the leader's full barrier expects both CTAs' bytes; each CTA loads half
+                const uint32_t both = diag ? 2 * A2_BYTES : 2 * STAGE2_BYTES;
+                ex->fill_bytes[stage] = leader ? both : both / 2;
+                ++fills;
+                if (leader) mbar_expect_tx(fb_local, both);
                 const uint32_t sa = smem_u32(smem_a + stage * A2_BYTES);
                 const uint32_t sb = smem_u32(smem_b + stage * B2_BYTES);
                 if (KPS == 2) {
@@ -704,14 +753,7 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
                 if (++stage == STAGES2) { stage = 0; phase ^= 1; }
             }
         }
-        if (!ok && leader) {
-            for (int s = 0; s < STAGES2; ++s) {
-                const unsigned long long t0 = global_ns();
-                while (global_ns() - t0 < 20000000ull) {
-                    if (mbar_try_wait(full0 + 8 * s, 0) || mbar_try_wait(full0 + 8 * s, 1)) break;
-                }
-            }
-        }
+        ex->fills = fills;
     } else if (warp == 1 && lane == 0 && leader) {
         // ---------------- MMA issuer (even CTA only) ----------------
         const uint32_t idesc = idesc_pair(p.a_mn != 0, p.b_mn != 0);
@@ -723,6 +765,7 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
+        int consumed = 0;
         for (int t = cid; t < total && ok; t += ncl) {
             bool diag = false;
             if (MODE != NS_APPLY) {
@@ -734,11 +777,12 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             // B of a diagonal tile is read from A's buffer (same layout and size)
             const uint64_t b_base = diag ? a_desc0 : b_desc0;
             const int b_stage = diag ? A2_BYTES : B2_BYTES;
-            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status)) break;
+            if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status, tlimit)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int ks = 0; ks < num_ks; ++ks) {
-                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, tlimit)) { ok = false; break; }
+                ++consumed;
                 tc_fence_after();
 #pragma unroll
                 for (int j = 0; j < KPS; ++j) {
@@ -757,6 +801,11 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             mma_commit_pair(tfull0 + 8 * acc);
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        ex->consumed = consumed;
+        // every MMA this thread issued (they read both CTAs' shared memory and
+        // write both CTAs' TMEM) has completed before either CTA moves on
+        mma_commit_pair(drain_bar, 1);
+        mbar_drain_wait(drain_bar, 0, p.status, tlimit);
     } else if (warp >= 2) {
         // ---------------- epilogue (both CTAs: 128 rows each) ----------------
         const int e = warp - 2;
@@ -789,7 +838,29 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     tc_fence_before();
     __syncwarp();
     __syncthreads();
-    cluster_sync();   // no CTA leaves while its peer may still signal or read it
+    cluster_sync();   // neither CTA issues another copy or MMA from here on
+    if (leader && threadIdx.x == 0) {
+        // Stage fills issued but never consumed (a wait gave up) still land in
+        // either CTA's shared memory and complete on this CTA's full
+        // barriers.  Both producers walk the same stage sequence, each fill
+        // waits for the consumption of the fill one ring earlier, so every
+        // unconsumed fill is the only one outstanding on its stage.  Fill i
+        // is complete when its phase is: where only one producer issued it,
+        // the missing half of the barrier's accounting is supplied first.
+        const int C = ex->consumed, n_lead = ex->fills;
+        const int n_peer = (int)ld_cluster_u32(map_to_rank(smem_u32(&ex->fills), 1));
+        const int n_max = max(n_lead, n_peer);
+        for (int i = C; i < n_max; ++i) {
+            const int s = i % STAGES2;
+            const uint32_t fb = full0 + 8 * s;
+            if (i >= n_lead)        // the peer loaded, the leader never armed the barrier
+                mbar_expect_tx(fb, ld_cluster_u32(map_to_rank(smem_u32(&ex->fill_bytes[s]), 1)));
+            else if (i >= n_peer)   // the leader expected the peer's half, which never comes
+                mbar_complete_tx(fb, ex->fill_bytes[s] / 2);
+            mbar_drain_wait(fb, (uint32_t)(i / STAGES2) & 1u, p.status, tlimit);
+        }
+    }
+    cluster_sync();   // no CTA leaves while its peer may still signal, read or receive into it
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)

@@ -50,20 +50,42 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Bounded wait: false if the CTA has aborted or the time limit passed (then
 // *abort_flag is set and MUONH_STATUS_KERNEL_TIMEOUT raised).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status) {
+                                          uint32_t* status, unsigned long long limit_ns = kTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > kTimeoutNs) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 raise_status(status, MUONH_STATUS_KERNEL_TIMEOUT);
                 return false;
             }
         }
     }
+}
+
+// Bounded wait that ignores the abort flag: used on the way out of an
+// aborted kernel, to let asynchronous copies and MMAs already issued finish
+// before the shared memory and TMEM they touch are given up.  False if the
+// limit passed (then MUONH_STATUS_KERNEL_TIMEOUT is raised).
+__device__ __forceinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity, uint32_t* status,
+                                                unsigned long long limit_ns) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && global_ns() - t0 > limit_ns) {
+            raise_status(status, MUONH_STATUS_KERNEL_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Decrements the barrier's pending transaction count by `bytes`, as if that
+// many bytes of asynchronous copies had landed.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
@@ -213,6 +235,11 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
     asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 __device__ __forceinline__ void st_cluster_f64(uint32_t addr, double v) {
     asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
