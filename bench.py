@@ -61,6 +61,32 @@ def _dist():
     return world, rank, local
 
 
+def launch_plan(gpus: int, env) -> str:
+    """How a run with --gpus N starts: "run" (this process is one of the N
+    ranks, or N = 1), "relaunch" (N > 1 and no launcher: start N ranks with
+    torch.distributed.run) or an error text (a launcher started a different
+    number of ranks than --gpus asks for)."""
+    if gpus < 1:
+        return f"--gpus must be >= 1, got {gpus}"
+    if "WORLD_SIZE" in env:
+        world = int(env["WORLD_SIZE"])
+        if world != gpus:
+            return f"--gpus {gpus} but the launcher started WORLD_SIZE={world} ranks"
+        return "run"
+    return "run" if gpus == 1 else "relaunch"
+
+
+def _relaunch(gpus: int):
+    """Re-runs this command as `gpus` ranks on 127.0.0.1 (one per GPU)."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={gpus}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+    os.execv(sys.executable, cmd)
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples in the background (every 200 ms)."""
 
@@ -269,6 +295,12 @@ def main():
         run_reference(args, work, world, rank)
         return
 
+    plan = launch_plan(args.gpus, os.environ)
+    if plan == "relaunch":
+        _relaunch(args.gpus)
+    elif plan != "run":
+        raise SystemExit(plan)
+
     import torch
     import torch.distributed as dist
 
@@ -313,8 +345,9 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
+    # The headline: K steps with no tracing (the library's per-launch events
+    # off), between a barrier and a synchronise on each side.
     n_launch0 = mh.lib.muonh_launch_count()
-    mh.lib.muonh_profile_enable(1)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local) as clk:
         barrier()
@@ -325,8 +358,6 @@ def main():
         barrier()
     gpu_launches = mh.lib.muonh_launch_count() - n_launch0
     ms_total = ev0.elapsed_time(ev1)
-    prof = mh.profile_read()
-    mh.lib.muonh_profile_enable(0)
     if world > 1:
         t_ = torch.tensor([ms_total], device=dev)
         dist.all_reduce(t_, op=dist.ReduceOp.MAX)
@@ -334,11 +365,26 @@ def main():
     ms_step = ms_total / args.steps
     value = world * args.steps / (ms_total / 1000.0)
 
+    # The per-kernel breakdown and the roofline: more steps of the same
+    # schedule with the library's CUDA events around every launch (on the
+    # stream it is launched on), outside the headline's timed region.
+    prof_steps = min(args.steps, 10)
+    mh.lib.muonh_profile_enable(1)
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pe0.record(stream)
+    for t in range(prof_steps):
+        opt.step(grads[t % 2])
+    pe1.record(stream)
+    torch.cuda.synchronize()
+    prof = mh.profile_read()
+    mh.lib.muonh_profile_enable(0)
+    prof_ms_step = pe0.elapsed_time(pe1) / prof_steps
+
     # The HBM kernels' roofline comes from a few more steps with every launch
     # on the caller's stream: on the side streams a bucket's momentum or
     # hyperball launch can wait for SMs that other buckets' GEMMs hold, and
     # its event interval counts that wait.
-    prof_hbm, hbm_steps = prof, args.steps
+    prof_hbm, hbm_steps = prof, prof_steps
     if args.optimizer != "adamw" and not args.one_stream:
         hbm_steps = 3
         flags1 = gemm_flags | mh.FLAG_ONE_STREAM
@@ -395,7 +441,7 @@ def main():
                 mh.get_status()           # synchronises the compute stream; 4-byte device->host read
 
         run(2)
-        e_steps = max(2, min(args.steps, 5))
+        e_steps = max(20, args.steps)
         barrier()
         t0 = time.perf_counter()
         run(e_steps)
@@ -473,11 +519,13 @@ def main():
             "traffic": tr["bytes_per_launch"] if tr and tr.get("current") else None,
             "launches": ns_launches, "flops_per_launch": ns_flops / max(ns_launches, 1),
             "ms_per_launch": ns_ms / max(ns_launches, 1),
-            "ns_ms_per_step": ns_ms / args.steps,
-            "ns_kind_busy_sum_per_step": ns_sum_ms / args.steps,
-            "timing": "per-launch CUDA events on each launch's stream; time = union of the launch intervals "
-                      "(per kind in 'kernels', over all Newton-Schulz kinds here)",
-            "ns_share_of_step": ns_ms / max(ms_total, 1e-9),
+            "ns_ms_per_step": ns_ms / prof_steps,
+            "ns_kind_busy_sum_per_step": ns_sum_ms / prof_steps,
+            "timing": f"per-launch CUDA events on each launch's stream over {prof_steps} profiled steps after the "
+                      "headline loop; time = union of the launch intervals (per kind in 'kernels', over all "
+                      "Newton-Schulz kinds here)",
+            "ns_share_of_step": ns_ms / prof_steps / max(prof_ms_step, 1e-9),
+            "profiled_ms_per_step": prof_ms_step,
         }
     hbm = {}
     for k in ("momentum", "hyperball_norm", "hyperball_apply", "hyperball_scale", "muon_finish"):
@@ -511,9 +559,10 @@ def main():
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
         "e2e": e2e,
-        "kernels": {k: {"launches": v["launches"], "ms_per_step": v["ms"] / args.steps} for k, v in prof.items()},
-        "kernels_timing": "per kind, the union of its launches' event intervals in the timed region; with side "
-                          "streams an interval includes time a launch waits for SMs held by other buckets' launches",
+        "kernels": {k: {"launches": v["launches"], "ms_per_step": v["ms"] / prof_steps} for k, v in prof.items()},
+        "kernels_timing": f"per kind, the union of its launches' event intervals over {prof_steps} profiled steps "
+                          "(not the headline loop, which runs without per-launch events); with side streams an "
+                          "interval includes time a launch waits for SMs held by other buckets' launches",
     }
     if cpu is not None:
         v, cores, sample = cpu

@@ -113,38 +113,48 @@ def orthogonalize_workspace_size(rows: int, cols: int, flags: int = 0) -> int:
     return out.value
 
 
+def _dtype_code(t, name):
+    if not t.is_cuda or not t.is_contiguous() or t.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"{name} must be a contiguous CUDA float32 or bfloat16 tensor")
+    return _lib.DTYPE_F32 if t.dtype == torch.float32 else _lib.DTYPE_BF16
+
+
 def orthogonalize(x: torch.Tensor, ns_steps: int = 5, coeffs=NS_COEFFS, eps: float = 1e-7,
-                  flags: int = 0, out=None, workspace=None, stream=None) -> torch.Tensor:
-    """Newton-Schulz of a fp32 CUDA matrix (muonh_orthogonalize)."""
-    _check_tensor(x, "x")
+                  flags: int = 0, out=None, workspace=None, stream=None, out_dtype=torch.float32) -> torch.Tensor:
+    """Newton-Schulz of a fp32 or bf16 CUDA matrix (muonh_orthogonalize);
+    the result is fp32 unless ``out_dtype`` (or ``out``) says bf16."""
+    in_code = _dtype_code(x, "x")
     if out is None:
-        out = torch.empty_like(x)
+        out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    out_code = _dtype_code(out, "out")
     r, c_ = x.shape
     need = orthogonalize_workspace_size(r, c_, flags)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     cf = (ctypes.c_float * 3)(*coeffs)
-    check(lib.muonh_orthogonalize(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()), r, c_,
-                                  ns_steps, cf, eps, flags, ctypes.c_void_p(workspace.data_ptr()),
+    check(lib.muonh_orthogonalize(ctypes.c_void_p(x.data_ptr()), in_code, ctypes.c_void_p(out.data_ptr()), out_code,
+                                  r, c_, ns_steps, cf, eps, flags, ctypes.c_void_p(workspace.data_ptr()),
                                   workspace.numel(), _stream(stream)), "muonh_orthogonalize")
     return out
 
 
 def orthogonalize_static(x: torch.Tensor, ns_steps: int = 5, coeffs=NS_COEFFS, eps: float = 1e-7,
-                         flags: int = 0, out=None, stream=None) -> torch.Tensor:
+                         flags: int = 0, out=None, stream=None, out_dtype=torch.float32) -> torch.Tensor:
     """Newton-Schulz without a workspace (muonh_orthogonalize_static).
 
     For code that cannot allocate device memory: scratch comes from the
     library's fixed device array (see include/muonh.h).  ``out`` must be
     given by such callers; calls that may overlap on the GPU race.
     """
-    _check_tensor(x, "x")
+    in_code = _dtype_code(x, "x")
     if out is None:
-        out = torch.empty_like(x)
+        out = torch.empty(x.shape, dtype=out_dtype, device=x.device)
+    out_code = _dtype_code(out, "out")
     r, c_ = x.shape
     cf = (ctypes.c_float * 3)(*coeffs)
-    check(lib.muonh_orthogonalize_static(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()), r, c_,
-                                         ns_steps, cf, eps, flags, _stream(stream)), "muonh_orthogonalize_static")
+    check(lib.muonh_orthogonalize_static(ctypes.c_void_p(x.data_ptr()), in_code, ctypes.c_void_p(out.data_ptr()),
+                                         out_code, r, c_, ns_steps, cf, eps, flags, _stream(stream)),
+          "muonh_orthogonalize_static")
     return out
 
 

@@ -36,6 +36,9 @@ FLAG_GRAD_BF16 = 0x40
 
 MAX_SIDE = 65536
 
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+
 # Every symbol include/muonh.h declares.
 EXPORTS = (
     "muonh_capture_norms", "muonh_workspace_size", "muonh_step",
@@ -43,9 +46,11 @@ EXPORTS = (
     "muonh_status_string", "muonh_last_error", "muonh_version",
     "muonh_profile_enable", "muonh_profile_read", "muonh_launch_count",
     "muonh_orthogonalize_static", "muon_step", "adamw_step", "muonh_partition",
+    "muonh_test_gemm_timeout",
 )
 
 STATIC_SCRATCH_BYTES = 80 * 1024 * 1024
+TEST_TIMEOUT_WS_BYTES = 512 * 1024
 
 
 class MatrixT(ctypes.Structure):
@@ -106,8 +111,8 @@ def _load():
     lib.adamw_step.argtypes = [ctypes.POINTER(AdamParamT), I, I, F, F, F, F, F, P]
     lib.muonh_partition.argtypes = [mp, I, I, ctypes.POINTER(I)]
     lib.muonh_orthogonalize_workspace_size.argtypes = [I64, I64, U32, ctypes.POINTER(SZ)]
-    lib.muonh_orthogonalize.argtypes = [P, P, I64, I64, I, fp, F, U32, P, SZ, P]
-    lib.muonh_orthogonalize_static.argtypes = [P, P, I64, I64, I, fp, F, U32, P]
+    lib.muonh_orthogonalize.argtypes = [P, I, P, I, I64, I64, I, fp, F, U32, P, SZ, P]
+    lib.muonh_orthogonalize_static.argtypes = [P, I, P, I, I64, I64, I, fp, F, U32, P]
     lib.muonh_get_status.argtypes = [ctypes.POINTER(U32), P]
     lib.muonh_status_string.argtypes = [I]
     lib.muonh_status_string.restype = ctypes.c_char_p
@@ -117,6 +122,7 @@ def _load():
     lib.muonh_profile_enable.argtypes = [I]
     lib.muonh_profile_read.argtypes = [ctypes.POINTER(ProfileEntry), I, ctypes.POINTER(I)]
     lib.muonh_launch_count.argtypes = []
+    lib.muonh_test_gemm_timeout.argtypes = [U32, ctypes.c_uint64, P, SZ, P]
     for name in EXPORTS:
         if name not in ("muonh_status_string", "muonh_last_error"):
             getattr(lib, name).restype = ctypes.c_int

@@ -22,6 +22,7 @@ FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std
 def _inputs():
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     files.append(os.path.join(os.path.dirname(HERE), "include", "muonh.h"))
+    files.append(os.path.join(os.path.dirname(HERE), "include", "muonh_test.h"))
     return files
 
 

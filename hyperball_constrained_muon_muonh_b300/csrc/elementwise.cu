@@ -339,9 +339,10 @@ muon_finish_kernel(const __grid_constant__ DescBatch b, float lr, float wdecay, 
     hyperball_chunk<HB_MUON>(D, r_begin, r_end, nlr, wdecay, unused);
 }
 
-// Standalone orthogonalisation output: out (D.w) = o_scale * X_state.
+// Standalone orthogonalisation output: out (D.w) = o_scale * X_state, as
+// fp32 or, with out_bf16, as bf16 (round to nearest even of that fp32 value).
 __global__ void __launch_bounds__(kThreads)
-emit_kernel(const __grid_constant__ DescBatch b, const float* __restrict__ o_scale) {
+emit_kernel(const __grid_constant__ DescBatch b, const float* __restrict__ o_scale, bool out_bf16) {
     const int chunk = b.chunk_begin + blockIdx.x;
     const int mi = find_matrix(b, chunk);
     const MatDesc& D = b.d[mi];
@@ -352,9 +353,14 @@ emit_kernel(const __grid_constant__ DescBatch b, const float* __restrict__ o_sca
     const int r_end = min(D.rows, r_begin + cr);
     const float os = o_scale ? o_scale[p] : 1.f;
     const size_t n = (size_t)(r_end - r_begin) * cols;
+    uint16_t* wb = reinterpret_cast<uint16_t*>(D.w);
     for (size_t e = threadIdx.x; e < n; e += kThreads) {
         const size_t r = r_begin + e / cols, c = e % cols;
-        D.w[r * cols + c] = os * D.xs[r * ld + c];
+        const float y = os * D.xs[r * ld + c];
+        if (out_bf16)
+            wb[r * cols + c] = bf16_bits(y);
+        else
+            D.w[r * cols + c] = y;
     }
 }
 
@@ -478,10 +484,10 @@ cudaError_t launch_muon_finish(const DescBatch& b, float lr, float wdecay, const
     return cudaGetLastError();
 }
 
-cudaError_t launch_emit(const DescBatch& b, const float* o_scale, cudaStream_t st) {
+cudaError_t launch_emit(const DescBatch& b, const float* o_scale, bool out_bf16, cudaStream_t st) {
     const int nblk = b.chunk_end - b.chunk_begin;
     if (nblk <= 0) return cudaSuccess;
-    emit_kernel<<<nblk, kThreads, 0, st>>>(b, o_scale);
+    emit_kernel<<<nblk, kThreads, 0, st>>>(b, o_scale, out_bf16);
     return cudaGetLastError();
 }
 

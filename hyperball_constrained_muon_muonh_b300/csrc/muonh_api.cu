@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "ns_gemm.h"
+#include "../../include/muonh_test.h"
 
 namespace muonh {
 
@@ -41,7 +42,7 @@ cudaError_t launch_hyperball_finish(const DescBatch& b, float lr, const Scalars&
                                     cudaStream_t st);
 cudaError_t launch_muon_finish(const DescBatch& b, float lr, float wdecay, const Scalars& sc, const float* o_scale,
                                cudaStream_t st);
-cudaError_t launch_emit(const DescBatch& b, const float* o_scale, cudaStream_t st);
+cudaError_t launch_emit(const DescBatch& b, const float* o_scale, bool out_bf16, cudaStream_t st);
 cudaError_t launch_capture_norms(const DescBatch& b, float* r0, cudaStream_t st);
 cudaError_t status_word(uint32_t** ptr);
 int adamw_launch(const adamw_param_t* params, int n, int step, float lr, float beta1, float beta2, float eps,
@@ -1172,12 +1173,15 @@ int muonh_orthogonalize_workspace_size(int64_t rows, int64_t cols, uint32_t flag
     return MUONH_OK;
 }
 
-int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols, int ns_steps,
-                        const float ns_coeffs[3], float eps, uint32_t flags, void* workspace, size_t ws_bytes,
-                        void* stream) {
+int muonh_orthogonalize(const void* in, int in_dtype, void* out, int out_dtype, int64_t rows, int64_t cols,
+                        int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags, void* workspace,
+                        size_t ws_bytes, void* stream) {
     g_last_error.clear();
     if (!in || !out || !aligned16(in) || !aligned16(out))
         return fail(MUONH_ERR_INVALID_ARG, "in/out NULL or not 16-byte aligned");
+    if ((in_dtype != MUONH_DTYPE_F32 && in_dtype != MUONH_DTYPE_BF16) ||
+        (out_dtype != MUONH_DTYPE_F32 && out_dtype != MUONH_DTYPE_BF16))
+        return fail(MUONH_ERR_UNSUPPORTED, "in_dtype/out_dtype must be MUONH_DTYPE_F32 or MUONH_DTYPE_BF16");
     if (rows < 1 || cols < 1 || rows > MUONH_MAX_SIDE || cols > MUONH_MAX_SIDE)
         return fail(MUONH_ERR_INVALID_ARG, "rows/cols out of range");
     int r = check_scalars(ns_steps, ns_coeffs, eps, flags);
@@ -1194,21 +1198,25 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const Scalars sc = scalars_of(P, ws);
     double* partials = reinterpret_cast<double*>(ws + P.off_partials);
+    const bool in_bf16 = in_dtype == MUONH_DTYPE_BF16, out_bf16 = out_dtype == MUONH_DTYPE_BF16;
     muonh_matrix_t m{};
-    m.w = const_cast<float*>(in);
+    m.w = static_cast<float*>(const_cast<void*>(in));   // read by the first kernel as the input
     m.rows = rows;
     m.cols = cols;
     const double el = (double)rows * cols;
     NsFuse fuse;
     fuse.check = (flags & MUONH_FLAG_FP32_CHECK) != 0;
-    fuse.in = !fuse.check && ns_steps >= 1;
+    // the first apply can read an fp32 input in place of an fp32 copy of X;
+    // a bf16 input is widened into the fp32 state by the first kernel
+    fuse.in = !fuse.check && ns_steps >= 1 && !in_bf16;
     NsIO* io = fuse.in ? reinterpret_cast<NsIO*>(ws + P.off_io) : nullptr;
     std::vector<DescBatch> batches = make_batches(P, &m, ws, false, false, fuse);
     const bool in_fused = (batches[0].d[0].fused & kFusedIn) != 0;
     {
+        // bytes: the input read (4 or 2), X_op written (2), and the fp32 state (4) unless fused
         Trace tr(K_MOMENTUM, st);
-        r = sy.check(tr.done(launch_momentum(batches[0], 0.f, partials, io, false, false, st), 0,
-                             el * (in_fused ? 6 : 10)),
+        r = sy.check(tr.done(launch_momentum(batches[0], 0.f, partials, io, false, in_bf16, st), 0,
+                             el * ((in_bf16 ? 2 : 4) + 2 + (in_fused ? 0 : 4))),
                      "momentum launch");
     }
     if (r) return r;
@@ -1226,11 +1234,12 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
     if (r) return r;
     r = S.close();
     if (r) return r;
-    m.w = out;
+    m.w = static_cast<float*>(out);
     batches = make_batches(P, &m, ws, x_alt, false, fuse);
     {
         Trace tr(K_EMIT, st);
-        r = sy.check(tr.done(launch_emit(batches[0], ns_steps == 0 ? sc.inv_nu : nullptr, st), 0, el * 8),
+        r = sy.check(tr.done(launch_emit(batches[0], ns_steps == 0 ? sc.inv_nu : nullptr, out_bf16, st), 0,
+                             el * (4 + (out_bf16 ? 2 : 4))),
                      "emit launch");
     }
     return r;
@@ -1364,5 +1373,36 @@ int muonh_profile_read(muonh_profile_entry_t* out, int max_entries, int* n_out) 
 }
 
 int64_t muonh_launch_count(void) { return g_launches.load(); }
+
+int muonh_test_gemm_timeout(uint32_t flags, uint64_t timeout_ns, void* workspace, size_t ws_bytes, void* stream) {
+    g_last_error.clear();
+    if (flags & ~(uint32_t)MUONH_FLAG_GEMM_1SM) return fail(MUONH_ERR_UNSUPPORTED, "flags: only MUONH_FLAG_GEMM_1SM");
+    if (timeout_ns < 1000ull || timeout_ns > 10000000000ull)
+        return fail(MUONH_ERR_INVALID_ARG, "timeout_ns must be in [1e3, 1e10]");
+    int r = check_workspace(workspace, ws_bytes, MUONH_TEST_TIMEOUT_WS_BYTES);
+    if (r) return r;
+    uint32_t* status = nullptr;
+    r = get_status_ptr(&status);
+    if (r) return r;
+    // a 256 x 256 Gram: X_op bf16 [256][256], A fp32 [256][256], A_op bf16 [256][256]
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    GemmParams g{};
+    g.mode = NS_GRAM; g.G = 1; g.M = 256; g.N = 256; g.K = 256;
+    g.ld_x = 256; g.ld_s = 256;
+    g.a_f32 = reinterpret_cast<float*>(ws + 128 * 1024);
+    g.sym_bf16 = reinterpret_cast<__nv_bfloat16*>(ws + 384 * 1024);
+    g.status = status;
+    g.timeout_ns = timeout_ns;
+    g.test_no_loads = 1;
+    const char* why = "";
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Trace tr(K_GRAM, st);
+    cudaError_t e = tr.done(tc::launch_ns_gemm(g, ws, 256, ws, 256,
+                                               (flags & MUONH_FLAG_GEMM_1SM) ? tc::kGemmSingle : tc::kGemmPair, st,
+                                               &why),
+                            0, 0);
+    if (e != cudaSuccess) return e == cudaErrorInvalidValue ? fail(MUONH_ERR_CUDA, why) : cuda_fail(e, "test GEMM launch");
+    return MUONH_OK;
+}
 
 }  // extern "C"

@@ -26,8 +26,13 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 }  // namespace
 
-extern "C" int muonh_orthogonalize_static(const float* in, float* out, int64_t rows, int64_t cols, int ns_steps,
-                                          const float ns_coeffs[3], float eps, uint32_t flags, void* stream) {
+extern "C" int muonh_orthogonalize_static(const void* in, int in_dtype, void* out, int out_dtype, int64_t rows,
+                                          int64_t cols, int ns_steps, const float ns_coeffs[3], float eps,
+                                          uint32_t flags, void* stream) {
+    if ((in_dtype != MUONH_DTYPE_F32 && in_dtype != MUONH_DTYPE_BF16) ||
+        (out_dtype != MUONH_DTYPE_F32 && out_dtype != MUONH_DTYPE_BF16))
+        return muonh::report_error(MUONH_ERR_UNSUPPORTED,
+                                   "in_dtype/out_dtype must be MUONH_DTYPE_F32 or MUONH_DTYPE_BF16");
     size_t need = 0;
     int r = muonh_orthogonalize_workspace_size(rows, cols, flags, &need);
     if (r != MUONH_OK) return r;
@@ -52,6 +57,6 @@ extern "C" int muonh_orthogonalize_static(const float* in, float* out, int64_t r
         }
         scratch = g_scratch_ptr[dev];
     }
-    return muonh_orthogonalize(in, out, rows, cols, ns_steps, ns_coeffs, eps, flags, scratch, kScratchBytes,
-                               stream);
+    return muonh_orthogonalize(in, in_dtype, out, out_dtype, rows, cols, ns_steps, ns_coeffs, eps, flags, scratch,
+                               kScratchBytes, stream);
 }

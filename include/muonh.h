@@ -121,7 +121,13 @@ int muonh_workspace_size(const muonh_matrix_t* mats, int n, uint32_t flags, size
 
 /*
  * One MuonH step over mats[0..n) (host array): momentum, Newton-Schulz,
- * hyperball projection, as in the header comment.
+ * hyperball projection, as in the header comment.  Defined by the Puro-2B
+ * digest (jacksunwei.me), section "The load-bearing tricks aren't in the
+ * abstract" (MuonH: Muon's update with every weight matrix kept at its
+ * initial Frobenius norm by projection onto that hypersphere; footnote 4:
+ * the Newton-Schulz iterations), and the Puro-2B model card (axforge.ai),
+ * section "Training" (zero weight decay on the MuonH group; FP32 master
+ * weights and optimizer state).
  *   r0_dev     device array of n radii (from muonh_capture_norms)
  *   lr         step size eta (the effective, already-multiplied rate)
  *   beta       momentum coefficient
@@ -141,14 +147,16 @@ int muonh_step(const muonh_matrix_t* mats, int n, const float* r0_dev,
                uint32_t flags, void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * One plain Muon step (the optimizer MuonH is compared with: Puro-2B paper
- * part 6, section 4.3.1, and the digest's "standard weight decay"): the same
+ * One plain Muon step, the optimizer MuonH is measured against: Puro-2B
+ * paper part 6, section 4.3.1 "Cost-Saving Factors" (the matched-ladder
+ * comparison of MuonH with Muon), and the digest's footnote 3 ("standard
+ * weight decay").  The pages give no formula for it; here it is the same
  * momentum and Newton-Schulz as muonh_step, then
  *     W <- (1 - lr*weight_decay) * W - lr*O,   W_bf16 <- bf16(W)  (RNE)
- * with no norm constraint (no r0).  Arguments as muonh_step; the workspace
- * is sized by muonh_workspace_size for the same list and flags.  A matrix
- * whose momentum turns non-finite keeps its W and sets
- * MUONH_STATUS_NONFINITE_INPUT.
+ * (decoupled weight decay), with no norm constraint (no r0).  Arguments as
+ * muonh_step; the workspace is sized by muonh_workspace_size for the same
+ * list and flags.  A matrix whose momentum turns non-finite keeps its W and
+ * sets MUONH_STATUS_NONFINITE_INPUT.
  */
 int muon_step(const muonh_matrix_t* mats, int n, float lr, float beta, float weight_decay,
               int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags,
@@ -185,14 +193,28 @@ int adamw_step(const adamw_param_t* params, int n, int step, float lr, float bet
  */
 int muonh_orthogonalize_workspace_size(int64_t rows, int64_t cols, uint32_t flags, size_t* bytes);
 
+/* Element types of muonh_orthogonalize's input and output. */
+#define MUONH_DTYPE_F32  0   /* fp32 */
+#define MUONH_DTYPE_BF16 1   /* bfloat16 bit patterns (uint16) */
+
 /*
- * Newton-Schulz alone (the "X <- ... ; O <- X" lines of the header comment)
- * on one fp32 rows x cols device matrix `in`, written to fp32 `out` (same
- * shape; may equal `in`).  Same meaning of ns_steps, ns_coeffs, eps, flags
- * and workspace as muonh_step.  A non-finite ||in||_F sets
- * MUONH_STATUS_NONFINITE_INPUT and `out` is then unspecified.
+ * Newton-Schulz alone (the "X <- ... ; O <- X" lines of the header comment):
+ * the orthogonalisation step of Muon that the Puro-2B digest, section "The
+ * load-bearing tricks aren't in the abstract" and its footnote 4, names as
+ * Muon's cost.  One rows x cols row-major device matrix `in` (element type
+ * in_dtype) is normalised by its Frobenius norm and iterated; the result O
+ * is written to `out` (same shape, element type out_dtype; bf16 output is
+ * the round-to-nearest-even of the fp32 result).  The model card's
+ * "Training" section keeps state "in BF16 or FP32 as appropriate", hence
+ * both types on either side.  `out` may equal `in` when the types match.
+ * A bf16 input is widened exactly to fp32 before the iteration.  Same
+ * meaning of ns_steps, ns_coeffs, eps, flags and workspace as muonh_step;
+ * the workspace size does not depend on the types.  A dtype other than
+ * MUONH_DTYPE_F32 / MUONH_DTYPE_BF16 returns MUONH_ERR_UNSUPPORTED before
+ * any launch.  A non-finite ||in||_F sets MUONH_STATUS_NONFINITE_INPUT and
+ * `out` is then unspecified.
  */
-int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
+int muonh_orthogonalize(const void* in, int in_dtype, void* out, int out_dtype, int64_t rows, int64_t cols,
                         int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags,
                         void* workspace, size_t ws_bytes, void* stream);
 
@@ -212,17 +234,22 @@ int muonh_orthogonalize(const float* in, float* out, int64_t rows, int64_t cols,
  * 1024 x 8192 and anything smaller fit.
  *
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and keeps it; make that
- * first call before any stream capture.  The call allocates no device memory
- * and calls no cudaMalloc/cudaFree.  All calls share the one array, so two
- * calls that may overlap on the GPU (different streams, or different host
- * threads on one device) race and corrupt each other's results: order them
- * on one stream.  No scratch byte is read before the same call writes it, so
- * stale contents from an earlier call do not matter.
+ * (cudaGetSymbolAddress, with that device current) and keeps it, keyed by
+ * the device index, for the life of the process; make that first call
+ * before any stream capture.  The kept address belongs to the device's
+ * primary context: do not call this entry point after cudaDeviceReset, or
+ * from a thread whose current context is one created with the driver API
+ * (there the array lives at another address).  The call allocates no device
+ * memory and calls no cudaMalloc/cudaFree.  All calls share the one array,
+ * so two calls that may overlap on the GPU (different streams, or different
+ * host threads on one device) race and corrupt each other's results: order
+ * them on one stream.  No scratch byte is read before the same call writes
+ * it, so stale contents from an earlier call do not matter.  in_dtype and
+ * out_dtype as for muonh_orthogonalize.
  */
 #define MUONH_STATIC_SCRATCH_BYTES (80u * 1024u * 1024u)
-int muonh_orthogonalize_static(const float* in, float* out, int64_t rows, int64_t cols,
-                               int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags,
+int muonh_orthogonalize_static(const void* in, int in_dtype, void* out, int out_dtype, int64_t rows,
+                               int64_t cols, int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags,
                                void* stream);
 
 /*

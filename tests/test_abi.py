@@ -37,6 +37,8 @@ def test_binding_constants_match_header():
     text = open(os.path.join(ROOT, "include", "muonh.h")).read()
     defs = {m.group(1): int(m.group(2), 0)
             for m in re.finditer(r"#define\s+MUONH_((?:FLAG|STATUS|ERR)_[A-Z0-9_]+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", text)}
+    dtypes = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+MUONH_(DTYPE_[A-Z0-9]+)\s+(\d+)", text)}
+    assert dtypes == {"DTYPE_F32": _lib.DTYPE_F32, "DTYPE_BF16": _lib.DTYPE_BF16}
     assert len(defs) >= 16   # 4 error codes, 3 status bits, 9 flags
     for name, value in defs.items():
         assert getattr(_lib, name) == value, name
@@ -99,11 +101,16 @@ def test_capture_and_orthogonalize_reject_bad_arguments():
     assert _lib.lib.muonh_capture_norms(None, 1, None, None) == _lib.ERR_INVALID_ARG
     assert _lib.lib.muonh_capture_norms(_arr([(4, 4)]), 1, None, None) == _lib.ERR_INVALID_ARG
     o = _lib.lib.muonh_orthogonalize
-    assert o(None, None, 4, 4, 5, COEFFS, 1e-7, 0, None, 0, None) == _lib.ERR_INVALID_ARG
-    assert o(ctypes.c_void_p(256), ctypes.c_void_p(256), 0, 4, 5, COEFFS, 1e-7, 0, None, 0, None) \
-        == _lib.ERR_INVALID_ARG
-    assert o(ctypes.c_void_p(256), ctypes.c_void_p(256), 4, 4, 5, COEFFS, 1e-7, 0, None, 0, None) \
-        == _lib.ERR_WORKSPACE
+    p, f32, bf16 = ctypes.c_void_p(256), _lib.DTYPE_F32, _lib.DTYPE_BF16
+    assert o(None, f32, None, f32, 4, 4, 5, COEFFS, 1e-7, 0, None, 0, None) == _lib.ERR_INVALID_ARG
+    assert o(p, f32, p, f32, 0, 4, 5, COEFFS, 1e-7, 0, None, 0, None) == _lib.ERR_INVALID_ARG
+    assert o(p, f32, p, f32, 4, 4, 5, COEFFS, 1e-7, 0, None, 0, None) == _lib.ERR_WORKSPACE
+    assert o(p, bf16, p, bf16, 4, 4, 5, COEFFS, 1e-7, 0, None, 0, None) == _lib.ERR_WORKSPACE
+    # element types other than fp32 (0) and bf16 (1) are rejected before anything else is looked at
+    for bad_in, bad_out in ((2, f32), (f32, 2), (-1, f32), (f32, 7)):
+        assert o(p, bad_in, p, bad_out, 4, 4, 5, COEFFS, 1e-7, 0, None, 0, None) == _lib.ERR_UNSUPPORTED
+        assert _lib.lib.muonh_orthogonalize_static(p, bad_in, p, bad_out, 4, 4, 5, COEFFS, 1e-7, 0, None) \
+            == _lib.ERR_UNSUPPORTED
 
 
 def test_workspace_size_layout():
@@ -169,3 +176,14 @@ def test_adamw_step_rejects_bad_arguments_before_launch():
     assert call(lr=float("nan")) == _lib.ERR_INVALID_ARG
     assert call(a=arr(numel=0)) == _lib.ERR_INVALID_ARG
     assert call(a=arr(ptr=264)) == _lib.ERR_INVALID_ARG
+
+
+def test_timeout_hook_rejects_bad_arguments_before_launch():
+    ws = ctypes.c_void_p(256)
+    f = _lib.lib.muonh_test_gemm_timeout
+    assert f(0x1, 1_000_000, ws, _lib.TEST_TIMEOUT_WS_BYTES, None) == _lib.ERR_UNSUPPORTED     # fp32 check
+    assert f(0, 10, ws, _lib.TEST_TIMEOUT_WS_BYTES, None) == _lib.ERR_INVALID_ARG             # < 1 us
+    assert f(0, 10 ** 11, ws, _lib.TEST_TIMEOUT_WS_BYTES, None) == _lib.ERR_INVALID_ARG       # > 10 s
+    assert f(0, 1_000_000, None, _lib.TEST_TIMEOUT_WS_BYTES, None) == _lib.ERR_WORKSPACE
+    assert f(0, 1_000_000, ws, _lib.TEST_TIMEOUT_WS_BYTES - 1, None) == _lib.ERR_WORKSPACE
+    assert f(0, 1_000_000, ctypes.c_void_p(260), _lib.TEST_TIMEOUT_WS_BYTES, None) == _lib.ERR_WORKSPACE

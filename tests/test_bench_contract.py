@@ -1,5 +1,6 @@
 """bench.py's reference arm (the float64 oracle on the host) prints one JSON
-line with the keys the benchmark contract names; no GPU involved."""
+line with the keys the benchmark contract names, and --gpus N agrees with the
+number of ranks a launcher started; no GPU involved."""
 
 import json
 import os
@@ -33,3 +34,24 @@ def test_reference_arm_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_gpus_flag_and_world_size_agree():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.launch_plan(1, {}) == "run"
+    assert bench.launch_plan(8, {}) == "relaunch"                       # N ranks started by bench.py itself
+    assert bench.launch_plan(4, {"WORLD_SIZE": "4"}) == "run"           # started by torchrun with N ranks
+    assert bench.launch_plan(1, {"WORLD_SIZE": "1"}) == "run"
+    for gpus, env in ((8, {"WORLD_SIZE": "1"}), (1, {"WORLD_SIZE": "2"}), (0, {})):
+        plan = bench.launch_plan(gpus, env)
+        assert plan not in ("run", "relaunch") and plan
+
+
+def test_mismatched_world_size_exits_nonzero():
+    env = dict(os.environ, WORLD_SIZE="3", RANK="0", LOCAL_RANK="0")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--workload",
+                          "single_256x128", "--no-cpu-baseline"], cwd=ROOT, capture_output=True, text=True,
+                         timeout=600, env=env)
+    assert out.returncode != 0
+    assert "WORLD_SIZE=3" in out.stderr

@@ -128,6 +128,35 @@ def test_orthogonalize_matches_oracle(shape, mode):
     assert mh.get_status() == 0
 
 
+@pytest.mark.parametrize("mode", ["pair", "1sm", "fp32"])
+@pytest.mark.parametrize("shape", [(300, 200), (200, 300), (2048, 1024), (1024, 2048), (256, 128), (64, 32),
+                                   (129, 520)])
+def test_orthogonalize_bf16_input_and_output(shape, mode):
+    # bf16 in: widened exactly, so the result equals the fp32 call on the
+    # widened values bit for bit; bf16 out: the round-to-nearest-even of the
+    # fp32 result, bit for bit; both against the oracle within the Newton-
+    # Schulz tolerance (plus bf16 rounding of O, <= 2^-9 relative per element)
+    flags = MODES[mode]
+    g = wl.ragged([shape]).grad(0, 0, "cuda")
+    x16 = g.to(torch.bfloat16)
+    xw = x16.float()
+    o32 = mh.orthogonalize(xw, 5, wl.NS_COEFFS, 1e-7, flags=flags)
+    o_in16 = mh.orthogonalize(x16, 5, wl.NS_COEFFS, 1e-7, flags=flags)
+    o_out16 = mh.orthogonalize(xw, 5, wl.NS_COEFFS, 1e-7, flags=flags, out_dtype=torch.bfloat16)
+    o_both16 = mh.orthogonalize(x16, 5, wl.NS_COEFFS, 1e-7, flags=flags, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert o_in16.dtype == torch.float32 and o_out16.dtype == torch.bfloat16
+    assert torch.equal(o_in16, o32)
+    assert torch.equal(o_both16, o_out16)
+    want_bits = om.bf16_round(o32.cpu().numpy()).view(np.uint32) >> 16
+    assert np.array_equal(o_out16.cpu().view(torch.int16).numpy().view(np.uint16).astype(np.uint32), want_bits)
+    want = om.newton_schulz(xw.cpu().numpy(), 5, wl.NS_COEFFS, 1e-7)
+    tol = TOL_O[int(mode == "fp32")]
+    assert _rel(o32.cpu().numpy(), want) <= tol
+    assert _rel(o_out16.float().cpu().numpy(), want) <= tol + 4e-3
+    assert mh.get_status() == 0
+
+
 @pytest.mark.parametrize("steps", [0, 1, 2])
 def test_orthogonalize_step_counts(steps):
     g = wl.ragged([(384, 640)]).grad(0, 0, "cuda")
@@ -260,22 +289,40 @@ def test_nonfinite_gradient_keeps_weight_and_sets_status():
     assert abs(ws[1].double().norm().item() / opt.r0[1].item() - 1) < 1e-5
 
 
-def test_degenerate_norm_sets_status():
-    # W = lr*O exactly: W is the orthogonalised gradient scaled by lr, taken
-    # from the library's own orthogonalisation of the same momentum.
-    g = wl.ragged([(16, 16)]).grad(0, 0, "cuda")
-    o = mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7)
-    w = (0.5 * o).contiguous()
-    keep = w.clone()
-    opt = mh.MuonH([w], lr=0.5)
-    opt.step([g])
+# shapes that take each path of the step: the fused tensor-core path (row
+# length a multiple of 4), the unfused one (hyperball norm pass), the on-chip
+# small-matrix kernel, fp32 CUDA cores for short sides <= 80, and the fp32
+# check mode
+DEGENERATE_PATHS = {"pair": ((384, 512), 0), "unfused": ((300, 202), 0), "small": ((256, 128), 0),
+                    "cuda_cores": ((64, 32), 0), "fp32": ((384, 512), 1)}
+
+
+@pytest.mark.parametrize("case", ["zero_lr", "zero_grad"])
+@pytest.mark.parametrize("path", list(DEGENERATE_PATHS))
+def test_degenerate_norm_sets_status(path, case):
+    # W = 0 (so r0 = 0) stepped with lr = 0, or with G = 0 (then M = 0 and
+    # O = 0): U = W - lr*O is exactly zero in any arithmetic, so ||U|| = 0,
+    # the status bit is set and W is kept.  A second matrix of the same
+    # shape with ordinary inputs is stepped in the same call.
+    shape, fp32 = DEGENERATE_PATHS[path]
+    work = wl.ragged([shape, shape])
+    ws = work.weights("cuda")
+    ws[0].zero_()
+    keep = [w.clone() for w in ws]
+    lr = 0.0 if case == "zero_lr" else 0.02
+    opt = mh.MuonH(ws, lr=lr, fp32_check=bool(fp32), bf16_copies=True)
+    assert opt.r0[0].item() == 0.0
+    gs = work.grads(0, "cuda")
+    if case == "zero_grad":
+        gs[0].zero_()
+    opt.step(gs)
     st = mh.get_status()
-    # bf16 rounding inside the step may leave ||U|| tiny but non-zero; either
-    # the status bit is set and W kept, or W stays on the sphere
-    if st & mh.STATUS_DEGENERATE_NORM:
-        assert torch.equal(w, keep)
-    else:
-        assert abs(w.double().norm().item() / opt.r0[0].item() - 1) < 1e-5
+    assert st == mh.STATUS_DEGENERATE_NORM
+    assert torch.equal(ws[0], keep[0])                    # kept: still all zero
+    assert torch.equal(opt.moms[0], gs[0])                # the momentum still moves (M = beta*0 + G)
+    assert abs(ws[1].double().norm().item() / opt.r0[1].item() - 1) < 1e-5
+    if case == "zero_grad":
+        assert not torch.equal(ws[1], keep[1])            # the ordinary matrix moves
 
 
 def test_zero_gradient_and_zero_lr_fixed_points():

@@ -122,13 +122,38 @@ def test_momentum_small_integers():
     assert seq == [1.0, 1.5, 1.75]
 
 
-def test_capture_norms_brute_force():
+def _r0_pin_holds(capture) -> bool:
+    """r0 of a 3-4-12 matrix is exactly 13, and of a random 5 x 7 matrix it
+    is the correctly rounded square root of the exact (math.fsum) sum of
+    squares, to 1 ulp of float64."""
     w = np.array([[3.0, -4.0], [12.0, 0.0]], np.float32)
-    assert om.capture_norms([w])[0] == 13.0
+    if capture([w])[0] != 13.0:
+        return False
     rng = np.random.default_rng(4)
     v = rng.standard_normal((5, 7)).astype(np.float32)
     brute = math.sqrt(math.fsum(float(x) * float(x) for x in v.ravel()))
-    assert abs(om.capture_norms([v])[0] - brute) <= 1e-15 * brute
+    return abs(capture([v])[0] - brute) <= 1e-15 * brute
+
+
+def test_capture_norms_brute_force():
+    assert _r0_pin_holds(om.capture_norms)
+
+
+PLANTED_NORMS = {
+    "l1": lambda x: float(np.sum(np.abs(np.asarray(x, np.float64)))),
+    "no_sqrt": lambda x: float(np.sum(np.square(np.asarray(x, np.float64)))),
+    "max_abs": lambda x: float(np.max(np.abs(np.asarray(x, np.float64)))),
+    "fp32_accumulate": lambda x: float(np.sqrt(np.sum(np.square(np.asarray(x, np.float32)), dtype=np.float32))),
+    "first_row": lambda x: float(np.linalg.norm(np.asarray(x, np.float64)[0])),
+}
+
+
+@pytest.mark.parametrize("kind", list(PLANTED_NORMS))
+def test_planted_norm_mistakes_are_caught(kind, monkeypatch):
+    # the mistake goes into the oracle itself: capture_norms then calls the
+    # wrong norm, and the brute-force pin above must reject it
+    monkeypatch.setattr(om, "frobenius_norm", PLANTED_NORMS[kind])
+    assert not _r0_pin_holds(om.capture_norms)
 
 
 def test_hyperball_norm_invariant_and_fixed_points():
@@ -243,10 +268,3 @@ def test_planted_ns_mistakes_are_caught(kind):
     with np.errstate(all="ignore"):
         err = _ns_svd_error(_ns_variant(kind))
     assert not err <= 1e-3
-
-
-def test_planted_norm_mistake_is_caught():
-    def bad_norm(x):
-        return float(np.sum(np.abs(np.asarray(x, np.float64))))
-    w = np.array([[3.0, -4.0], [12.0, 0.0]], np.float32)
-    assert bad_norm(w) != 13.0
