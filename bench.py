@@ -559,7 +559,11 @@ def main():
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
         "e2e": e2e,
-        "kernels": {k: {"launches": v["launches"], "ms_per_step": v["ms"] / prof_steps} for k, v in prof.items()},
+        "kernels": {k: {"launches": v["launches"], "ms_per_step": v["ms"] / prof_steps,
+                        **({"tflops": v["flops"] / (v["ms"] / 1000.0) / 1e12} if v["flops"] and v["ms"] > 0 else {}),
+                        **({"GB/s": v["bytes"] / (v["ms"] / 1000.0) / 1e9} if not v["flops"] and v["bytes"] and
+                           v["ms"] > 0 else {})}
+                    for k, v in prof.items()},
         "kernels_timing": f"per kind, the union of its launches' event intervals over {prof_steps} profiled steps "
                           "(not the headline loop, which runs without per-launch events); with side streams an "
                           "interval includes time a launch waits for SMs held by other buckets' launches",

@@ -49,7 +49,7 @@ EXPORTS = (
     "muonh_test_gemm_timeout",
 )
 
-STATIC_SCRATCH_BYTES = 80 * 1024 * 1024
+STATIC_SCRATCH_BYTES = 96 * 1024 * 1024
 TEST_TIMEOUT_WS_BYTES = 512 * 1024
 
 

@@ -179,6 +179,8 @@ struct Bucket {
     long long upart0;                         // first ||U||^2 partial of this bucket (index into the
                                               // plan's partial region; written by the last apply GEMM)
     int tiles1, tiles2;                       // apply tiles per matrix: 1-SM and pair kernel
+    int gsplits = 1;                          // K ranges of its pair-kernel Gram (tc::gram_splits)
+    size_t off_kpart = 0, off_kcount = 0;     // split-K Gram partials and arrival counters
     size_t x_elems() const { return (size_t)G * R * ld_x; }
 };
 
@@ -219,6 +221,8 @@ std::string plan_key(const int64_t* rc, int n, uint32_t flags) {
     return k;
 }
 
+// Buckets whose pair-kernel Gram has few tiles get split-K partial buffers
+// (tc::gram_splits).
 Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
     (void)flags;
     Plan P;
@@ -301,6 +305,14 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
             g_in_group += B.G;
             B.tiles1 = tc::tiles_per_matrix(NS_APPLY, B.R, B.C);
             B.tiles2 = tc::pair_tiles_per_matrix(NS_APPLY, B.R, B.C);
+            if (!B.small) {
+                const long long gtiles = (long long)B.G * tc::pair_tiles_per_matrix(NS_GRAM, B.s, B.s);
+                B.gsplits = tc::gram_splits(gtiles, B.l);
+                if (B.gsplits > 1) {
+                    B.off_kpart = take(tc::kSplitPartialBytesPerTile * (size_t)gtiles * B.gsplits);
+                    B.off_kcount = take(tc::kSplitCountBytesPerTile * (size_t)gtiles);
+                }
+            }
             B.upart0 = n_upart;
             n_upart += (long long)B.G * std::max((long long)B.tiles1 * tc::kUPartsPerTile1,
                                                  (long long)B.tiles2 * tc::kUPartsPerTilePair);
@@ -682,6 +694,18 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         g.sym_bf16 = reinterpret_cast<__nv_bfloat16*>(ws + B.off_aop);
         g.scale = it == 0 ? sc.inv_nu2 + B.first : nullptr;
         g.status = status;
+        if (B.gsplits > 1 && pair != tc::kGemmSingle) {
+            // split K: the arrival counters start at zero (each launch leaves them at zero)
+            g.splits = B.gsplits;
+            g.kpart = reinterpret_cast<float*>(ws + B.off_kpart);
+            g.kcount = reinterpret_cast<int*>(ws + B.off_kcount);
+            if (it == 0) {
+                const size_t cnt_bytes =
+                    tc::kSplitCountBytesPerTile * (size_t)B.G * tc::pair_tiles_per_matrix(NS_GRAM, B.s, B.s);
+                const int r = sy.check_on(cur, cudaMemsetAsync(g.kcount, 0, cnt_bytes, cur), "split-K counters");
+                if (r) return r;
+            }
+        }
         const double G = B.G, S = B.s, L = B.l;
         cudaError_t e;
         {
@@ -876,6 +900,10 @@ int get_status_ptr(uint32_t** p) {
 
 // Lets other translation units of the library report an error text.
 int report_error(int code, const char* msg) { return fail(code, msg); }
+
+int orthogonalize_impl(const void* in, int in_dtype, void* out, int out_dtype, int64_t rows, int64_t cols,
+                       int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags, void* workspace,
+                       size_t ws_bytes, void* stream);
 
 }  // namespace muonh
 
@@ -1177,6 +1205,19 @@ int muonh_orthogonalize(const void* in, int in_dtype, void* out, int out_dtype, 
                         int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags, void* workspace,
                         size_t ws_bytes, void* stream) {
     g_last_error.clear();
+    return muonh::orthogonalize_impl(in, in_dtype, out, out_dtype, rows, cols, ns_steps, ns_coeffs, eps, flags,
+                                     workspace, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace muonh {
+
+// Newton-Schulz of one matrix (muonh_orthogonalize).
+int orthogonalize_impl(const void* in, int in_dtype, void* out, int out_dtype, int64_t rows, int64_t cols,
+                       int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags, void* workspace,
+                       size_t ws_bytes, void* stream) {
+    g_last_error.clear();
     if (!in || !out || !aligned16(in) || !aligned16(out))
         return fail(MUONH_ERR_INVALID_ARG, "in/out NULL or not 16-byte aligned");
     if ((in_dtype != MUONH_DTYPE_F32 && in_dtype != MUONH_DTYPE_BF16) ||
@@ -1244,6 +1285,10 @@ int muonh_orthogonalize(const void* in, int in_dtype, void* out, int out_dtype, 
     }
     return r;
 }
+
+}  // namespace muonh
+
+extern "C" {
 
 int muonh_partition(const muonh_matrix_t* mats, int n, int world_size, int* owner_out) {
     g_last_error.clear();

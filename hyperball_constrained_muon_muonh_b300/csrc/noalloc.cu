@@ -39,7 +39,7 @@ extern "C" int muonh_orthogonalize_static(const void* in, int in_dtype, void* ou
     if (need > kScratchBytes)
         return muonh::report_error(MUONH_ERR_WORKSPACE,
                                    "muonh_orthogonalize_static: this shape needs more scratch than the "
-                                   "library's fixed 80 MiB array; use muonh_orthogonalize with a workspace");
+                                   "library's fixed 96 MiB array; use muonh_orthogonalize with a workspace");
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return muonh::report_error(MUONH_ERR_CUDA, cudaGetErrorString(e));

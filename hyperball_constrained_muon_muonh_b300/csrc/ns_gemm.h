@@ -58,6 +58,16 @@ struct GemmParams {
     float wdecay;           // NS_OUT_W: 1 - lr*weight_decay
     float ca, cb, cc;
     uint32_t* status;       // device status word
+    // Split K (the Gram in the pair kernel, when a launch has few tiles): the
+    // K steps are cut into `splits` ranges of kb_per_split 64-wide steps
+    // (even); each (tile, range) is a work unit.  Every unit writes its
+    // partial product to kpart; the last unit of a tile to finish sums the
+    // partials in range order and runs the epilogue, so the result does not
+    // depend on which finishes last.
+    int splits;             // 1: no split
+    int kb_per_split;
+    float* kpart;           // [splits][tiles][2 CTAs][8 warps][4096] fp32
+    int* kcount;            // [tiles][2][8] arrivals: zero before a launch, and again after it
     unsigned long long timeout_ns;   // limit of every pipeline wait (0: the default, 4 s)
     int test_no_loads;      // test hook: the TMA producer issues nothing, so the first wait of the
                             // MMA issuer runs out (nothing is in flight when the kernel gives up)
@@ -74,6 +84,11 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
 int pair_cluster_capacity();
 int tiles_per_matrix(int mode, int M, int N);
 int pair_tiles_per_matrix(int mode, int M, int N);
+// K ranges a pair-kernel Gram launch of `tiles` tiles with K = `K` is split
+// into, and the workspace it needs (partials and arrival counters).
+int gram_splits(long long tiles, int K);
+constexpr size_t kSplitPartialBytesPerTile = 2 * 8 * 4096 * sizeof(float);
+constexpr size_t kSplitCountBytesPerTile = 2 * 8 * sizeof(int);
 // ||U||^2 partials one apply tile writes: one per epilogue warp (8 per CTA,
 // two CTAs per tile in the pair kernel).
 constexpr int kUPartsPerTile1 = 8, kUPartsPerTilePair = 16;

@@ -361,6 +361,20 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
         // ---- Newton-Schulz iterations ----
         for (int it = 0; it < p.ns_steps; ++it) {
             const bool first = it == 0, last = it + 1 == p.ns_steps;
+            if (last && threadIdx.x == 0) {
+                // While the last iteration runs on chip, pull into L2 this
+                // matrix's weight (read by the write-out) and the gradient and
+                // momentum of this cluster's next matrix (read by its load
+                // phase), so those phases read L2 instead of HBM.
+                if (rank == 1) {
+                    prefetch_l2(D.w, (size_t)R * C * 4);
+                } else if (mi + (int)cluster_count() < b.n) {
+                    const SmallDesc& Dn = b.d[mi + (int)cluster_count()];
+                    const size_t el = (size_t)Dn.rows * Dn.cols;
+                    prefetch_l2(Dn.g, el * (p.grad_bf16 ? 2 : 4));
+                    prefetch_l2(Dn.m, el * 4);
+                }
+            }
             mma_gram(xr, tmem + 256);
             wait_mma();
             const float sa = first ? inv * inv : 1.f;
@@ -429,6 +443,8 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
             }
             cluster_sync();
         } else {
+            // U = W - lr*O goes to the accumulator columns (free now), so W is
+            // read once
             double up = 0.0;
 #pragma unroll 1
             for (int k = 0; k < 4; ++k) {
@@ -439,11 +455,13 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
                 float acc = 0.f;
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
-                    const float u = fmaf(nlr, o[t], wv[t]);
-                    if (row_ok && j0 + t < l) acc = fmaf(u, u, acc);
+                    wv[t] = fmaf(nlr, o[t], wv[t]);
+                    if (row_ok && j0 + t < l) acc = fmaf(wv[t], wv[t], acc);
                 }
                 up += (double)acc;
+                tmem_st32(tacc + j0, wv);
             }
+            tmem_st_wait();
             const double rho2 = pair_sum(up, red, peer, peer_remote, (int)rank);
             const bool degenerate = !isfinite(rho2) || rho2 == 0.0;
             if (!keep && degenerate && threadIdx.x == 0 && rank == 0)
@@ -453,15 +471,16 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
 #pragma unroll 1
                 for (int k = 0; k < 4; ++k) {
                     const int j0 = 128 * h + 32 * k;
-                    float o[32], wv[32];
-                    tmem_ld32(tx + j0, o);
-                    load_w(D, tall, C, i, j0, row_ok, l, wv);
+                    float u[32];
+                    tmem_ld32(tacc + j0, u);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) wv[t] = f * fmaf(nlr, o[t], wv[t]);
-                    store_w(D, tall, C, i, j0, row_ok, l, wv);
+                    for (int t = 0; t < 32; ++t) u[t] = f * u[t];
+                    store_w(D, tall, C, i, j0, row_ok, l, u);
                 }
             }
-            cluster_sync();   // the reduction slots are free again
+            tc_fence_before();
+            cluster_sync();   // the reduction slots and the accumulator are free again
+            tc_fence_after();
         }
     }
 

@@ -31,6 +31,9 @@
 
 #include <cuda.h>
 
+#include <algorithm>
+#include <type_traits>
+
 #include "common.cuh"
 #include "ns_gemm.h"
 #include "tc_ptx.cuh"
@@ -113,7 +116,7 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int local, int&
     nj = (m >> 1) + local;
 }
 
-// ---- epilogues -----------------------------------------------------------------
+// ---- epilogues, staged (one-K-step pipelines) -------------------------------------
 // tcgen05.ld gives each lane one accumulator row (32 consecutive columns).
 // Row-wise global access from that layout touches 32 rows per instruction,
 // so each warp stages its 32 x 32 slice in shared memory and reads it back
@@ -166,7 +169,7 @@ __device__ __forceinline__ void prefetch_rm(const float* base, int ld, int M, in
 
 // Prefetch for POLY: A[i][j] for this lane's row i and columns j0..j0+31,
 // read as A[j][i] (A is exactly symmetric), which is coalesced over lanes.
-__device__ __forceinline__ void prefetch_a(const GemmParams& p, int g, int i0, int lane, int j0, float (&ap)[32]) {
+__device__ __forceinline__ void prefetch_a_st(const GemmParams& p, int g, int i0, int lane, int j0, float (&ap)[32]) {
     const int i = i0 + lane;
     const float* a = p.a_f32 + (size_t)g * p.ld_s * p.M + i;
 #pragma unroll
@@ -180,7 +183,7 @@ __device__ __forceinline__ void prefetch_a(const GemmParams& p, int g, int i0, i
 // NS_IN_SRC the matrix's own input, row stride N).  y = sc*(a*x + (B X)); with NS_OUT_U, u = W - lr*y replaces
 // y and u^2 is added to hacc for the elements inside the matrix.
 template <int VAR>
-__device__ __forceinline__ void apply_slice(const GemmParams& p, const NsIO& io, bool keep_w, int g, int i0,
+__device__ __forceinline__ void apply_slice_st(const GemmParams& p, const NsIO& io, bool keep_w, int g, int i0,
                                             int lane, int j0, const float (&v)[32], float* st,
                                             const float4 (&xp)[8], const float4 (&wp)[8], float sc, float& hacc) {
     stage_rows(st, lane, v);
@@ -234,7 +237,7 @@ __device__ __forceinline__ void apply_slice(const GemmParams& p, const NsIO& io,
 // GRAM / POLY: element (i, j) is written when j >= i, its mirror (j, i) when
 // j > i; tiles entirely below the diagonal are never scheduled.
 template <int MODE>
-__device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, int lane, int j0, float (&v)[32],
+__device__ __forceinline__ void sym_slice_st(const GemmParams& p, int g, int i0, int lane, int j0, float (&v)[32],
                                           float* st, const float (&ap)[32], float sc) {
     const int M = p.M, N = p.N;
     const int i = i0 + lane;
@@ -281,19 +284,246 @@ __device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, in
     }
 }
 
+// ---- epilogues, fragment layout (two-K-step pipelines) ------------------------------
+// The accumulator is read with tcgen05.ld.16x256b: two loads (TMEM lanes
+// +0..15 and +16..31 of this warp's lane quarter) of four 8-column groups
+// give each thread, for a 32 x 32 slice at (i0, j0), the values
+//   v[8*rr + 2*j + e] = acc[i0 + 8*rr + lane/4][j0 + 8*j + 2*(lane%4) + e]
+// for rr, j in 0..3 and e in 0..1: four rows and four column pairs.  Four
+// consecutive lanes hold 8 consecutive columns (32 bytes) of one row, so
+// every row-wise global access is in whole 32-byte sectors without staging
+// the slice in shared memory; for the mirror of a symmetric product, eight
+// lanes with the same lane%4 hold 8 consecutive rows of one column, which
+// are 8 consecutive elements of the transposed row.  Operands the epilogue
+// reads (X for APPLY, A for POLY) are loaded in the same layout one slice
+// ahead so that their latency overlaps the previous slice's stores.
+
+__device__ __forceinline__ int quad_row(int lane, int rr) { return 8 * rr + (lane >> 2); }
+__device__ __forceinline__ int quad_col(int lane, int j) { return 8 * j + 2 * (lane & 3); }
+
+__device__ __forceinline__ void store_bf16x2(__nv_bfloat16* dst, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(a, b);
+}
+
+// Prefetch in the fragment layout from a row-major array with row stride
+// `ld`: xp[rr][j] = X[i0 + row(rr)][j0 + col(j) .. +1].  For the fp32 state
+// the row stride is a multiple of 8 elements, so a pair at a column < N stays
+// inside the padded row (padding columns are never read back); a caller's
+// buffer (row stride N) is read this way only when N % 4 == 0.
+__device__ __forceinline__ void prefetch_q(const float* base, int ld, int M, int N, int i0, int lane, int j0,
+                                           float2 (&xp)[16]) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+        const int row = i0 + quad_row(lane, rr);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = j0 + quad_col(lane, j);
+            xp[4 * rr + j] = (row < M && col < N)
+                                 ? __ldcs(reinterpret_cast<const float2*>(base + (size_t)row * ld + col))
+                                 : make_float2(0.f, 0.f);
+        }
+    }
+}
+
+// Prefetch for POLY: A[i][j] (fp32, both triangles written by the Gram) at
+// this thread's positions on or above the diagonal.
+__device__ __forceinline__ void prefetch_a(const GemmParams& p, int g, int i0, int lane, int j0, float2 (&ap)[16]) {
+    const float* a = p.a_f32 + (size_t)g * p.ld_s * p.M;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+        const int row = i0 + quad_row(lane, rr);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = j0 + quad_col(lane, j);
+            ap[4 * rr + j] = (row < p.M && col < p.N && col + 1 >= row)
+                                 ? *reinterpret_cast<const float2*>(a + (size_t)row * p.ld_s + col)
+                                 : make_float2(0.f, 0.f);
+        }
+    }
+}
+
+// APPLY slice: y = sc*(a*x + (B X)), X from the fp32 state (or with
+// NS_IN_SRC the matrix's own input, row stride N).  With NS_OUT_U, u = W -
+// lr*y replaces y and u^2 is added to hacc for the elements inside the
+// matrix; with NS_OUT_W the new weight goes to the caller's buffers.
+template <int VAR>
+__device__ __forceinline__ void apply_slice(const GemmParams& p, const NsIO& io, bool keep_w, int g, int i0,
+                                            int lane, int j0, const float (&v)[32], const float2 (&xp)[16],
+                                            const float2 (&wp)[16], float sc, float& hacc) {
+    float* xs = p.x_state + (size_t)g * p.ld_x * p.M;
+    __nv_bfloat16* xo = p.x_op_out ? p.x_op_out + (size_t)g * p.ld_x * p.M : nullptr;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+        const int row = i0 + quad_row(lane, rr);
+        if (row >= p.M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = j0 + quad_col(lane, j);
+            if (col >= p.N) continue;
+            const int q = 4 * rr + j;
+            float2 y;
+            y.x = sc * fmaf(p.ca, xp[q].x, v[2 * q]);
+            y.y = sc * fmaf(p.ca, xp[q].y, v[2 * q + 1]);
+            if (VAR & NS_OUT_U) {
+                y.x = fmaf(p.nlr, y.x, wp[q].x);
+                y.y = fmaf(p.nlr, y.y, wp[q].y);
+                hacc = fmaf(y.x, y.x, hacc);
+                if (col + 1 < p.N) hacc = fmaf(y.y, y.y, hacc);
+            }
+            if (VAR & NS_OUT_W) {
+                // new weight, written to the caller's buffers (row stride N)
+                if (!keep_w) {
+                    float2 u;
+                    u.x = fmaf(p.nlr, y.x, p.wdecay * wp[q].x);
+                    u.y = fmaf(p.nlr, y.y, p.wdecay * wp[q].y);
+                    const size_t woff = (size_t)row * p.N + col;
+                    __stcs(reinterpret_cast<float2*>(io.w + woff), u);
+                    if (io.wb) store_bf16x2(reinterpret_cast<__nv_bfloat16*>(io.wb) + woff, u.x, u.y);
+                }
+                continue;
+            }
+            // the fp32 state is read again only by the next apply's epilogue:
+            // streaming store, so it does not push the GEMM operands out of L2
+            const size_t off = (size_t)row * p.ld_x + col;
+            __stcs(reinterpret_cast<float2*>(xs + off), y);
+            if (xo) store_bf16x2(xo + off, y.x, y.y);
+        }
+    }
+}
+
+// GRAM / POLY slice: element (i, j) is written when j >= i, its mirror (j, i)
+// when j > i; tiles entirely below the diagonal are never scheduled.
+template <int MODE>
+__device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, int lane, int j0, const float (&v)[32],
+                                          const float2 (&ap)[16], float sc) {
+    const int M = p.M, N = p.N;
+    const size_t mbase = (size_t)g * p.ld_s * M;
+    float* af = (MODE == NS_GRAM) ? p.a_f32 + mbase : nullptr;
+    __nv_bfloat16* ob = p.sym_bf16 + mbase;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+        const int row = i0 + quad_row(lane, rr);
+        if (row >= M) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = j0 + quad_col(lane, j);
+            if (col >= N || col + 1 < row) continue;
+            const int q = 4 * rr + j;
+            float y0, y1;
+            if (MODE == NS_GRAM) {
+                y0 = sc * v[2 * q];
+                y1 = sc * v[2 * q + 1];
+            } else {
+                y0 = fmaf(p.cb, ap[q].x, p.cc * v[2 * q]);
+                y1 = fmaf(p.cb, ap[q].y, p.cc * v[2 * q + 1]);
+            }
+            const size_t off = (size_t)row * p.ld_s + col;
+            const bool in1 = col + 1 < N;
+            if (col >= row && in1) {
+                if (MODE == NS_GRAM) *reinterpret_cast<float2*>(af + off) = make_float2(y0, y1);
+                store_bf16x2(ob + off, y0, y1);
+            } else {
+                // col + 1 == row (only y1 is on the diagonal), or col + 1 == N
+                if (col >= row) {
+                    if (MODE == NS_GRAM) af[off] = y0;
+                    ob[off] = __float2bfloat16_rn(y0);
+                }
+                if (in1 && col + 1 >= row) {
+                    if (MODE == NS_GRAM) af[off + 1] = y1;
+                    ob[off + 1] = __float2bfloat16_rn(y1);
+                }
+            }
+            // mirrors (strictly above the diagonal)
+            if (col > row) {
+                if (MODE == NS_GRAM) af[(size_t)col * p.ld_s + row] = y0;
+                ob[(size_t)col * p.ld_s + row] = __float2bfloat16_rn(y0);
+            }
+            if (in1 && col + 1 > row) {
+                if (MODE == NS_GRAM) af[(size_t)(col + 1) * p.ld_s + row] = y1;
+                ob[(size_t)(col + 1) * p.ld_s + row] = __float2bfloat16_rn(y1);
+            }
+        }
+    }
+}
+
 // One accumulator tile's epilogue for one warp: rows i0..i0+31 (TMEM lane
 // quarter of this warp), columns jb..jb+127 (four 32-column slices).  Loads
 // the operands the epilogue reads one slice ahead, waits for the
 // accumulator, releases it after the last TMEM read (`release`), and for
 // NS_OUT_U writes this warp's ||U||^2 partial to *upart_slot (0 when the
 // warp's rows or columns fall outside the matrix).  False if the wait gave up.
-template <int MODE, int VAR, class Release>
+// QUAD selects the fragment-layout epilogue (no staging); otherwise slices
+// pass through the warp's 4 KB staging tile `st`.
+//
+// Split-K Gram (`kp0` set): this warp's partial for K range `split` goes to
+// kp0 + split*kstride (a private layout: value i of slice k of lane l at
+// (32k + i)*32 + l, so every store is one coalesced 128-byte row); after the
+// stores, one arrival on *kcnt.  The warp that brings the count to `splits`
+// resets it, sums the partials in range order and runs the epilogue.
+template <int MODE, int VAR, bool QUAD, class Release>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0, int jb, uint32_t tfull_bar,
                                               uint32_t acc_phase, uint32_t trow, float* st, int lane,
-                                              volatile int* abort_flag, double* upart_slot, Release release) {
+                                              volatile int* abort_flag, double* upart_slot, Release release,
+                                              float* kp0 = nullptr, size_t kstride = 0, int split = 0,
+                                              int* kcnt = nullptr) {
     const int nsl = max(0, min(BN / 64, (p.N - jb + 31) / 32));
     float sc = 1.f;
     if (MODE != NS_POLY && p.scale) sc = p.scale[g];
+    auto load_slice = [&](uint32_t taddr, float (&v)[32]) {
+        if constexpr (QUAD) tmem_ld_quad32(taddr, v);
+        else tmem_ld32(taddr, v);
+    };
+    if (MODE == NS_GRAM && kp0 != nullptr) {
+        if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, wait_limit(p))) return false;
+        tc_fence_after();
+        if (nsl == 0) {   // no column of this warp's half lies inside the matrix, for any range
+            release();
+            return true;
+        }
+        float* mine = kp0 + (size_t)split * kstride;
+#pragma unroll
+        for (int k = 0; k < BN / 64; ++k) {
+            if (k < nsl) {
+                float v[32];
+                load_slice(trow + 32 * k, v);
+                if (k == nsl - 1) {
+                    tc_fence_before();
+                    release();
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) __stcg(mine + (32 * k + i) * 32 + lane, v[i]);
+            }
+        }
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(kcnt, 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev != p.splits - 1) return true;
+        __threadfence();
+        if (lane == 0) *kcnt = 0;   // every range has arrived: ready for the next launch
+#pragma unroll
+        for (int k = 0; k < BN / 64; ++k) {
+            if (k < nsl) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __ldcg(kp0 + (32 * k + i) * 32 + lane);
+                for (int sp = 1; sp < p.splits; ++sp) {
+                    const float* part = kp0 + (size_t)sp * kstride;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] += __ldcg(part + (32 * k + i) * 32 + lane);
+                }
+                if constexpr (QUAD) {
+                    const float2 unused[16] = {};
+                    sym_slice<NS_GRAM>(p, g, i0, lane, jb + 32 * k, v, unused, sc);
+                } else {
+                    const float unused[32] = {};
+                    sym_slice_st<NS_GRAM>(p, g, i0, lane, jb + 32 * k, v, st, unused, sc);
+                }
+            }
+        }
+        return true;
+    }
     // X source of the apply epilogue: the fp32 state (row stride ld_x), or
     // the matrix's own input (row stride N; the variants need N % 4 == 0)
     NsIO io{nullptr, nullptr, nullptr};
@@ -314,12 +544,26 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
     constexpr bool reads_w = MODE == NS_APPLY && (VAR & (NS_OUT_U | NS_OUT_W));
     constexpr bool ahead = !reads_w;
     const bool keep_w = (MODE == NS_APPLY && (VAR & NS_OUT_W)) ? p.mflags[g] != 0 : false;
-    float4 xc[8], xn[8], wc[8];
+    // prefetched operands: 32 floats per slice in either layout
+    using Pre = typename std::conditional<QUAD, float2[16], float4[8]>::type;
+    Pre xc, xn, wc;
     float ac[32], an[32];
+    auto pre_x = [&](int j0, Pre& dst) {
+        if constexpr (QUAD) prefetch_q(xbase, xld, p.M, p.N, i0, lane, j0, dst);
+        else prefetch_rm(xbase, xld, p.M, p.N, i0, lane, j0, dst);
+    };
+    auto pre_w = [&](int j0, Pre& dst) {
+        if constexpr (QUAD) prefetch_q(io.w, p.N, p.M, p.N, i0, lane, j0, dst);
+        else prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, j0, dst);
+    };
+    auto pre_a = [&](int j0, float (&dst)[32]) {
+        if constexpr (QUAD) prefetch_a(p, g, i0, lane, j0, *reinterpret_cast<float2(*)[16]>(&dst));
+        else prefetch_a_st(p, g, i0, lane, j0, dst);
+    };
     if (nsl > 0) {
-        if (MODE == NS_APPLY) prefetch_rm(xbase, xld, p.M, p.N, i0, lane, jb, xc);
-        if (reads_w) prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, jb, wc);
-        if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, jb, ac);
+        if (MODE == NS_APPLY) pre_x(jb, xc);
+        if (reads_w) pre_w(jb, wc);
+        if (MODE == NS_POLY) pre_a(jb, ac);
     }
     if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, wait_limit(p))) return false;
     tc_fence_after();
@@ -330,28 +574,30 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
         if (k < nsl) {
             const int j0 = jb + 32 * k;
             if (!ahead && k > 0) {
-                prefetch_rm(xbase, xld, p.M, p.N, i0, lane, j0, xc);
-                prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, j0, wc);
+                pre_x(j0, xc);
+                pre_w(j0, wc);
             }
             float v[32];
-            tmem_ld32(trow + 32 * k, v);
+            load_slice(trow + 32 * k, v);
             if (k == nsl - 1) {
                 // last read of this accumulator by this warp
                 tc_fence_before();
                 release();
             }
             if (k + 1 < nsl) {
-                if (MODE == NS_APPLY && ahead) prefetch_rm(xbase, xld, p.M, p.N, i0, lane, j0 + 32, xn);
-                if (MODE == NS_POLY) prefetch_a(p, g, i0, lane, j0 + 32, an);
+                if (MODE == NS_APPLY && ahead) pre_x(j0 + 32, xn);
+                if (MODE == NS_POLY) pre_a(j0 + 32, an);
             }
             if (MODE == NS_APPLY) {
-                apply_slice<VAR>(p, io, keep_w, g, i0, lane, j0, v, st, xc, wc, sc, hacc);
+                if constexpr (QUAD) apply_slice<VAR>(p, io, keep_w, g, i0, lane, j0, v, xc, wc, sc, hacc);
+                else apply_slice_st<VAR>(p, io, keep_w, g, i0, lane, j0, v, st, xc, wc, sc, hacc);
                 if (ahead) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) xc[u] = xn[u];
+                    for (int u = 0; u < (QUAD ? 16 : 8); ++u) xc[u] = xn[u];
                 }
             } else {
-                sym_slice<MODE>(p, g, i0, lane, j0, v, st, ac, sc);
+                if constexpr (QUAD) sym_slice<MODE>(p, g, i0, lane, j0, v, *reinterpret_cast<float2(*)[16]>(&ac), sc);
+                else sym_slice_st<MODE>(p, g, i0, lane, j0, v, st, ac, sc);
                 if (MODE == NS_POLY) {
 #pragma unroll
                     for (int u = 0; u < 32; ++u) ac[u] = an[u];
@@ -497,7 +743,6 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const int e = warp - 2;
         const int q = warp & 3;
         const int h = e >> 2;
-        float* st = stage_base + e * ST_FLOATS;
         int acc = 0;
         uint32_t acc_phase = 0;
         const uint32_t tempty_bar = tempty0;
@@ -508,8 +753,9 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + h * (BN / 2));
             const uint32_t te = tempty_bar + 8 * acc;
             double* slot = (VAR & NS_OUT_U) ? p.upart + (size_t)t * kUPartsPerTile1 + e : nullptr;
-            if (!epilogue_tile<MODE, VAR>(p, g, mi * BM + q * 32, nj * BN + h * (BN / 2), tfull0 + 8 * acc,
-                                          acc_phase, trow, st, lane, abort_flag, slot, [&]() { mbar_arrive(te); }))
+            if (!epilogue_tile<MODE, VAR, false>(p, g, mi * BM + q * 32, nj * BN + h * (BN / 2), tfull0 + 8 * acc,
+                                                 acc_phase, trow, stage_base + e * ST_FLOATS, lane, abort_flag, slot,
+                                                 [&]() { mbar_arrive(te); }))
                 break;
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
@@ -542,11 +788,14 @@ ns_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 // tmem-empty barrier.
 namespace pair {
 
-constexpr int STAGES2 = 6;
+constexpr int STAGES2 = 6;                            // one-K-step stages (32 KB each) of the ring
 constexpr int A2_BYTES = BM * BK * 2;                 // 16 KB: this CTA's 128 rows of A
 constexpr int B2_BYTES = (BN / 2) * BK * 2;           // 16 KB: this CTA's 128 rows of B
 constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
+// the ring, barriers and exit state, and the epilogue warps' staging tiles
+// (used by the one-K-step pipeline's epilogue)
 constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + 1024 + 256 + EPI_WARPS * ST_FLOATS * 4;
+static_assert(SMEM2_BYTES <= 232448, "shared memory per CTA");
 
 // Pipeline shape of the pair kernel: KPS K steps of BK per stage.  Alone,
 // TMA moves about 56 bytes per SM clock into shared memory with 16 KB boxes
@@ -561,7 +810,7 @@ constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + 1024 + 256 + EPI_WARPS * ST
 // flight, so the host takes two steps only where that measured faster.
 template <int KPS>
 struct PairPipe {
-    static constexpr int STAGES = 6 / KPS;
+    static constexpr int STAGES = STAGES2 / KPS;
     static constexpr int A_STEP = BM * BK * 2;          // 16 KB: one K step of this CTA's A rows
     static constexpr int B_STEP = (BN / 2) * BK * 2;    // 16 KB: one K step of this CTA's B rows
     static constexpr int A_BYTES = KPS * A_STEP;
@@ -689,9 +938,11 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    // work units: (K range, tile), the range outermost; one range unless the
+    // Gram is split (splits > 1)
     const int total = p.G * p.tiles_per_mat;
+    const int units = total * p.splits;
     const int num_kb = (p.K + BK - 1) / BK;
-    const int num_ks = (num_kb + KPS - 1) / KPS;
     const int cid = (int)cluster_id(), ncl = (int)cluster_count();
 
     if (warp == 0 && lane == 0) {
@@ -700,7 +951,9 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         uint32_t phase = 0;
         bool ok = !p.test_no_loads;
         int fills = 0;
-        for (int t = cid; t < total && ok; t += ncl) {
+        for (int u = cid; u < units && ok; u += ncl) {
+            const int split = u / total, t = u - split * total;
+            const int kb0 = split * p.kb_per_split, kb1 = min(num_kb, kb0 + p.kb_per_split);
             const int g = t / p.tiles_per_mat;
             int mp, nj;
             pair_coords(p, t - g * p.tiles_per_mat, mp, nj);
@@ -709,7 +962,7 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             // diagonal tile of a symmetric product: this CTA's B rows are its A
             // rows (same operand tensor), so B is not fetched
             const bool diag = MODE != NS_APPLY && mp == nj;
-            for (int ks = 0; ks < num_ks; ++ks) {
+            for (int ks = kb0 / KPS; ks * KPS < kb1; ++ks) {
                 if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, tlimit)) { ok = false; break; }
                 const uint32_t fb_local = full0 + 8 * stage;
                 const uint32_t fb = map_to_rank(fb_local, 0);
@@ -766,7 +1019,9 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         uint32_t acc_phase = 0;
         bool ok = true;
         int consumed = 0;
-        for (int t = cid; t < total && ok; t += ncl) {
+        for (int u = cid; u < units && ok; u += ncl) {
+            const int split = u / total, t = u - split * total;
+            const int kb0 = split * p.kb_per_split, kb1 = min(num_kb, kb0 + p.kb_per_split);
             bool diag = false;
             if (MODE != NS_APPLY) {
                 const int g = t / p.tiles_per_mat;
@@ -780,19 +1035,20 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag, p.status, tlimit)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int ks = 0; ks < num_ks; ++ks) {
+            for (int ks = kb0 / KPS; ks * KPS < kb1; ++ks) {
                 if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, tlimit)) { ok = false; break; }
                 ++consumed;
                 tc_fence_after();
 #pragma unroll
                 for (int j = 0; j < KPS; ++j) {
                     const int kb = ks * KPS + j;
-                    if (KPS > 1 && kb >= num_kb) break;
+                    if (KPS > 1 && kb >= kb1) break;
                     const uint64_t ad = a_desc0 + (uint64_t)((stage * A2_BYTES + j * Pipe::A_STEP) >> 4);
                     const uint64_t bd = b_base + (uint64_t)((stage * b_stage + j * Pipe::B_STEP) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_bf16_pair(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc, (kb | kk) ? 1u : 0u);
+                        mma_bf16_pair(d_tmem, ad + kk * a_step, bd + kk * b_step, idesc,
+                                      ((kb - kb0) | kk) ? 1u : 0u);
                 }
                 mma_commit_pair(empty0 + 8 * stage);
                 if (++stage == STAGES2) { stage = 0; phase ^= 1; }
@@ -811,11 +1067,13 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
         const int e = warp - 2;
         const int q = warp & 3;
         const int h = e >> 2;
-        float* st = stage_base + e * ST_FLOATS;
         const uint32_t tempty_leader = map_to_rank(tempty0, 0);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = cid; t < total; t += ncl) {
+        const bool split_k = MODE == NS_GRAM && p.splits > 1;
+        const size_t kstride = (size_t)total * 2 * 8 * 4096;
+        for (int u = cid; u < units; u += ncl) {
+            const int split = u / total, t = u - split * total;
             const int g = t / p.tiles_per_mat;
             int mp, nj;
             pair_coords(p, t - g * p.tiles_per_mat, mp, nj);
@@ -824,12 +1082,18 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
             double* slot = (VAR & NS_OUT_U)
                                ? p.upart + ((size_t)t * 2 + rank) * (kUPartsPerTilePair / 2) + e
                                : nullptr;
-            if (!epilogue_tile<MODE, VAR>(p, g, mp * 2 * BM + (int)rank * BM + q * 32, nj * BN + h * (BN / 2),
-                                          tfull0 + 8 * acc, acc_phase, trow, st, lane, abort_flag, slot,
+            const size_t wslot = ((size_t)t * 2 + rank) * 8 + e;   // this warp's (tile, CTA, warp)
+            // two-K-step stages take the fragment-layout epilogue (it measured
+            // faster there), one-K-step stages the staged one
+            if (!epilogue_tile<MODE, VAR, KPS == 2>(p, g, mp * 2 * BM + (int)rank * BM + q * 32,
+                                          nj * BN + h * (BN / 2), tfull0 + 8 * acc, acc_phase, trow,
+                                          stage_base + e * ST_FLOATS, lane, abort_flag, slot,
                                           [&]() {
                                               __syncwarp();
                                               if (lane == 0) remote_arrive(te);
-                                          }))
+                                          },
+                                          split_k ? p.kpart + wslot * 4096 : nullptr, kstride, split,
+                                          split_k ? p.kcount + wslot : nullptr))
                 break;
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
@@ -957,6 +1221,28 @@ int pair_tiles_per_matrix(int mode, int M, int N) {
     return cnt;
 }
 
+// A Gram launch with fewer pair tiles than twice the CTA pairs of a B300
+// (74) leaves SMs idle for its whole duration: its K steps (>= 16 per range)
+// are cut into ranges so that the units number at least 148.
+#ifndef MUONH_SPLIT_MAX
+#define MUONH_SPLIT_MAX 8
+#endif
+#ifndef MUONH_SPLIT_TARGET
+#define MUONH_SPLIT_TARGET 148
+#endif
+#ifndef MUONH_SPLIT_MIN_STEPS
+#define MUONH_SPLIT_MIN_STEPS 16
+#endif
+int gram_splits(long long tiles, int K) {
+    constexpr long long kTargetUnits = MUONH_SPLIT_TARGET;
+    const int nkb = (K + BK - 1) / BK;
+    if (tiles <= 0 || tiles >= kTargetUnits) return 1;
+    long long sp = (kTargetUnits + tiles - 1) / tiles;
+    sp = std::min<long long>(sp, nkb / MUONH_SPLIT_MIN_STEPS);
+    sp = std::min<long long>(sp, MUONH_SPLIT_MAX);
+    return sp < 1 ? 1 : (int)sp;
+}
+
 template <int MODE, int VAR, int KPS>
 static int max_pair_clusters() {
     static int cached = 0;
@@ -1064,9 +1350,16 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
     // vs 745, apply 635-675 vs 636-669.  Three 64 KB stages keep less data
     // in flight than six 32 KB ones, which only the tall Gram's four 8 KB
     // MN-major boxes per step outweigh; the other launches keep one step.
-    if (kind == kGemmPair &&
-        !(p.mode == NS_GRAM && p.a_mn && (p.K % 64) == 0 && (p.M % 64) == 0 && (p.N % 64) == 0))
-        kind = kGemmPairStep1;
+#ifndef MUONH_KPS2_RULE
+#define MUONH_KPS2_RULE 0
+#endif
+    // MUONH_KPS2_RULE (build-time): 0 two-step stages for the tall Gram only,
+    // 1 for every Gram and polynomial, 2 for every launch whose shape allows
+    const bool two_step_ok = (p.K % 64) == 0 && (!p.a_mn || (p.M % 64) == 0) && (!p.b_mn || (p.N % 64) == 0);
+    const bool two_step_wanted = MUONH_KPS2_RULE == 2   ? true
+                                 : MUONH_KPS2_RULE == 1 ? p.mode != NS_APPLY
+                                                        : (p.mode == NS_GRAM && p.a_mn);
+    if (kind == kGemmPair && !(two_step_ok && two_step_wanted)) kind = kGemmPairStep1;
     const bool multi = kind != kGemmSingle;
     const int a_box = BM;
     const int b_box = kind == kGemmPairStep1 ? BN / 2 : BN;
@@ -1094,8 +1387,22 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
         p.tiles_n = (p.N + BN - 1) / BN;
         p.tiles_per_mat = tiles_per_matrix(p.mode, p.M, p.N);
     }
-    const long long total = (long long)p.G * p.tiles_per_mat;
+    long long total = (long long)p.G * p.tiles_per_mat;
     if (total <= 0) return cudaSuccess;
+    // split K: pair kernel, Gram only; ranges of an even number of K steps, so
+    // one- and two-step pipeline stages cut K at the same places
+    const int num_kb = (p.K + BK - 1) / BK;
+    if (p.splits > 1 && multi && p.mode == NS_GRAM) {
+        if (!p.kpart || !p.kcount) { *why = "split-K Gram without partial buffers"; return cudaErrorInvalidValue; }
+        int len = (num_kb + p.splits - 1) / p.splits;
+        len += len & 1;
+        p.kb_per_split = len;
+        p.splits = (num_kb + len - 1) / len;
+    } else {
+        p.splits = 1;
+        p.kb_per_split = num_kb;
+    }
+    total *= p.splits;
     cudaError_t e = kind == kGemmPair        ? dispatch<kGemmPair>(ta, tb, p, total, st)
                     : kind == kGemmPairStep1 ? dispatch<kGemmPairStep1>(ta, tb, p, total, st)
                                              : dispatch<kGemmSingle>(ta, tb, p, total, st);

@@ -97,6 +97,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (no completion to wait for); the
+// size is rounded down to a multiple of 16 bytes, p must be 16-byte aligned.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+    const uint64_t a = reinterpret_cast<uint64_t>(p);
+    for (size_t off = 0; off + 16 <= bytes;) {
+        size_t n = bytes - off;
+        if (n > (1u << 20)) n = 1u << 20;
+        n &= ~(size_t)15;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a + off), "r"((uint32_t)n) : "memory");
+        off += n;
+    }
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -178,6 +191,36 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 TMEM lanes (this warp's quarter, from taddr's lane) x 32 columns, in
+// the 16x256b fragment layout: two loads (lanes +0..15, +16..31) of four
+// 8-column groups.  v[8*rr + 2*j + e] = row 8*rr + lane/4, column
+// 8*j + 2*(lane%4) + e (rr, j in 0..3; e in 0..1): four consecutive lanes
+// hold 32 contiguous bytes of one row.
+__device__ __forceinline__ void tmem_ld_quad32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        asm volatile(
+            "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[16 * h + 0]), "=r"(r[16 * h + 1]), "=r"(r[16 * h + 2]), "=r"(r[16 * h + 3]),
+              "=r"(r[16 * h + 4]), "=r"(r[16 * h + 5]), "=r"(r[16 * h + 6]), "=r"(r[16 * h + 7]),
+              "=r"(r[16 * h + 8]), "=r"(r[16 * h + 9]), "=r"(r[16 * h + 10]), "=r"(r[16 * h + 11]),
+              "=r"(r[16 * h + 12]), "=r"(r[16 * h + 13]), "=r"(r[16 * h + 14]), "=r"(r[16 * h + 15])
+            : "r"(taddr + ((uint32_t)(16 * h) << 16)));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    // load h, group j, register 2*s + e holds row 16*h + 8*s + lane/4, column 8*j + 2*(lane%4) + e
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    v[8 * (2 * h + s) + 2 * j + e] = __uint_as_float(r[16 * h + 4 * j + 2 * s + e]);
 }
 
 // The inverse of tmem_ld32: lane i writes row i's 32 values.  Completion is

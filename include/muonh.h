@@ -230,8 +230,8 @@ int muonh_orthogonalize(const void* in, int in_dtype, void* out, int out_dtype, 
  * library holds in device memory (a file-scope __device__ variable), on
  * every device that loads the library, until the process exits.  Shapes
  * whose muonh_orthogonalize_workspace_size() exceeds it are rejected with
- * MUONH_ERR_WORKSPACE and a message (muonh_last_error); 2048 x 2048,
- * 1024 x 8192 and anything smaller fit.
+ * MUONH_ERR_WORKSPACE and a message (muonh_last_error); 2048 x 2048 and
+ * 1024 x 8192 fit.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and keeps it, keyed by
@@ -247,7 +247,7 @@ int muonh_orthogonalize(const void* in, int in_dtype, void* out, int out_dtype, 
  * it, so stale contents from an earlier call do not matter.  in_dtype and
  * out_dtype as for muonh_orthogonalize.
  */
-#define MUONH_STATIC_SCRATCH_BYTES (80u * 1024u * 1024u)
+#define MUONH_STATIC_SCRATCH_BYTES (96u * 1024u * 1024u)
 int muonh_orthogonalize_static(const void* in, int in_dtype, void* out, int out_dtype, int64_t rows,
                                int64_t cols, int ns_steps, const float ns_coeffs[3], float eps, uint32_t flags,
                                void* stream);

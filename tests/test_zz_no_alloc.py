@@ -49,7 +49,7 @@ def test_static_rejects_oversized_shapes():
     rc = _lib.lib.muonh_orthogonalize_static(x, _lib.DTYPE_F32, x, _lib.DTYPE_F32, 4096, 4096, 5, COEFFS, 1e-7, 0,
                                              None)
     assert rc == _lib.ERR_WORKSPACE
-    assert b"80 MiB" in _lib.lib.muonh_last_error()
+    assert b"96 MiB" in _lib.lib.muonh_last_error()
 
 
 @pytest.mark.gpu
