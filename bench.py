@@ -406,6 +406,36 @@ def main():
         del opt1
         torch.cuda.empty_cache()
 
+    # ---- multi-GPU only: the sharded step (each rank steps the matrices it
+    # owns, then every updated weight is broadcast from its owner, NCCL inside
+    # the timed region): strong scaling of one step of the set ----
+    sharded = None
+    if world > 1 and args.optimizer == "muonh":
+        try:
+            ws_s = work.weights(dev)
+            sopt = mh.ShardedMuonH(ws_s, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps,
+                                   ns_coeffs=work.coeffs, eps=work.eps, bf16_copies=True, flags=gemm_flags)
+            for t in range(args.warmup):
+                sopt.step(grads[t % 2])
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            s0.record(stream)
+            for t in range(args.steps):
+                sopt.step(grads[t % 2])
+            s1.record(stream)
+            barrier()
+            t_ = torch.tensor([s0.elapsed_time(s1)], device=dev)
+            dist.all_reduce(t_, op=dist.ReduceOp.MAX)
+            sms = t_.item() / args.steps
+            sharded = {"value": 1000.0 / sms, "unit": "steps/s", "ms_per_step": sms, "scaling": "strong",
+                       "what": "one step of the whole set split across the ranks by Newton-Schulz cost "
+                               "(muonh_partition), then one NCCL broadcast per rank of its updated fp32 weights",
+                       "matrices_on_rank0": len(sopt.mine)}
+            del sopt, ws_s
+            torch.cuda.empty_cache()
+        except Exception as exc:  # reported, not fatal: the replica line above stands
+            sharded = {"error": f"{type(exc).__name__}: {exc}"[:300]}
+
     # ---- end to end: host gradients in, status word out, every step ----
     # Each step's gradients come from pinned host memory.  The copy for step
     # t+1 runs on a side stream while step t computes (two device gradient
@@ -559,6 +589,7 @@ def main():
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
         "e2e": e2e,
+        **({"sharded": sharded} if sharded is not None else {}),
         "kernels": {k: {"launches": v["launches"], "ms_per_step": v["ms"] / prof_steps,
                         **({"tflops": v["flops"] / (v["ms"] / 1000.0) / 1e12} if v["flops"] and v["ms"] > 0 else {}),
                         **({"GB/s": v["bytes"] / (v["ms"] / 1000.0) / 1e9} if not v["flops"] and v["bytes"] and

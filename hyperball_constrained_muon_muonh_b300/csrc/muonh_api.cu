@@ -305,7 +305,10 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
             g_in_group += B.G;
             B.tiles1 = tc::tiles_per_matrix(NS_APPLY, B.R, B.C);
             B.tiles2 = tc::pair_tiles_per_matrix(NS_APPLY, B.R, B.C);
-            if (!B.small) {
+            // split K only for a lone bucket (a standalone orthogonalisation,
+            // or a step over one shape) with few Gram tiles: beside other
+            // buckets on the side streams, the SMs it would fill are busy anyway
+            if (!B.small && groups.size() == 1) {
                 const long long gtiles = (long long)B.G * tc::pair_tiles_per_matrix(NS_GRAM, B.s, B.s);
                 B.gsplits = tc::gram_splits(gtiles, B.l);
                 if (B.gsplits > 1) {

@@ -28,7 +28,8 @@ struct NsIO;
 // One launch = one Newton-Schulz stage over a bucket of G same-shape
 // matrices.  X keeps the matrix's own orientation, R x C (row stride ld_x);
 // s = min(R, C), l = max(R, C); ld_s = row stride of the s x s buffers.
-//   GRAM : M = N = s, K = l.  a_f32 <- scale*Gram, sym_bf16 <- bf16 of it,
+//   GRAM : M = N = s, K = l.  a_f32 <- scale*Gram (its lower triangle and
+//          diagonal only: all the polynomial reads), sym_bf16 <- bf16 of it,
 //          Gram = X X^T (wide, R <= C) or X^T X (tall, R > C)
 //   POLY : M = N = K = s.     sym_bf16 <- cb*a_f32 + cc*(A A)
 //   APPLY: M = R, N = C, K = s.  x_state <- scale*(ca*x_state + P), with

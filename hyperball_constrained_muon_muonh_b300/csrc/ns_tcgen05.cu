@@ -268,18 +268,16 @@ __device__ __forceinline__ void sym_slice_st(const GemmParams& p, int g, int i0,
         if (row >= M || col >= N || col + 3 < row) continue;
         const float4 y = staged(st, r, lane & 7);
         const size_t off = (size_t)row * p.ld_s + col;
+        const float ys[4] = {y.x, y.y, y.z, y.w};
+        // fp32 A: the diagonal here, the rest as the mirror (the lower
+        // triangle is the one the polynomial's epilogue reads)
+        if (MODE == NS_GRAM && row >= col && row < col + 4 && row < N) af[off + (row - col)] = ys[row - col];
         if (col >= row) {
-            if (MODE == NS_GRAM) *reinterpret_cast<float4*>(af + off) = y;
             store_bf16x4(ob + off, y);
         } else {
-            const float ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (col + e >= row && col + e < N) {
-                    if (MODE == NS_GRAM) af[off + e] = ys[e];
-                    ob[off + e] = __float2bfloat16_rn(ys[e]);
-                }
-            }
+            for (int e = 0; e < 4; ++e)
+                if (col + e >= row && col + e < N) ob[off + e] = __float2bfloat16_rn(ys[e]);
         }
     }
 }
@@ -325,8 +323,9 @@ __device__ __forceinline__ void prefetch_q(const float* base, int ld, int M, int
     }
 }
 
-// Prefetch for POLY: A[i][j] (fp32, both triangles written by the Gram) at
-// this thread's positions on or above the diagonal.
+// Prefetch for POLY: A[i][j] at this thread's positions on or above the
+// diagonal, read as A[j][i] (A is exactly symmetric; the Gram writes the fp32
+// A's lower triangle and diagonal only).
 __device__ __forceinline__ void prefetch_a(const GemmParams& p, int g, int i0, int lane, int j0, float2 (&ap)[16]) {
     const float* a = p.a_f32 + (size_t)g * p.ld_s * p.M;
 #pragma unroll
@@ -335,9 +334,9 @@ __device__ __forceinline__ void prefetch_a(const GemmParams& p, int g, int i0, i
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int col = j0 + quad_col(lane, j);
-            ap[4 * rr + j] = (row < p.M && col < p.N && col + 1 >= row)
-                                 ? *reinterpret_cast<const float2*>(a + (size_t)row * p.ld_s + col)
-                                 : make_float2(0.f, 0.f);
+            const bool ok = row < p.M;
+            ap[4 * rr + j].x = (ok && col < p.N && col >= row) ? a[(size_t)col * p.ld_s + row] : 0.f;
+            ap[4 * rr + j].y = (ok && col + 1 < p.N && col + 1 >= row) ? a[(size_t)(col + 1) * p.ld_s + row] : 0.f;
         }
     }
 }
@@ -419,19 +418,18 @@ __device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, in
             }
             const size_t off = (size_t)row * p.ld_s + col;
             const bool in1 = col + 1 < N;
+            // fp32 A: the diagonal here, the rest as the mirror (the lower
+            // triangle is the one the polynomial's epilogue reads)
+            if (MODE == NS_GRAM) {
+                if (col == row) af[off] = y0;
+                if (in1 && col + 1 == row) af[off + 1] = y1;
+            }
             if (col >= row && in1) {
-                if (MODE == NS_GRAM) *reinterpret_cast<float2*>(af + off) = make_float2(y0, y1);
                 store_bf16x2(ob + off, y0, y1);
             } else {
-                // col + 1 == row (only y1 is on the diagonal), or col + 1 == N
-                if (col >= row) {
-                    if (MODE == NS_GRAM) af[off] = y0;
-                    ob[off] = __float2bfloat16_rn(y0);
-                }
-                if (in1 && col + 1 >= row) {
-                    if (MODE == NS_GRAM) af[off + 1] = y1;
-                    ob[off + 1] = __float2bfloat16_rn(y1);
-                }
+                // col + 1 == row (only y1 is on or above the diagonal), or col + 1 == N
+                if (col >= row) ob[off] = __float2bfloat16_rn(y0);
+                if (in1 && col + 1 >= row) ob[off + 1] = __float2bfloat16_rn(y1);
             }
             // mirrors (strictly above the diagonal)
             if (col > row) {
@@ -825,29 +823,70 @@ static_assert(PairPipe<1>::A_BYTES == PairPipe<1>::B_BYTES && PairPipe<2>::A_BYT
 
 // TMA load into this CTA's shared memory, completing on a barrier that may
 // belong to the peer CTA of the pair.
+// MUONH_TMA_L2_HINT (build-time): 1 tags the operand loads with an L2
+// evict_last cache policy (operand panels are re-read by the neighbouring
+// tiles of a launch), 0 loads them with the default policy.
+#ifndef MUONH_TMA_L2_HINT
+#define MUONH_TMA_L2_HINT 0
+#endif
+__device__ __forceinline__ uint64_t operand_policy() {
+    uint64_t pol = 0;
+#if MUONH_TMA_L2_HINT
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+#endif
+    return pol;
+}
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int x,
-                                                 int y, int z) {
+                                                 int y, int z, uint64_t pol = 0) {
+#if MUONH_TMA_L2_HINT
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "r"(z), "l"(pol)
+        : "memory");
+#else
+    (void)pol;
     asm volatile(
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "r"(z)
         : "memory");
+#endif
 }
 __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int c0,
-                                                 int c1, int c2, int c3) {
+                                                 int c1, int c2, int c3, uint64_t pol = 0) {
+#if MUONH_TMA_L2_HINT
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(pol)
+        : "memory");
+#else
+    (void)pol;
     asm volatile(
         "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
+#endif
 }
 __device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cluster_bar, int c0,
-                                                 int c1, int c2, int c3, int c4) {
+                                                 int c1, int c2, int c3, int c4, uint64_t pol = 0) {
+#if MUONH_TMA_L2_HINT
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "l"(pol)
+        : "memory");
+#else
+    (void)pol;
     asm volatile(
         "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
+#endif
 }
 __host__ __device__ constexpr uint32_t idesc_pair(bool a_mn_major, bool b_mn_major) {
     return idesc_f16(2 * BM, BN, a_mn_major, b_mn_major);
@@ -947,6 +986,7 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer (both CTAs) ----------------
+        const uint64_t pol = operand_policy();
         int stage = 0;
         uint32_t phase = 0;
         bool ok = !p.test_no_loads;
@@ -976,32 +1016,32 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
                 if (KPS == 2) {
                     // K steps 2ks and 2ks+1 (the second is zero-filled past K)
                     if (!p.a_mn)
-                        tma_load_4d_pair(sa, &tm_a, fb, 0, row_a, 2 * ks, g);
+                        tma_load_4d_pair(sa, &tm_a, fb, 0, row_a, 2 * ks, g, pol);
                     else
-                        tma_load_5d_pair(sa, &tm_a, fb, 0, 0, row_a / 64, 2 * ks, g);
+                        tma_load_5d_pair(sa, &tm_a, fb, 0, 0, row_a / 64, 2 * ks, g, pol);
                     if (diag) {
                     } else if (!p.b_mn)
-                        tma_load_4d_pair(sb, &tm_b, fb, 0, row_b, 2 * ks, g);
+                        tma_load_4d_pair(sb, &tm_b, fb, 0, row_b, 2 * ks, g, pol);
                     else
-                        tma_load_5d_pair(sb, &tm_b, fb, 0, 0, row_b / 64, 2 * ks, g);
+                        tma_load_5d_pair(sb, &tm_b, fb, 0, 0, row_b / 64, 2 * ks, g, pol);
                     if (++stage == STAGES2) { stage = 0; phase ^= 1; }
                     continue;
                 }
                 const int kb = ks;
                 if (!p.a_mn) {
-                    tma_load_3d_pair(sa, &tm_a, fb, kb * BK, row_a, g);
+                    tma_load_3d_pair(sa, &tm_a, fb, kb * BK, row_a, g, pol);
                 } else {
 #pragma unroll
                     for (int c = 0; c < BM / 64; ++c)
-                        tma_load_3d_pair(sa + c * (64 * BK * 2), &tm_a, fb, row_a + c * 64, kb * BK, g);
+                        tma_load_3d_pair(sa + c * (64 * BK * 2), &tm_a, fb, row_a + c * 64, kb * BK, g, pol);
                 }
                 if (diag) {
                 } else if (!p.b_mn) {
-                    tma_load_3d_pair(sb, &tm_b, fb, kb * BK, row_b, g);
+                    tma_load_3d_pair(sb, &tm_b, fb, kb * BK, row_b, g, pol);
                 } else {
 #pragma unroll
                     for (int c = 0; c < BN / 128; ++c)
-                        tma_load_3d_pair(sb + c * (64 * BK * 2), &tm_b, fb, row_b + c * 64, kb * BK, g);
+                        tma_load_3d_pair(sb + c * (64 * BK * 2), &tm_b, fb, row_b + c * 64, kb * BK, g, pol);
                 }
                 if (++stage == STAGES2) { stage = 0; phase ^= 1; }
             }
@@ -1135,6 +1175,9 @@ ns_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_const
 }  // namespace pair
 
 // ---- host side -------------------------------------------------------------------
+#ifndef MUONH_TMA_PROMOTION
+#define MUONH_TMA_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -1163,7 +1206,7 @@ static bool encode_bf16_3d(CUtensorMap* map, const void* base, int cols, int row
     cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, MUONH_TMA_PROMOTION,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1181,7 +1224,7 @@ static bool encode_bf16_kmajor_2step(CUtensorMap* map, const void* base, int K, 
     cuuint32_t box[4] = {64, (cuuint32_t)BM, 2, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, MUONH_TMA_PROMOTION,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1193,7 +1236,7 @@ static bool encode_bf16_mnmajor_2step(CUtensorMap* map, const void* base, int co
     cuuint32_t box[5] = {64, 64, 2, 2, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, MUONH_TMA_PROMOTION,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1221,14 +1264,19 @@ int pair_tiles_per_matrix(int mode, int M, int N) {
     return cnt;
 }
 
-// A Gram launch with fewer pair tiles than twice the CTA pairs of a B300
-// (74) leaves SMs idle for its whole duration: its K steps (>= 16 per range)
-// are cut into ranges so that the units number at least 148.
+// A Gram launch with few pair tiles (<= 16; a B300 runs 74 CTA pairs)
+// leaves most SMs idle for its whole duration: its K steps (>= 16 per range)
+// are cut into ranges so that the units number about 148.  Measured on a
+// lone 16384x1024 orthogonalisation (10 tiles): 1.09 -> 0.97 ms; launches
+// with 36 tiles were 3-7 % slower split, so they are not.
 #ifndef MUONH_SPLIT_MAX
 #define MUONH_SPLIT_MAX 8
 #endif
 #ifndef MUONH_SPLIT_TARGET
 #define MUONH_SPLIT_TARGET 148
+#endif
+#ifndef MUONH_SPLIT_MAX_TILES
+#define MUONH_SPLIT_MAX_TILES 16
 #endif
 #ifndef MUONH_SPLIT_MIN_STEPS
 #define MUONH_SPLIT_MIN_STEPS 16
@@ -1236,7 +1284,7 @@ int pair_tiles_per_matrix(int mode, int M, int N) {
 int gram_splits(long long tiles, int K) {
     constexpr long long kTargetUnits = MUONH_SPLIT_TARGET;
     const int nkb = (K + BK - 1) / BK;
-    if (tiles <= 0 || tiles >= kTargetUnits) return 1;
+    if (tiles <= 0 || tiles > MUONH_SPLIT_MAX_TILES || tiles >= kTargetUnits) return 1;
     long long sp = (kTargetUnits + tiles - 1) / tiles;
     sp = std::min<long long>(sp, nkb / MUONH_SPLIT_MIN_STEPS);
     sp = std::min<long long>(sp, MUONH_SPLIT_MAX);

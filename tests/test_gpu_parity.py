@@ -157,12 +157,14 @@ def test_orthogonalize_bf16_input_and_output(shape, mode):
     assert mh.get_status() == 0
 
 
-@pytest.mark.parametrize("shape", [(16384, 1024), (1024, 16384), (2048, 2048), (6144, 2048), (1024, 2048)])
+@pytest.mark.parametrize("shape", [(16384, 1024), (1024, 16384), (1024, 2048), (4096, 1024), (1024, 3000),
+                                   (65536, 256)])
 def test_split_k_gram_repeatable(shape):
-    # alone, these matrices' Grams have fewer pair tiles than twice the CTA
-    # pairs, so K is split into ranges (2 to 8 here) whose partial products
-    # are summed in range order by whichever range finishes last: repeated
-    # calls agree bit for bit, and with the oracle within the tolerance
+    # alone, these matrices' Grams have at most 16 pair tiles, so K is split
+    # into ranges (2 to 8 here, the last one shorter where K is ragged) whose
+    # partial products are summed in range order by whichever range finishes
+    # last: repeated calls agree bit for bit, and with the oracle within the
+    # tolerance
     g = wl.ragged([shape]).grad(0, 0, "cuda")
     outs = [mh.orthogonalize(g, 5, wl.NS_COEFFS, 1e-7) for _ in range(3)]
     torch.cuda.synchronize()
