@@ -173,6 +173,7 @@ struct Bucket {
     int first;            // bucket-order index of its first matrix
     int ld_x, ld_s;
     size_t off_xs, off_xo;                    // byte offsets in the workspace
+    size_t off_xlo;                           // bf16 lo part of the two-part Newton-Schulz state
     size_t off_af, off_aop, off_bop;          // this bucket's slice of its s-group's s x s buffers
     size_t off_bf32;                          // fp32 check mode: its slice of the group's fp32 B
     int sgroup;                               // index of its s-group
@@ -276,7 +277,11 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
             S.G += (int)sh.idx.size();
             if (sh.R > kSmallStepSide || sh.C > kSmallStepSide) S.small_step = false;
         }
-        S.off_af = take(sizeof(float) * S.elems());
+        // the fp32 Gram A: for Newton-Schulz on CUDA cores only (the fp32
+        // check mode, short sides <= kSmallSide); the tensor-core path keeps A
+        // in bf16 (A_op) alone
+        const bool simt_group = (flags & MUONH_FLAG_FP32_CHECK) || S.s <= kSmallSide;
+        S.off_af = simt_group ? take(sizeof(float) * S.elems()) : 0;
         S.off_aop = take(sizeof(__nv_bfloat16) * S.elems());
         // fp32 check mode keeps an fp32 B at off_aop, spanning A_op and B_op
         S.off_bop = take(sizeof(__nv_bfloat16) * S.elems());
@@ -296,6 +301,7 @@ Plan build_plan(const int64_t* rc, int n, uint32_t flags) {
             B.ld_s = S.ld_s;
             B.off_xs = take(sizeof(float) * B.x_elems());
             B.off_xo = take(2 * sizeof(__nv_bfloat16) * B.x_elems());    // two bf16 buffers (ping-pong)
+            B.off_xlo = take(sizeof(__nv_bfloat16) * B.x_elems());
             const size_t so = (size_t)g_in_group * S.s * S.ld_s;
             B.off_af = S.off_af + sizeof(float) * so;
             B.off_aop = S.off_aop + sizeof(__nv_bfloat16) * so;
@@ -693,7 +699,6 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         g.mode = NS_GRAM; g.G = B.G; g.M = B.s; g.N = B.s; g.K = B.l;
         g.a_mn = g.b_mn = B.tall;
         g.ld_x = B.ld_x; g.ld_s = B.ld_s;
-        g.a_f32 = reinterpret_cast<float*>(ws + B.off_af);
         g.sym_bf16 = reinterpret_cast<__nv_bfloat16*>(ws + B.off_aop);
         g.scale = it == 0 ? sc.inv_nu2 + B.first : nullptr;
         g.status = status;
@@ -714,7 +719,7 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         {
             Trace tr(K_GRAM, cur);
             e = tr.done(tc::launch_ns_gemm(g, xc, B.ld_x, xc, B.ld_x, pair, cur, &why), G * S * S * L,
-                        G * S * L * 2 + G * S * S * 6);
+                        G * S * L * 2 + G * S * S * 2);
         }
         return sy.check_on(cur, e, e == cudaErrorInvalidValue ? why : "tcgen05 Gram launch");
     };
@@ -724,7 +729,7 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         GemmParams q{};
         q.mode = NS_POLY; q.G = Q.G; q.M = Q.s; q.N = Q.s; q.K = Q.s;
         q.ld_s = Q.ld_s;
-        q.a_f32 = reinterpret_cast<float*>(ws + Q.off_af);
+        q.a_op = aop;
         q.sym_bf16 = reinterpret_cast<__nv_bfloat16*>(ws + Q.off_bop);
         q.cb = coeffs[1]; q.cc = coeffs[2];
         q.status = status;
@@ -733,7 +738,7 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         {
             Trace tr(K_POLY, cur);
             e = tr.done(tc::launch_ns_gemm(q, aop, Q.ld_s, aop, Q.ld_s, pair, cur, &why), G * S * S * S,
-                        G * S * S * 8);
+                        G * S * S * 6);
         }
         return sy.check_on(cur, e, e == cudaErrorInvalidValue ? why : "tcgen05 polynomial launch");
     };
@@ -751,6 +756,11 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         a.ld_x = B.ld_x; a.ld_s = B.ld_s;
         a.x_state = reinterpret_cast<float*>(ws + B.off_xs);
         a.x_op_out = (it + 1 < ns_steps) ? xn : nullptr;
+        // two-part state: written by every apply but the last, read from the
+        // second iteration on (hi is the current operand copy of X)
+        a.x_hi = xc;
+        a.x_lo = reinterpret_cast<__nv_bfloat16*>(ws + B.off_xlo);
+        a.in_hilo = it > 0;
         a.scale = it == 0 ? sc.inv_nu + B.first : nullptr;
         a.ca = coeffs[0];
         a.status = status;
@@ -767,9 +777,10 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         const double G = B.G, S = B.s, L = B.l;
         cudaError_t e;
         {
-            // bytes: B_op, X read and written (fp32), X_op written unless last, W read when fused;
-            // NS_OUT_W writes the weight (fp32 and bf16) in place of X
-            double per_el = 8.0 + (a.x_op_out ? 2.0 : 0.0) + ((a.variant & NS_OUT_U) ? 4.0 : 0.0);
+            // bytes per element: X read (fp32 4, or hi + lo 2 + 2), X written (hi + lo 2 + 2
+            // unless last, else fp32 4), W read when fused (4); NS_OUT_W writes the weight
+            // (fp32 and bf16) in place of X
+            double per_el = 4.0 + 4.0 + ((a.variant & NS_OUT_U) ? 4.0 : 0.0);
             if (a.variant & NS_OUT_W) per_el = 4.0 + 4.0 + 4.0 + 2.0;
             Trace tr(apply_kind(a.variant), cur);
             e = tr.done(B.tall ? tc::launch_ns_gemm(a, xc, B.ld_x, bop, B.ld_s, pair, cur, &why)
@@ -1437,7 +1448,7 @@ int muonh_test_gemm_timeout(uint32_t flags, uint64_t timeout_ns, void* workspace
     GemmParams g{};
     g.mode = NS_GRAM; g.G = 1; g.M = 256; g.N = 256; g.K = 256;
     g.ld_x = 256; g.ld_s = 256;
-    g.a_f32 = reinterpret_cast<float*>(ws + 128 * 1024);
+
     g.sym_bf16 = reinterpret_cast<__nv_bfloat16*>(ws + 384 * 1024);
     g.status = status;
     g.timeout_ns = timeout_ns;

@@ -28,13 +28,14 @@ struct NsIO;
 // One launch = one Newton-Schulz stage over a bucket of G same-shape
 // matrices.  X keeps the matrix's own orientation, R x C (row stride ld_x);
 // s = min(R, C), l = max(R, C); ld_s = row stride of the s x s buffers.
-//   GRAM : M = N = s, K = l.  a_f32 <- scale*Gram (its lower triangle and
-//          diagonal only: all the polynomial reads), sym_bf16 <- bf16 of it,
+//   GRAM : M = N = s, K = l.  sym_bf16 <- bf16(scale*Gram) (both triangles),
 //          Gram = X X^T (wide, R <= C) or X^T X (tall, R > C)
-//   POLY : M = N = K = s.     sym_bf16 <- cb*a_f32 + cc*(A A)
-//   APPLY: M = R, N = C, K = s.  x_state <- scale*(ca*x_state + P), with
-//          P = B X (wide) or X B (tall); x_op_out <- bf16(x_state) unless
-//          null.  `variant` (NS_IN_SRC, NS_OUT_U) selects where X comes
+//   POLY : M = N = K = s.     sym_bf16 <- bf16(cb*A + cc*(A A)), with A the
+//          Gram's bf16 copy a_op in both terms
+//   APPLY: M = R, N = C, K = s.  X <- scale*(ca*X + P), with P = B X (wide)
+//          or X B (tall); the new X goes to (x_op_out, x_lo) as hi + lo
+//          when x_op_out is set, else to x_state (fp32).  `variant`
+//          (NS_IN_SRC, NS_OUT_U, NS_OUT_W) and in_hilo select where X comes
 //          from and what is written.
 // Operand tiles are K-major (rows of the operand run along M or N, K
 // contiguous) unless a_mn / b_mn say MN-major (K runs along the rows).
@@ -49,7 +50,15 @@ struct GemmParams {
     int ld_x, ld_s;
     float* x_state;
     __nv_bfloat16* x_op_out;
-    float* a_f32;
+    // APPLY: the two-part state X = hi + lo (bf16 each, [G][M][ld_x]) that
+    // every apply with another iteration after it writes (hi to x_op_out, lo
+    // to x_lo, in place) and that in_hilo applies read (hi from x_hi, the
+    // current operand copy of X).  The momentum kernel's fp32 state is read
+    // by the first apply of unfused matrices; the last apply writes fp32.
+    const __nv_bfloat16* x_hi;
+    __nv_bfloat16* x_lo;
+    int in_hilo;
+    const __nv_bfloat16* a_op;   // POLY: the Gram's bf16 output (read for the b*A term)
     __nv_bfloat16* sym_bf16;
     const float* scale;     // per-matrix factor (bucket-local index) or null
     const NsIO* io;         // NS_IN_SRC / NS_OUT_U: per-matrix buffers (bucket-local index)

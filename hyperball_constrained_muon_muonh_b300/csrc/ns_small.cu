@@ -197,11 +197,63 @@ __device__ __forceinline__ void store_w(const SmallDesc& D, bool tall, int C, in
     }
 }
 
+// ---- coalesced HBM phases ---------------------------------------------------------
+// The momentum and write-out phases move the matrix between HBM and the
+// lane-per-row layout of TMEM through a per-warp 32 x 32 fp32 staging tile
+// (in the A buffer, free in those phases), XOR-swizzled in 16-byte chunks
+// (chunk c of row r at c ^ (r & 7)).  In global memory lane l then covers
+// columns 4*(l%8)..+3 of rows 4*kk + l/8 (kk = 0..7): every warp access is
+// four whole 128-byte row segments.
+__device__ __forceinline__ float* stage_at(float* st, int r, int c) { return st + r * 32 + ((c ^ (r & 7)) << 2); }
+
+// coalesced row / column of pass kk of this lane within the warp's block
+__device__ __forceinline__ int co_row(int lane, int kk) { return 4 * kk + (lane >> 3); }
+__device__ __forceinline__ int co_col(int lane) { return 4 * (lane & 7); }
+
+// the lane-per-row view (lane = row) of the staged tile: 32 values
+__device__ __forceinline__ void staged_row(const float* st, int lane, float (&v)[32]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const float4 q = *reinterpret_cast<const float4*>(stage_at(const_cast<float*>(st), lane, c));
+        v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
+    }
+}
+__device__ __forceinline__ void stage_row(float* st, int lane, const float (&v)[32]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(stage_at(st, lane, c)) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+
+// 8 coalesced float4 of a row-major fp32 (or bf16, widened) matrix: rows
+// row0 + co_row, columns col0 + co_col; zero for rows >= nrows
+__device__ __forceinline__ void load_co(const float* base, bool bf16, int C, int row0, int nrows, int col0, int lane,
+                                        float4 (&o)[8], bool streaming) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const int row = row0 + co_row(lane, kk);
+        const size_t e = (size_t)row * C + col0 + co_col(lane);
+        if (row >= nrows) {
+            o[kk] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if (bf16) {
+            const uint2 u = __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(base) + e));
+            o[kk] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                                __uint_as_float(u.y & 0xFFFF0000u));
+        } else {
+            o[kk] = streaming ? __ldcs(reinterpret_cast<const float4*>(base + e))
+                              : *reinterpret_cast<const float4*>(base + e);
+        }
+    }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ SmallParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t xr = smem_u32(smem), xcl = smem_u32(smem + OP_BYTES), ar = smem_u32(smem + 2 * OP_BYTES);
+    // staging tiles of the coalesced HBM phases (in the A buffer, free then)
+    // and the write-out's U buffer (X's two buffers, 128 rows x 256 fp32)
+    float* const stage_base = reinterpret_cast<float*>(smem + 2 * OP_BYTES);
+    float* const ubuf = reinterpret_cast<float*>(smem);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 3 * OP_BYTES);
     double* red = reinterpret_cast<double*>(smem + 3 * OP_BYTES + 8);        // [8]
     double* peer = red + 8;                                                  // [2]
@@ -291,7 +343,57 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
         const bool vec = !tall && (C & 3) == 0;
 
         // ---- momentum; the Newton-Schulz input into TMEM (fp32) and XR / XC (bf16) ----
+        // Wide matrices with whole 32-column slices stream G and M coalesced
+        // through the staging tile, the next slice's loads in flight while
+        // the current one is processed; other shapes take element loads.
         double part = 0.0;
+        float* st = stage_base + warp * (32 * 32);
+        const int wrow0 = 128 * (int)rank + 32 * q;   // this warp's first X row
+        const bool coal = !tall && C == 256;   // whole rows of 256 columns: every slice in range
+        if (coal) {
+            float4 gc[8], mc[8], gn[8], mn[8];
+            load_co(D.g, p.grad_bf16, C, wrow0, s, 128 * h, lane, gc, true);
+            load_co(D.m, false, C, wrow0, s, 128 * h, lane, mc, false);
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k) {
+                const int j0 = 128 * h + 32 * k;
+                if (k + 1 < 4) {
+                    load_co(D.g, p.grad_bf16, C, wrow0, s, j0 + 32, lane, gn, true);
+                    load_co(D.m, false, C, wrow0, s, j0 + 32, lane, mn, false);
+                }
+                float acc = 0.f;
+                __syncwarp();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int r = co_row(lane, kk);
+                    float4 m = mc[kk];
+                    const float4 g = gc[kk];
+                    m.x = fmaf(p.beta, m.x, g.x); m.y = fmaf(p.beta, m.y, g.y);
+                    m.z = fmaf(p.beta, m.z, g.z); m.w = fmaf(p.beta, m.w, g.w);
+                    if (wrow0 + r < s)
+                        *reinterpret_cast<float4*>(D.m + (size_t)(wrow0 + r) * C + j0 + co_col(lane)) = m;
+                    float4 x = m;
+                    if (p.nesterov) {
+                        x.x = fmaf(p.beta, m.x, g.x); x.y = fmaf(p.beta, m.y, g.y);
+                        x.z = fmaf(p.beta, m.z, g.z); x.w = fmaf(p.beta, m.w, g.w);
+                    }
+                    acc = fmaf(x.x, x.x, acc); acc = fmaf(x.y, x.y, acc);
+                    acc = fmaf(x.z, x.z, acc); acc = fmaf(x.w, x.w, acc);
+                    *reinterpret_cast<float4*>(stage_at(st, r, lane & 7)) = x;
+                }
+                __syncwarp();
+                part += (double)acc;
+                float x[32];
+                staged_row(st, lane, x);
+                tmem_st32(tx + j0, x);
+                put_kmajor(xr, row_l, j0, x);
+                put_mnmajor(xc, i, j0, x);
+                if (k + 1 < 4) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) { gc[kk] = gn[kk]; mc[kk] = mn[kk]; }
+                }
+            }
+        } else {
 #pragma unroll 1
         for (int k = 0; k < 4; ++k) {
             const int j0 = 128 * h + 32 * k;
@@ -351,6 +453,7 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
             tmem_st32(tx + j0, x);
             put_kmajor(xr, row_l, j0, x);
             put_mnmajor(xc, i, j0, x);
+        }
         }
         const double nu2 = pair_sum(part, red, peer, peer_remote, (int)rank);
         const bool finite = isfinite(nu2);
@@ -426,10 +529,53 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
         }
 
         // ---- write-out: MuonH retraction or plain Muon update ----
+        // Whole 256-column rows go coalesced: O through the staging tile, W
+        // loaded one slice ahead, U kept in the U buffer (shared memory) for
+        // the rescale.  Other shapes: element access, U in the accumulator.
         const float nlr = -p.lr * update_scale(R, C, p.scale_mode);
         const bool keep = !finite || *abort_flag;
+        auto o_coalesced = [&](int j0, float4 (&o4)[8]) {
+            float o[32];
+            tmem_ld32(tx + j0, o);
+            __syncwarp();
+            stage_row(st, lane, o);
+            __syncwarp();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) o4[kk] = *reinterpret_cast<const float4*>(stage_at(st, co_row(lane, kk), lane & 7));
+        };
+        auto store_w_co = [&](int j0, int kk, float4 w) {
+            const int row = wrow0 + co_row(lane, kk);
+            if (row >= s) return;
+            const size_t e = (size_t)row * C + j0 + co_col(lane);
+            __stcs(reinterpret_cast<float4*>(D.w + e), w);
+            if (D.wb) {
+                const __nv_bfloat162 a = __floats2bfloat162_rn(w.x, w.y), b2 = __floats2bfloat162_rn(w.z, w.w);
+                *reinterpret_cast<uint2*>(D.wb + e) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b2));
+            }
+        };
         if (p.muon) {
-            if (!keep) {
+            if (!keep && coal) {
+                float4 wc[8], wn[8];
+                load_co(D.w, false, C, wrow0, s, 128 * h, lane, wc, true);
+#pragma unroll 1
+                for (int k = 0; k < 4; ++k) {
+                    const int j0 = 128 * h + 32 * k;
+                    if (k + 1 < 4) load_co(D.w, false, C, wrow0, s, j0 + 32, lane, wn, true);
+                    float4 o4[8];
+                    o_coalesced(j0, o4);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const float4 w = wc[kk], o = o4[kk];
+                        store_w_co(j0, kk, make_float4(fmaf(nlr, o.x, p.wdecay * w.x), fmaf(nlr, o.y, p.wdecay * w.y),
+                                                       fmaf(nlr, o.z, p.wdecay * w.z), fmaf(nlr, o.w, p.wdecay * w.w)));
+                    }
+                    if (k + 1 < 4) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) wc[kk] = wn[kk];
+                    }
+                }
+            } else if (!keep) {
 #pragma unroll 1
                 for (int k = 0; k < 4; ++k) {
                     const int j0 = 128 * h + 32 * k;
@@ -443,43 +589,86 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
             }
             cluster_sync();
         } else {
-            // U = W - lr*O goes to the accumulator columns (free now), so W is
-            // read once
             double up = 0.0;
+            if (coal) {
+                float4 wc[8], wn[8];
+                load_co(D.w, false, C, wrow0, s, 128 * h, lane, wc, true);
 #pragma unroll 1
-            for (int k = 0; k < 4; ++k) {
-                const int j0 = 128 * h + 32 * k;
-                float o[32], wv[32];
-                tmem_ld32(tx + j0, o);
-                load_w(D, tall, C, i, j0, row_ok, l, wv);
-                float acc = 0.f;
+                for (int k = 0; k < 4; ++k) {
+                    const int j0 = 128 * h + 32 * k;
+                    if (k + 1 < 4) load_co(D.w, false, C, wrow0, s, j0 + 32, lane, wn, true);
+                    float4 o4[8];
+                    o_coalesced(j0, o4);
+                    float acc = 0.f;
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    wv[t] = fmaf(nlr, o[t], wv[t]);
-                    if (row_ok && j0 + t < l) acc = fmaf(wv[t], wv[t], acc);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const float4 w = wc[kk], o = o4[kk];
+                        const float4 u = make_float4(fmaf(nlr, o.x, w.x), fmaf(nlr, o.y, w.y), fmaf(nlr, o.z, w.z),
+                                                     fmaf(nlr, o.w, w.w));
+                        const int r = co_row(lane, kk);
+                        if (wrow0 + r < s) {
+                            acc = fmaf(u.x, u.x, acc); acc = fmaf(u.y, u.y, acc);
+                            acc = fmaf(u.z, u.z, acc); acc = fmaf(u.w, u.w, acc);
+                        }
+                        *reinterpret_cast<float4*>(ubuf + (32 * q + r) * 256 + j0 + co_col(lane)) = u;
+                    }
+                    up += (double)acc;
+                    if (k + 1 < 4) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) wc[kk] = wn[kk];
+                    }
                 }
-                up += (double)acc;
-                tmem_st32(tacc + j0, wv);
+            } else {
+                // U = W - lr*O goes to the accumulator columns (free now), so W
+                // is read once
+#pragma unroll 1
+                for (int k = 0; k < 4; ++k) {
+                    const int j0 = 128 * h + 32 * k;
+                    float o[32], wv[32];
+                    tmem_ld32(tx + j0, o);
+                    load_w(D, tall, C, i, j0, row_ok, l, wv);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        wv[t] = fmaf(nlr, o[t], wv[t]);
+                        if (row_ok && j0 + t < l) acc = fmaf(wv[t], wv[t], acc);
+                    }
+                    up += (double)acc;
+                    tmem_st32(tacc + j0, wv);
+                }
+                tmem_st_wait();
             }
-            tmem_st_wait();
             const double rho2 = pair_sum(up, red, peer, peer_remote, (int)rank);
             const bool degenerate = !isfinite(rho2) || rho2 == 0.0;
             if (!keep && degenerate && threadIdx.x == 0 && rank == 0)
                 raise_status(p.status, MUONH_STATUS_DEGENERATE_NORM);
             if (!keep && !degenerate) {
                 const float f = (float)((double)p.r0[D.r0_index] / sqrt(rho2));
+                if (coal) {
 #pragma unroll 1
-                for (int k = 0; k < 4; ++k) {
-                    const int j0 = 128 * h + 32 * k;
-                    float u[32];
-                    tmem_ld32(tacc + j0, u);
+                    for (int k = 0; k < 4; ++k) {
+                        const int j0 = 128 * h + 32 * k;
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) u[t] = f * u[t];
-                    store_w(D, tall, C, i, j0, row_ok, l, u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const float4 u =
+                                *reinterpret_cast<const float4*>(ubuf + (32 * q + co_row(lane, kk)) * 256 + j0 + co_col(lane));
+                            store_w_co(j0, kk, make_float4(f * u.x, f * u.y, f * u.z, f * u.w));
+                        }
+                    }
+                } else {
+#pragma unroll 1
+                    for (int k = 0; k < 4; ++k) {
+                        const int j0 = 128 * h + 32 * k;
+                        float u[32];
+                        tmem_ld32(tacc + j0, u);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) u[t] = f * u[t];
+                        store_w(D, tall, C, i, j0, row_ok, l, u);
+                    }
                 }
             }
             tc_fence_before();
-            cluster_sync();   // the reduction slots and the accumulator are free again
+            cluster_sync();   // the reduction slots, the accumulator and the U buffer are free again
             tc_fence_after();
         }
     }

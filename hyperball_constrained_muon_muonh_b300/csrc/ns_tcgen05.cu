@@ -120,13 +120,16 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int local, int&
 // tcgen05.ld gives each lane one accumulator row (32 consecutive columns).
 // Row-wise global access from that layout touches 32 rows per instruction,
 // so each warp stages its 32 x 32 slice in shared memory and reads it back
-// so that 8 lanes cover one 128-byte row segment.  The staging tile is
-// XOR-swizzled in 16-byte chunks (chunk c of row r sits at c ^ (r & 7)),
-// which keeps both the row-per-lane writes and the row-segment reads free of
-// bank conflicts.  Mirror writes of the symmetric products go straight from
-// registers: for a fixed column the 32 lanes write one contiguous run.
-// Operands the epilogue reads (X for APPLY, A for POLY) are loaded one slice
-// ahead so that their latency overlaps the previous slice's stores.
+// so that each lane holds 8 consecutive columns of one row: lane l takes
+// columns 8*(l%4) .. +7 of rows 8k + l/4, k = 0..3.  Every global access is
+// then one 16-byte vector per lane (8 bf16 values, or half of 8 fp32 values),
+// which keeps the epilogue's memory instructions, not only its bytes, few.
+// The staging tile is XOR-swizzled in 16-byte chunks (chunk c of row r sits
+// at c ^ (r & 7)), which keeps the row-per-lane writes and the reads free of
+// bank conflicts.  The mirror of a symmetric product is written from the same
+// lane layout, element by element.  Operands the epilogue reads (X for APPLY, A for POLY) are loaded one slice
+// ahead, as raw bits that are turned into values only where they are used,
+// so that the loads stay in flight while the previous slice is processed.
 
 __device__ __forceinline__ void stage_rows(float* st, int lane, const float (&v)[32]) {
     __syncwarp();
@@ -142,147 +145,248 @@ __device__ __forceinline__ float4 staged(const float* st, int r, int c) {
     return *reinterpret_cast<const float4*>(st + r * 32 + ((c ^ (r & 7)) << 2));
 }
 
-__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float4 v) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&lo);
-    u.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dst) = u;
+// This lane's row (0..31) and first column (0..24) of the slice, pass k.
+__device__ __forceinline__ int st_row(int lane, int k) { return 8 * k + (lane >> 2); }
+__device__ __forceinline__ int st_col(int lane) { return 8 * (lane & 3); }
+
+// 8 values as bf16 (round to nearest even), packed for one 16-byte store
+__device__ __forceinline__ uint4 pack_bf16x8(float4 a, float4 b) {
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
+    const __nv_bfloat162 p2 = __floats2bfloat162_rn(b.x, b.y), p3 = __floats2bfloat162_rn(b.z, b.w);
+    return make_uint4(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1),
+                      *reinterpret_cast<const uint32_t*>(&p2), *reinterpret_cast<const uint32_t*>(&p3));
 }
 
-// Prefetch for APPLY: X[i0 + 4k + lane/8][j0 + 4*(lane%8) .. +3], k = 0..7,
-// from a row-major array with row stride `ld`.  For the fp32 state the row
-// stride is a multiple of 8 elements, so a 4-wide access at a column < N
-// stays inside the padded row (padding columns are never read back); a
-// caller's buffer (row stride N) is read this way only when N % 4 == 0.
+// two bf16 values of a 32-bit word as floats
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Raw bits of a 16-byte vector kept in a float4 register (a prefetch slot)
+__device__ __forceinline__ float4 as_slot(uint4 u) {
+    return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+}
+__device__ __forceinline__ uint4 slot_bits(float4 f) {
+    return make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
+}
+
+// Prefetch of an fp32 row-major array (row stride `ld`) for pass k = 0..3:
+// xp[2k], xp[2k+1] = X[i0 + 8k + lane/4][j0 + 8*(lane%4) .. +7].  A workspace
+// array's row stride is a multiple of 8 elements, so the 8-wide access at a
+// column < N stays inside the padded row (padding is never read back); a
+// caller's buffer (row stride N, N % 4 == 0) is read only up to column N.
 __device__ __forceinline__ void prefetch_rm(const float* base, int ld, int M, int N, int i0, int lane, int j0,
-                                            float4 (&xp)[8]) {
-    const int col = j0 + (lane & 7) * 4;
+                                            float4 (&xp)[8], bool exact_cols = false) {
+    const int col = j0 + st_col(lane);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int row = i0 + k * 4 + (lane >> 3);
-        xp[k] = (row < M && col < N) ? __ldcs(reinterpret_cast<const float4*>(base + (size_t)row * ld + col))
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < 4; ++k) {
+        const int row = i0 + st_row(lane, k);
+        const float4* q = reinterpret_cast<const float4*>(base + (size_t)row * ld + col);
+        const bool ok = row < M && col < N;
+        xp[2 * k] = ok ? __ldcs(q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xp[2 * k + 1] = (ok && (!exact_cols || col + 4 < N)) ? __ldcs(q + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
-// Prefetch for POLY: A[i][j] for this lane's row i and columns j0..j0+31,
-// read as A[j][i] (A is exactly symmetric), which is coalesced over lanes.
-__device__ __forceinline__ void prefetch_a_st(const GemmParams& p, int g, int i0, int lane, int j0, float (&ap)[32]) {
-    const int i = i0 + lane;
-    const float* a = p.a_f32 + (size_t)g * p.ld_s * p.M + i;
+// The same for the two-part state X = hi + lo (bf16 each, row stride ld):
+// xp[2k] holds hi's 8 values, xp[2k+1] lo's, as raw bits (hilo_values).
+__device__ __forceinline__ void prefetch_hilo(const __nv_bfloat16* hi, const __nv_bfloat16* lo, int ld, int M, int N,
+                                              int i0, int lane, int j0, float4 (&xp)[8]) {
+    const int col = j0 + st_col(lane);
 #pragma unroll
-    for (int t = 0; t < 32; ++t) {
-        const int j = j0 + t;
-        ap[t] = (i < p.M && j < p.N && j >= i) ? a[(size_t)j * p.ld_s] : 0.f;
+    for (int k = 0; k < 4; ++k) {
+        const int row = i0 + st_row(lane, k);
+        uint4 h = make_uint4(0u, 0u, 0u, 0u), l = h;
+        if (row < M && col < N) {
+            const size_t off = (size_t)row * ld + col;
+            // hi is also this launch's operand, which neighbouring tiles still
+            // fetch: a plain load, not an evict-first one
+            h = *reinterpret_cast<const uint4*>(hi + off);
+            l = __ldcs(reinterpret_cast<const uint4*>(lo + off));
+        }
+        xp[2 * k] = as_slot(h);
+        xp[2 * k + 1] = as_slot(l);
     }
 }
 
-// APPLY slice: X read in the staged layout (the fp32 state, or with
-// NS_IN_SRC the matrix's own input, row stride N).  y = sc*(a*x + (B X)); with NS_OUT_U, u = W - lr*y replaces
-// y and u^2 is added to hacc for the elements inside the matrix.
+// The 8 values hi + lo of pass k of a prefetch_hilo slot pair
+__device__ __forceinline__ void hilo_values(float4 hs, float4 ls, float (&x)[8]) {
+    const uint4 h = slot_bits(hs), l = slot_bits(ls);
+    const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, lw[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        x[2 * w] = bf_lo(hw[w]) + bf_lo(lw[w]);
+        x[2 * w + 1] = bf_hi(hw[w]) + bf_hi(lw[w]);
+    }
+}
+
+// hi = bf16(y) (round to nearest even), lo = bf16(y - hi): y's two-part
+// form, exact to about 16 significant bits.
+__device__ __forceinline__ void split_hilo8(const float (&y)[8], uint4& hi, uint4& lo) {
+    hi = pack_bf16x8(make_float4(y[0], y[1], y[2], y[3]), make_float4(y[4], y[5], y[6], y[7]));
+    const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
+    float r[8];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        r[2 * w] = y[2 * w] - bf_lo(hw[w]);
+        r[2 * w + 1] = y[2 * w + 1] - bf_hi(hw[w]);
+    }
+    lo = pack_bf16x8(make_float4(r[0], r[1], r[2], r[3]), make_float4(r[4], r[5], r[6], r[7]));
+}
+
+// Prefetch for POLY: A[i][j..j+7] for pass k from the bf16 operand copy A_op
+// (both triangles written by the Gram; the b*A term uses the same rounded A
+// as the A*A product), one 16-byte vector per pass, raw bits in ap[k].
+__device__ __forceinline__ void prefetch_a_st(const GemmParams& p, int g, int i0, int lane, int j0, float4 (&ap)[8]) {
+    const uint16_t* a = reinterpret_cast<const uint16_t*>(p.a_op) + (size_t)g * p.ld_s * p.M;
+    const int col = j0 + st_col(lane);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int row = i0 + st_row(lane, k);
+        ap[k] = (row < p.M && col < p.N && col + 7 >= row)
+                    ? as_slot(*reinterpret_cast<const uint4*>(a + (size_t)row * p.ld_s + col))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// The 8 values of pass k of an fp32 prefetch slot pair
+__device__ __forceinline__ void f32_values(float4 a, float4 b, float (&x)[8]) {
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// APPLY slice: X (prefetched by the caller: fp32, or the two-part state when
+// in_hilo) and the accumulator give y = sc*(a*x + (B X)).  Output: with
+// NS_OUT_U, u = W - lr*y goes to the fp32 state and u^2 is added to hacc for
+// the elements inside the matrix; with NS_OUT_W the new weight goes to the
+// caller's buffers; otherwise, when another iteration follows (x_op_out
+// set), the two-part state hi -> x_op_out (also the next Gram's operand),
+// lo -> x_lo; after the last iteration, y -> the fp32 state.
 template <int VAR>
 __device__ __forceinline__ void apply_slice_st(const GemmParams& p, const NsIO& io, bool keep_w, int g, int i0,
-                                            int lane, int j0, const float (&v)[32], float* st,
-                                            const float4 (&xp)[8], const float4 (&wp)[8], float sc, float& hacc) {
+                                               int lane, int j0, const float (&v)[32], float* st,
+                                               const float4 (&xp)[8], const float4 (&wp)[8], float sc, float& hacc) {
     stage_rows(st, lane, v);
-    const int col = j0 + (lane & 7) * 4;
-    float* xs = p.x_state + (size_t)g * p.ld_x * p.M;
-    __nv_bfloat16* xo = p.x_op_out ? p.x_op_out + (size_t)g * p.ld_x * p.M : nullptr;
+    const int col = j0 + st_col(lane);
+    const size_t moff = (size_t)g * p.ld_x * p.M;
+    float* xs = p.x_state + moff;
+    __nv_bfloat16* xo = p.x_op_out ? p.x_op_out + moff : nullptr;
+    __nv_bfloat16* xlo = p.x_lo + moff;
+    const bool hilo_in = !(VAR & NS_IN_SRC) && p.in_hilo;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int r = k * 4 + (lane >> 3), row = i0 + r;
-        const float4 a = staged(st, r, lane & 7);
-        if (row < p.M && col < p.N) {
-            float4 y;
-            y.x = sc * fmaf(p.ca, xp[k].x, a.x);
-            y.y = sc * fmaf(p.ca, xp[k].y, a.y);
-            y.z = sc * fmaf(p.ca, xp[k].z, a.z);
-            y.w = sc * fmaf(p.ca, xp[k].w, a.w);
+    for (int k = 0; k < 4; ++k) {
+        const int r = st_row(lane, k), row = i0 + r;
+        if (row >= p.M || col >= p.N) continue;
+        const float4 a0 = staged(st, r, 2 * (lane & 3)), a1 = staged(st, r, 2 * (lane & 3) + 1);
+        const float acc[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        float x[8];
+        if (hilo_in) hilo_values(xp[2 * k], xp[2 * k + 1], x);
+        else f32_values(xp[2 * k], xp[2 * k + 1], x);
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = sc * fmaf(p.ca, x[e], acc[e]);
+        if (VAR & (NS_OUT_U | NS_OUT_W)) {
+            float w[8];
+            f32_values(wp[2 * k], wp[2 * k + 1], w);
+            const int nv = p.N - col;   // >= 4: caller buffers have N % 4 == 0
             if (VAR & NS_OUT_U) {
-                y.x = fmaf(p.nlr, y.x, wp[k].x);
-                y.y = fmaf(p.nlr, y.y, wp[k].y);
-                y.z = fmaf(p.nlr, y.z, wp[k].z);
-                y.w = fmaf(p.nlr, y.w, wp[k].w);
-                const int nv = p.N - col;
-                hacc = fmaf(y.x, y.x, hacc);
-                if (nv > 1) hacc = fmaf(y.y, y.y, hacc);
-                if (nv > 2) hacc = fmaf(y.z, y.z, hacc);
-                if (nv > 3) hacc = fmaf(y.w, y.w, hacc);
-            }
-            if (VAR & NS_OUT_W) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    y[e] = fmaf(p.nlr, y[e], w[e]);
+                    if (e < nv) hacc = fmaf(y[e], y[e], hacc);
+                }
+            } else {
                 // new weight, written to the caller's buffers (row stride N)
                 if (!keep_w) {
-                    float4 u;
-                    u.x = fmaf(p.nlr, y.x, p.wdecay * wp[k].x);
-                    u.y = fmaf(p.nlr, y.y, p.wdecay * wp[k].y);
-                    u.z = fmaf(p.nlr, y.z, p.wdecay * wp[k].z);
-                    u.w = fmaf(p.nlr, y.w, p.wdecay * wp[k].w);
+                    float u[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) u[e] = fmaf(p.nlr, y[e], p.wdecay * w[e]);
                     const size_t woff = (size_t)row * p.N + col;
-                    __stcs(reinterpret_cast<float4*>(io.w + woff), u);
-                    if (io.wb) store_bf16x4(reinterpret_cast<__nv_bfloat16*>(io.wb) + woff, u);
+                    float4* wq = reinterpret_cast<float4*>(io.w + woff);
+                    __stcs(wq, make_float4(u[0], u[1], u[2], u[3]));
+                    if (nv > 4) __stcs(wq + 1, make_float4(u[4], u[5], u[6], u[7]));
+                    if (io.wb) {
+                        __nv_bfloat16* wb = reinterpret_cast<__nv_bfloat16*>(io.wb) + woff;
+                        const uint4 pk = pack_bf16x8(make_float4(u[0], u[1], u[2], u[3]),
+                                                     make_float4(u[4], u[5], u[6], u[7]));
+                        if (nv > 4 && (woff & 7) == 0) {
+                            *reinterpret_cast<uint4*>(wb) = pk;
+                        } else {
+                            *reinterpret_cast<uint2*>(wb) = make_uint2(pk.x, pk.y);
+                            if (nv > 4) *reinterpret_cast<uint2*>(wb + 4) = make_uint2(pk.z, pk.w);
+                        }
+                    }
                 }
                 continue;
             }
-            // the fp32 state is read again only by the next apply's epilogue:
-            // streaming store, so it does not push the GEMM operands out of L2
-            const size_t off = (size_t)row * p.ld_x + col;
-            __stcs(reinterpret_cast<float4*>(xs + off), y);
-            if (xo) store_bf16x4(xo + off, y);
+        }
+        const size_t off = (size_t)row * p.ld_x + col;
+        if (!(VAR & NS_OUT_U) && xo) {
+            uint4 hi, lo;
+            split_hilo8(y, hi, lo);
+            *reinterpret_cast<uint4*>(xo + off) = hi;
+            // lo is read again only by the next apply's epilogue: streaming
+            // store, so it does not push the GEMM operands out of L2
+            __stcs(reinterpret_cast<uint4*>(xlo + off), lo);
+        } else {
+            float4* q = reinterpret_cast<float4*>(xs + off);
+            __stcs(q, make_float4(y[0], y[1], y[2], y[3]));
+            __stcs(q + 1, make_float4(y[4], y[5], y[6], y[7]));
         }
     }
 }
 
 // GRAM / POLY: element (i, j) is written when j >= i, its mirror (j, i) when
-// j > i; tiles entirely below the diagonal are never scheduled.
+// j > i; tiles entirely below the diagonal are never scheduled.  The
+// polynomial's b*A term comes from A_op (ap: raw bits, one 16-byte vector per
+// pass), so both the element and its mirror get c*(A A) + b*A.
 template <int MODE>
 __device__ __forceinline__ void sym_slice_st(const GemmParams& p, int g, int i0, int lane, int j0, float (&v)[32],
-                                          float* st, const float (&ap)[32], float sc) {
+                                             float* st, const float4 (&ap)[8], float sc) {
     const int M = p.M, N = p.N;
-    const int i = i0 + lane;
-    const bool row_ok = i < M;
     const size_t mbase = (size_t)g * p.ld_s * M;
     if (MODE == NS_GRAM) {
 #pragma unroll
         for (int t = 0; t < 32; ++t) v[t] *= sc;
     } else {
 #pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = fmaf(p.cb, ap[t], p.cc * v[t]);
+        for (int t = 0; t < 32; ++t) v[t] *= p.cc;
     }
-    float* af = (MODE == NS_GRAM) ? p.a_f32 + mbase : nullptr;
     __nv_bfloat16* ob = p.sym_bf16 + mbase;
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-        const int j = j0 + t;
-        if (row_ok && j > i && j < N) {
-            if (MODE == NS_GRAM) af[(size_t)j * p.ld_s + i] = v[t];
-            ob[(size_t)j * p.ld_s + i] = __float2bfloat16_rn(v[t]);
-        }
-    }
     stage_rows(st, lane, v);
-    const int col = j0 + (lane & 7) * 4;
+    const int col = j0 + st_col(lane);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int r = k * 4 + (lane >> 3), row = i0 + r;
-        if (row >= M || col >= N || col + 3 < row) continue;
-        const float4 y = staged(st, r, lane & 7);
+    for (int k = 0; k < 4; ++k) {
+        const int r = st_row(lane, k), row = i0 + r;
+        if (row >= M || col >= N || col + 7 < row) continue;
+        const float4 a0 = staged(st, r, 2 * (lane & 3)), a1 = staged(st, r, 2 * (lane & 3) + 1);
+        float y[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        if (MODE == NS_POLY) {
+            const uint4 aw = slot_bits(ap[k]);
+            const uint32_t w4[4] = {aw.x, aw.y, aw.z, aw.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                y[2 * w] = fmaf(p.cb, bf_lo(w4[w]), y[2 * w]);
+                y[2 * w + 1] = fmaf(p.cb, bf_hi(w4[w]), y[2 * w + 1]);
+            }
+        }
         const size_t off = (size_t)row * p.ld_s + col;
-        const float ys[4] = {y.x, y.y, y.z, y.w};
-        // fp32 A: the diagonal here, the rest as the mirror (the lower
-        // triangle is the one the polynomial's epilogue reads)
-        if (MODE == NS_GRAM && row >= col && row < col + 4 && row < N) af[off + (row - col)] = ys[row - col];
-        if (col >= row) {
-            store_bf16x4(ob + off, y);
+        if (col >= row && col + 8 <= N) {
+            *reinterpret_cast<uint4*>(ob + off) =
+                pack_bf16x8(make_float4(y[0], y[1], y[2], y[3]), make_float4(y[4], y[5], y[6], y[7]));
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (col + e >= row && col + e < N) ob[off + e] = __float2bfloat16_rn(ys[e]);
+            for (int e = 0; e < 8; ++e)
+                if (col + e >= row && col + e < N) ob[off + e] = __float2bfloat16_rn(y[e]);
         }
+        // mirrors (strictly above the diagonal): for each e, the warp's lanes
+        // write 8 consecutive elements of 4 transposed rows
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (col + e > row && col + e < N) ob[(size_t)(col + e) * p.ld_s + row] = __float2bfloat16_rn(y[e]);
     }
 }
 
-// ---- epilogues, fragment layout (two-K-step pipelines) ------------------------------
+// ---- epilogue, fragment layout (the Gram with two-K-step pipelines) ------------------
 // The accumulator is read with tcgen05.ld.16x256b: two loads (TMEM lanes
 // +0..15 and +16..31 of this warp's lane quarter) of four 8-column groups
 // give each thread, for a 32 x 32 slice at (i0, j0), the values
@@ -290,11 +394,9 @@ __device__ __forceinline__ void sym_slice_st(const GemmParams& p, int g, int i0,
 // for rr, j in 0..3 and e in 0..1: four rows and four column pairs.  Four
 // consecutive lanes hold 8 consecutive columns (32 bytes) of one row, so
 // every row-wise global access is in whole 32-byte sectors without staging
-// the slice in shared memory; for the mirror of a symmetric product, eight
-// lanes with the same lane%4 hold 8 consecutive rows of one column, which
-// are 8 consecutive elements of the transposed row.  Operands the epilogue
-// reads (X for APPLY, A for POLY) are loaded in the same layout one slice
-// ahead so that their latency overlaps the previous slice's stores.
+// the slice in shared memory; for the mirror, eight lanes with the same
+// lane%4 hold 8 consecutive rows of one column, which are 8 consecutive
+// elements of the transposed row.
 
 __device__ __forceinline__ int quad_row(int lane, int rr) { return 8 * rr + (lane >> 2); }
 __device__ __forceinline__ int quad_col(int lane, int j) { return 8 * j + 2 * (lane & 3); }
@@ -303,101 +405,12 @@ __device__ __forceinline__ void store_bf16x2(__nv_bfloat16* dst, float a, float 
     *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(a, b);
 }
 
-// Prefetch in the fragment layout from a row-major array with row stride
-// `ld`: xp[rr][j] = X[i0 + row(rr)][j0 + col(j) .. +1].  For the fp32 state
-// the row stride is a multiple of 8 elements, so a pair at a column < N stays
-// inside the padded row (padding columns are never read back); a caller's
-// buffer (row stride N) is read this way only when N % 4 == 0.
-__device__ __forceinline__ void prefetch_q(const float* base, int ld, int M, int N, int i0, int lane, int j0,
-                                           float2 (&xp)[16]) {
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-        const int row = i0 + quad_row(lane, rr);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int col = j0 + quad_col(lane, j);
-            xp[4 * rr + j] = (row < M && col < N)
-                                 ? __ldcs(reinterpret_cast<const float2*>(base + (size_t)row * ld + col))
-                                 : make_float2(0.f, 0.f);
-        }
-    }
-}
-
-// Prefetch for POLY: A[i][j] at this thread's positions on or above the
-// diagonal, read as A[j][i] (A is exactly symmetric; the Gram writes the fp32
-// A's lower triangle and diagonal only).
-__device__ __forceinline__ void prefetch_a(const GemmParams& p, int g, int i0, int lane, int j0, float2 (&ap)[16]) {
-    const float* a = p.a_f32 + (size_t)g * p.ld_s * p.M;
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-        const int row = i0 + quad_row(lane, rr);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int col = j0 + quad_col(lane, j);
-            const bool ok = row < p.M;
-            ap[4 * rr + j].x = (ok && col < p.N && col >= row) ? a[(size_t)col * p.ld_s + row] : 0.f;
-            ap[4 * rr + j].y = (ok && col + 1 < p.N && col + 1 >= row) ? a[(size_t)(col + 1) * p.ld_s + row] : 0.f;
-        }
-    }
-}
-
-// APPLY slice: y = sc*(a*x + (B X)), X from the fp32 state (or with
-// NS_IN_SRC the matrix's own input, row stride N).  With NS_OUT_U, u = W -
-// lr*y replaces y and u^2 is added to hacc for the elements inside the
-// matrix; with NS_OUT_W the new weight goes to the caller's buffers.
-template <int VAR>
-__device__ __forceinline__ void apply_slice(const GemmParams& p, const NsIO& io, bool keep_w, int g, int i0,
-                                            int lane, int j0, const float (&v)[32], const float2 (&xp)[16],
-                                            const float2 (&wp)[16], float sc, float& hacc) {
-    float* xs = p.x_state + (size_t)g * p.ld_x * p.M;
-    __nv_bfloat16* xo = p.x_op_out ? p.x_op_out + (size_t)g * p.ld_x * p.M : nullptr;
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-        const int row = i0 + quad_row(lane, rr);
-        if (row >= p.M) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int col = j0 + quad_col(lane, j);
-            if (col >= p.N) continue;
-            const int q = 4 * rr + j;
-            float2 y;
-            y.x = sc * fmaf(p.ca, xp[q].x, v[2 * q]);
-            y.y = sc * fmaf(p.ca, xp[q].y, v[2 * q + 1]);
-            if (VAR & NS_OUT_U) {
-                y.x = fmaf(p.nlr, y.x, wp[q].x);
-                y.y = fmaf(p.nlr, y.y, wp[q].y);
-                hacc = fmaf(y.x, y.x, hacc);
-                if (col + 1 < p.N) hacc = fmaf(y.y, y.y, hacc);
-            }
-            if (VAR & NS_OUT_W) {
-                // new weight, written to the caller's buffers (row stride N)
-                if (!keep_w) {
-                    float2 u;
-                    u.x = fmaf(p.nlr, y.x, p.wdecay * wp[q].x);
-                    u.y = fmaf(p.nlr, y.y, p.wdecay * wp[q].y);
-                    const size_t woff = (size_t)row * p.N + col;
-                    __stcs(reinterpret_cast<float2*>(io.w + woff), u);
-                    if (io.wb) store_bf16x2(reinterpret_cast<__nv_bfloat16*>(io.wb) + woff, u.x, u.y);
-                }
-                continue;
-            }
-            // the fp32 state is read again only by the next apply's epilogue:
-            // streaming store, so it does not push the GEMM operands out of L2
-            const size_t off = (size_t)row * p.ld_x + col;
-            __stcs(reinterpret_cast<float2*>(xs + off), y);
-            if (xo) store_bf16x2(xo + off, y.x, y.y);
-        }
-    }
-}
-
-// GRAM / POLY slice: element (i, j) is written when j >= i, its mirror (j, i)
-// when j > i; tiles entirely below the diagonal are never scheduled.
-template <int MODE>
-__device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, int lane, int j0, const float (&v)[32],
-                                          const float2 (&ap)[16], float sc) {
+// GRAM slice: element (i, j) is written when j >= i, its mirror (j, i) when
+// j > i; tiles entirely below the diagonal are never scheduled.
+__device__ __forceinline__ void gram_slice(const GemmParams& p, int g, int i0, int lane, int j0, const float (&v)[32],
+                                           float sc) {
     const int M = p.M, N = p.N;
     const size_t mbase = (size_t)g * p.ld_s * M;
-    float* af = (MODE == NS_GRAM) ? p.a_f32 + mbase : nullptr;
     __nv_bfloat16* ob = p.sym_bf16 + mbase;
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
@@ -408,22 +421,9 @@ __device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, in
             const int col = j0 + quad_col(lane, j);
             if (col >= N || col + 1 < row) continue;
             const int q = 4 * rr + j;
-            float y0, y1;
-            if (MODE == NS_GRAM) {
-                y0 = sc * v[2 * q];
-                y1 = sc * v[2 * q + 1];
-            } else {
-                y0 = fmaf(p.cb, ap[q].x, p.cc * v[2 * q]);
-                y1 = fmaf(p.cb, ap[q].y, p.cc * v[2 * q + 1]);
-            }
+            const float y0 = sc * v[2 * q], y1 = sc * v[2 * q + 1];
             const size_t off = (size_t)row * p.ld_s + col;
             const bool in1 = col + 1 < N;
-            // fp32 A: the diagonal here, the rest as the mirror (the lower
-            // triangle is the one the polynomial's epilogue reads)
-            if (MODE == NS_GRAM) {
-                if (col == row) af[off] = y0;
-                if (in1 && col + 1 == row) af[off + 1] = y1;
-            }
             if (col >= row && in1) {
                 store_bf16x2(ob + off, y0, y1);
             } else {
@@ -432,14 +432,8 @@ __device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, in
                 if (in1 && col + 1 >= row) ob[off + 1] = __float2bfloat16_rn(y1);
             }
             // mirrors (strictly above the diagonal)
-            if (col > row) {
-                if (MODE == NS_GRAM) af[(size_t)col * p.ld_s + row] = y0;
-                ob[(size_t)col * p.ld_s + row] = __float2bfloat16_rn(y0);
-            }
-            if (in1 && col + 1 > row) {
-                if (MODE == NS_GRAM) af[(size_t)(col + 1) * p.ld_s + row] = y1;
-                ob[(size_t)(col + 1) * p.ld_s + row] = __float2bfloat16_rn(y1);
-            }
+            if (col > row) ob[(size_t)col * p.ld_s + row] = __float2bfloat16_rn(y0);
+            if (in1 && col + 1 > row) ob[(size_t)(col + 1) * p.ld_s + row] = __float2bfloat16_rn(y1);
         }
     }
 }
@@ -450,7 +444,7 @@ __device__ __forceinline__ void sym_slice(const GemmParams& p, int g, int i0, in
 // accumulator, releases it after the last TMEM read (`release`), and for
 // NS_OUT_U writes this warp's ||U||^2 partial to *upart_slot (0 when the
 // warp's rows or columns fall outside the matrix).  False if the wait gave up.
-// QUAD selects the fragment-layout epilogue (no staging); otherwise slices
+// QUAD (the Gram only) selects the fragment-layout epilogue; otherwise slices
 // pass through the warp's 4 KB staging tile `st`.
 //
 // Split-K Gram (`kp0` set): this warp's partial for K range `split` goes to
@@ -464,12 +458,21 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
                                               volatile int* abort_flag, double* upart_slot, Release release,
                                               float* kp0 = nullptr, size_t kstride = 0, int split = 0,
                                               int* kcnt = nullptr) {
+    static_assert(!QUAD || MODE == NS_GRAM, "the fragment-layout epilogue serves the Gram");
     const int nsl = max(0, min(BN / 64, (p.N - jb + 31) / 32));
     float sc = 1.f;
     if (MODE != NS_POLY && p.scale) sc = p.scale[g];
     auto load_slice = [&](uint32_t taddr, float (&v)[32]) {
         if constexpr (QUAD) tmem_ld_quad32(taddr, v);
         else tmem_ld32(taddr, v);
+    };
+    auto gram_out = [&](int j0, float (&v)[32]) {
+        if constexpr (QUAD) {
+            gram_slice(p, g, i0, lane, j0, v, sc);
+        } else {
+            const float4 unused[8] = {};
+            sym_slice_st<NS_GRAM>(p, g, i0, lane, j0, v, st, unused, sc);
+        }
     };
     if (MODE == NS_GRAM && kp0 != nullptr) {
         if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, wait_limit(p))) return false;
@@ -511,103 +514,102 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] += __ldcg(part + (32 * k + i) * 32 + lane);
                 }
-                if constexpr (QUAD) {
-                    const float2 unused[16] = {};
-                    sym_slice<NS_GRAM>(p, g, i0, lane, jb + 32 * k, v, unused, sc);
-                } else {
-                    const float unused[32] = {};
-                    sym_slice_st<NS_GRAM>(p, g, i0, lane, jb + 32 * k, v, st, unused, sc);
-                }
+                gram_out(jb + 32 * k, v);
             }
         }
         return true;
     }
-    // X source of the apply epilogue: the fp32 state (row stride ld_x), or
-    // the matrix's own input (row stride N; the variants need N % 4 == 0)
-    NsIO io{nullptr, nullptr, nullptr};
-    const float* xbase = nullptr;
-    int xld = p.ld_x;
-    if (MODE == NS_APPLY) {
-        if (VAR != 0) io = p.io[g];
-        if (VAR & NS_IN_SRC) {
-            xbase = io.src;
-            xld = p.N;
-        } else {
-            xbase = p.x_state + (size_t)g * p.ld_x * p.M;
-        }
-    }
-    // Operands the epilogue reads are loaded one slice ahead.  With
-    // NS_OUT_U / NS_OUT_W both X and W are read for the current slice only,
-    // at its start (the register budget holds two 32-value slices, not four).
-    constexpr bool reads_w = MODE == NS_APPLY && (VAR & (NS_OUT_U | NS_OUT_W));
-    constexpr bool ahead = !reads_w;
-    const bool keep_w = (MODE == NS_APPLY && (VAR & NS_OUT_W)) ? p.mflags[g] != 0 : false;
-    // prefetched operands: 32 floats per slice in either layout
-    using Pre = typename std::conditional<QUAD, float2[16], float4[8]>::type;
-    Pre xc, xn, wc;
-    float ac[32], an[32];
-    auto pre_x = [&](int j0, Pre& dst) {
-        if constexpr (QUAD) prefetch_q(xbase, xld, p.M, p.N, i0, lane, j0, dst);
-        else prefetch_rm(xbase, xld, p.M, p.N, i0, lane, j0, dst);
-    };
-    auto pre_w = [&](int j0, Pre& dst) {
-        if constexpr (QUAD) prefetch_q(io.w, p.N, p.M, p.N, i0, lane, j0, dst);
-        else prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, j0, dst);
-    };
-    auto pre_a = [&](int j0, float (&dst)[32]) {
-        if constexpr (QUAD) prefetch_a(p, g, i0, lane, j0, *reinterpret_cast<float2(*)[16]>(&dst));
-        else prefetch_a_st(p, g, i0, lane, j0, dst);
-    };
-    if (nsl > 0) {
-        if (MODE == NS_APPLY) pre_x(jb, xc);
-        if (reads_w) pre_w(jb, wc);
-        if (MODE == NS_POLY) pre_a(jb, ac);
-    }
-    if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, wait_limit(p))) return false;
-    tc_fence_after();
-    if (nsl == 0) release();
-    float hacc = 0.f;
+    if constexpr (QUAD) {
+        if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, wait_limit(p))) return false;
+        tc_fence_after();
+        if (nsl == 0) release();
 #pragma unroll
-    for (int k = 0; k < BN / 64; ++k) {
-        if (k < nsl) {
-            const int j0 = jb + 32 * k;
-            if (!ahead && k > 0) {
-                pre_x(j0, xc);
-                pre_w(j0, wc);
-            }
-            float v[32];
-            load_slice(trow + 32 * k, v);
-            if (k == nsl - 1) {
-                // last read of this accumulator by this warp
-                tc_fence_before();
-                release();
-            }
-            if (k + 1 < nsl) {
-                if (MODE == NS_APPLY && ahead) pre_x(j0 + 32, xn);
-                if (MODE == NS_POLY) pre_a(j0 + 32, an);
-            }
-            if (MODE == NS_APPLY) {
-                if constexpr (QUAD) apply_slice<VAR>(p, io, keep_w, g, i0, lane, j0, v, xc, wc, sc, hacc);
-                else apply_slice_st<VAR>(p, io, keep_w, g, i0, lane, j0, v, st, xc, wc, sc, hacc);
-                if (ahead) {
-#pragma unroll
-                    for (int u = 0; u < (QUAD ? 16 : 8); ++u) xc[u] = xn[u];
+        for (int k = 0; k < BN / 64; ++k) {
+            if (k < nsl) {
+                float v[32];
+                load_slice(trow + 32 * k, v);
+                if (k == nsl - 1) {
+                    tc_fence_before();
+                    release();
                 }
-            } else {
-                if constexpr (QUAD) sym_slice<MODE>(p, g, i0, lane, j0, v, *reinterpret_cast<float2(*)[16]>(&ac), sc);
-                else sym_slice_st<MODE>(p, g, i0, lane, j0, v, st, ac, sc);
-                if (MODE == NS_POLY) {
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) ac[u] = an[u];
-                }
+                gram_out(jb + 32 * k, v);
             }
         }
+        return true;
+    } else {
+        // Where the apply epilogue reads X: the matrix's own input (NS_IN_SRC,
+        // fp32, row stride N; the variants need N % 4 == 0), the two-part
+        // state written by the previous apply (in_hilo), or the fp32 state
+        // written by the momentum kernel.
+        NsIO io{nullptr, nullptr, nullptr};
+        if (MODE == NS_APPLY && VAR != 0) io = p.io[g];
+        const size_t xoff = (size_t)g * p.ld_x * p.M;
+        auto pre_x = [&](int j0, float4 (&dst)[8]) {
+            if (VAR & NS_IN_SRC)
+                prefetch_rm(io.src, p.N, p.M, p.N, i0, lane, j0, dst, true);
+            else if (p.in_hilo)
+                prefetch_hilo(p.x_hi + xoff, p.x_lo + xoff, p.ld_x, p.M, p.N, i0, lane, j0, dst);
+            else
+                prefetch_rm(p.x_state + xoff, p.ld_x, p.M, p.N, i0, lane, j0, dst);
+        };
+        // Operands the epilogue reads are loaded one slice ahead.  With
+        // NS_OUT_U / NS_OUT_W both X and W are read for the current slice
+        // only, at its start (the register budget holds two 32-value slices,
+        // not four).
+        constexpr bool reads_w = MODE == NS_APPLY && (VAR & (NS_OUT_U | NS_OUT_W));
+        constexpr bool ahead = !reads_w;
+        const bool keep_w = (MODE == NS_APPLY && (VAR & NS_OUT_W)) ? p.mflags[g] != 0 : false;
+        float4 xc[8], xn[8], wc[8];
+        float4 ac[8], an[8];   // POLY: A_op, raw bits (4 of 8 used)
+        if (nsl > 0) {
+            if (MODE == NS_APPLY) pre_x(jb, xc);
+            if (reads_w) prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, jb, wc, true);
+            if (MODE == NS_POLY) prefetch_a_st(p, g, i0, lane, jb, ac);
+        }
+        if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, wait_limit(p))) return false;
+        tc_fence_after();
+        if (nsl == 0) release();
+        float hacc = 0.f;
+#pragma unroll
+        for (int k = 0; k < BN / 64; ++k) {
+            if (k < nsl) {
+                const int j0 = jb + 32 * k;
+                if (!ahead && k > 0) {
+                    pre_x(j0, xc);
+                    prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, j0, wc, true);
+                }
+                float v[32];
+                load_slice(trow + 32 * k, v);
+                if (k == nsl - 1) {
+                    // last read of this accumulator by this warp
+                    tc_fence_before();
+                    release();
+                }
+                if (k + 1 < nsl) {
+                    if (MODE == NS_APPLY && ahead) pre_x(j0 + 32, xn);
+                    if (MODE == NS_POLY) prefetch_a_st(p, g, i0, lane, j0 + 32, an);
+                }
+                if (MODE == NS_APPLY) {
+                    apply_slice_st<VAR>(p, io, keep_w, g, i0, lane, j0, v, st, xc, wc, sc, hacc);
+                    if (ahead) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) xc[u] = xn[u];
+                    }
+                } else {
+                    sym_slice_st<MODE>(p, g, i0, lane, j0, v, st, ac, sc);
+                    if (MODE == NS_POLY) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) ac[u] = an[u];
+                    }
+                }
+            }
+        }
+        if (MODE == NS_APPLY && (VAR & NS_OUT_U)) {
+            const double s = warp_sum((double)hacc);
+            if (lane == 0 && upart_slot) *upart_slot = s;
+        }
+        return true;
     }
-    if (MODE == NS_APPLY && (VAR & NS_OUT_U)) {
-        const double s = warp_sum((double)hacc);
-        if (lane == 0 && upart_slot) *upart_slot = s;
-    }
-    return true;
 }
 
 // ---- the kernel ----------------------------------------------------------------
@@ -1352,10 +1354,11 @@ template <int KIND>
 static cudaError_t dispatch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, long long total,
                             cudaStream_t st) {
 #define MUONH_LAUNCH(M_, V_)                                                                      \
-    (KIND == kGemmPair         ? launch_pair<M_, V_, 2>(ta, tb, p, total, st)                      \
-     : KIND == kGemmPairStep1  ? launch_pair<M_, V_, 1>(ta, tb, p, total, st)                      \
-                               : launch_single<M_, V_>(ta, tb, p, total, st))
-    if (p.mode == NS_GRAM) return MUONH_LAUNCH(NS_GRAM, 0);
+    (KIND == kGemmPair || KIND == kGemmPairStep1 ? launch_pair<M_, V_, 1>(ta, tb, p, total, st)   \
+                                                 : launch_single<M_, V_>(ta, tb, p, total, st))
+    // two K steps per stage: the Gram only (the launcher picks the kind)
+    if (p.mode == NS_GRAM)
+        return KIND == kGemmPair ? launch_pair<NS_GRAM, 0, 2>(ta, tb, p, total, st) : MUONH_LAUNCH(NS_GRAM, 0);
     if (p.mode == NS_POLY) return MUONH_LAUNCH(NS_POLY, 0);
     switch (p.variant) {
         case 0: return MUONH_LAUNCH(NS_APPLY, 0);
@@ -1398,15 +1401,11 @@ cudaError_t launch_ns_gemm(GemmParams p, const void* a_op, int a_ld, const void*
     // vs 745, apply 635-675 vs 636-669.  Three 64 KB stages keep less data
     // in flight than six 32 KB ones, which only the tall Gram's four 8 KB
     // MN-major boxes per step outweigh; the other launches keep one step.
-#ifndef MUONH_KPS2_RULE
-#define MUONH_KPS2_RULE 0
-#endif
-    // MUONH_KPS2_RULE (build-time): 0 two-step stages for the tall Gram only,
-    // 1 for every Gram and polynomial, 2 for every launch whose shape allows
-    const bool two_step_ok = (p.K % 64) == 0 && (!p.a_mn || (p.M % 64) == 0) && (!p.b_mn || (p.N % 64) == 0);
-    const bool two_step_wanted = MUONH_KPS2_RULE == 2   ? true
-                                 : MUONH_KPS2_RULE == 1 ? p.mode != NS_APPLY
-                                                        : (p.mode == NS_GRAM && p.a_mn);
+    // Two-step stages for the tall Gram only (MN-major operands, whose one-
+    // step stages take four 8 KB boxes); measured slower for every other
+    // launch kind (see the comment above)
+    const bool two_step_ok = (p.K % 64) == 0 && (p.M % 64) == 0 && (p.N % 64) == 0;
+    const bool two_step_wanted = p.mode == NS_GRAM && p.a_mn;
     if (kind == kGemmPair && !(two_step_ok && two_step_wanted)) kind = kGemmPairStep1;
     const bool multi = kind != kGemmSingle;
     const int a_box = BM;

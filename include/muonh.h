@@ -230,8 +230,8 @@ int muonh_orthogonalize(const void* in, int in_dtype, void* out, int out_dtype, 
  * library holds in device memory (a file-scope __device__ variable), on
  * every device that loads the library, until the process exits.  Shapes
  * whose muonh_orthogonalize_workspace_size() exceeds it are rejected with
- * MUONH_ERR_WORKSPACE and a message (muonh_last_error); 2048 x 2048 and
- * 1024 x 8192 fit.
+ * MUONH_ERR_WORKSPACE and a message (muonh_last_error); 2048 x 2048,
+ * 2048 x 4096 and 1024 x 6144 fit.
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and keeps it, keyed by
