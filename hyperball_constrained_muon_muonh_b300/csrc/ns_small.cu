@@ -17,14 +17,18 @@
 //     AR  this CTA's 128 rows of A, then of B, K-major
 //
 // One iteration (a, b, c the coefficients):
-//   GRAM  acc = X X^T;  epilogue: A = acc (x inv^2 at the first iteration),
+//   GRAM  acc = X X^T;  epilogue: A = sigma^2 acc,
 //         AR = bf16(A), acc <- (b/c) A
-//   POLY  acc += A A;   epilogue: B = c acc (x inv at the first iteration),
-//         AR = bf16(B), X <- a X (x inv at the first iteration)
-//   APPLY X += B X;     epilogue: XR, XC = bf16(X) unless last
-// so X_{k+1} = a X_k + (b A + c A^2) X_k, with the first iteration's
-// 1/(||X0|| + eps) folded in as the tensor-core path does.  The step reads
-// G, M and W and writes M, W and the bf16 copy: 22 bytes per element.
+//   POLY  acc += A A;   epilogue: B' = c acc / a, AR = bf16(B')
+//   APPLY X += B' X;    epilogue: XR, XC = bf16(X) unless last
+// so X_{k+1} = a X_k + (b A + c A^2) X_k.  TMEM holds X up to a scalar
+// sigma (the iterate is sigma X): sigma starts at 1/(||X0|| + eps), the
+// Gram's epilogue scales A by sigma^2, and the factor a goes into sigma
+// instead of into a pass over X (sigma <- a sigma).  Should a sigma leave
+// [2^-32, 2^32] (or a = 0), that iteration folds it into X instead:
+// X <- (sigma a) X, B' = sigma B, sigma = 1.  The write-out scales O by sigma.
+// The step reads G, M and W and writes M, W and the bf16 copy: 22 bytes per
+// element.
 //
 // Every wait is bounded; after a timeout the CTA raises
 // MUONH_STATUS_KERNEL_TIMEOUT and runs on through the same barrier sequence
@@ -462,8 +466,9 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
         publish();
 
         // ---- Newton-Schulz iterations ----
+        float sigma = inv;   // the iterate is sigma times the X held in TMEM
         for (int it = 0; it < p.ns_steps; ++it) {
-            const bool first = it == 0, last = it + 1 == p.ns_steps;
+            const bool last = it + 1 == p.ns_steps;
             if (last && threadIdx.x == 0) {
                 // While the last iteration runs on chip, pull into L2 this
                 // matrix's weight (read by the write-out) and the gradient and
@@ -480,7 +485,7 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
             }
             mma_gram(xr, tmem + 256);
             wait_mma();
-            const float sa = first ? inv * inv : 1.f;
+            const float sa = sigma * sigma;
 #pragma unroll 1
             for (int k = 0; k < 4; ++k) {
                 const int j0 = 128 * h + 32 * k;
@@ -498,20 +503,27 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
                 mma_acc(ar, ar, false, tmem + 256);   // acc += A A, onto the (b/c) A preload
                 wait_mma();
             }
-            const float sb = first ? inv : 1.f;
+            // the a X term: a goes into sigma while sigma a stays in range;
+            // otherwise X <- (sigma a) X here, B' = sigma B and sigma = 1
+            const float sig_a = sigma * p.ca;
+            const bool defer = p.ca != 0.f && fabsf(sig_a) <= 0x1p32f && fabsf(sig_a) >= 0x1p-32f;
+            const float pb = (p.cc != 0.f ? p.cc : 1.f) * (defer ? 1.f / p.ca : sigma);
 #pragma unroll 1
             for (int k = 0; k < 4; ++k) {
                 const int j0 = 128 * h + 32 * k;
                 float v[32];
                 tmem_ld32(tacc + j0, v);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] = (p.cc != 0.f ? p.cc * v[t] : v[t]) * sb;
+                for (int t = 0; t < 32; ++t) v[t] *= pb;
                 put_kmajor(ar, row_l, j0, v);
-                tmem_ld32(tx + j0, v);
+                if (!defer) {
+                    tmem_ld32(tx + j0, v);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] = (p.ca * v[t]) * sb;
-                tmem_st32(tx + j0, v);
+                    for (int t = 0; t < 32; ++t) v[t] *= sig_a;
+                    tmem_st32(tx + j0, v);
+                }
             }
+            sigma = defer ? sig_a : 1.f;
             publish();
             mma_acc(ar, xcl, true, tmem);   // X += B X
             wait_mma();
@@ -532,7 +544,7 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
         // Whole 256-column rows go coalesced: O through the staging tile, W
         // loaded one slice ahead, U kept in the U buffer (shared memory) for
         // the rescale.  Other shapes: element access, U in the accumulator.
-        const float nlr = -p.lr * update_scale(R, C, p.scale_mode);
+        const float nlr = -p.lr * update_scale(R, C, p.scale_mode) * sigma;   // O = sigma X
         const bool keep = !finite || *abort_flag;
         auto o_coalesced = [&](int j0, float4 (&o4)[8]) {
             float o[32];

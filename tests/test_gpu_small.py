@@ -43,11 +43,12 @@ def _run(work, optimizer, steps=2, flags=0, nesterov=False, scale="none", wd=0.1
     ws = work.weights("cuda")
     idx = list(range(len(ws))) if idx is None else idx
     if optimizer == "muonh":
-        opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps, bf16_copies=True, flags=flags)
+        opt = mh.MuonH(ws, lr=work.lr, beta=work.beta, ns_steps=work.ns_steps, ns_coeffs=work.coeffs, eps=work.eps,
+                       bf16_copies=True, flags=flags)
         r0 = opt.r0.cpu().numpy().astype(np.float64)
     else:
-        opt = mh.Muon(ws, lr=work.lr, beta=work.beta, weight_decay=wd, ns_steps=work.ns_steps, bf16_copies=True,
-                      flags=flags)
+        opt = mh.Muon(ws, lr=work.lr, beta=work.beta, weight_decay=wd, ns_steps=work.ns_steps,
+                      ns_coeffs=work.coeffs, eps=work.eps, bf16_copies=True, flags=flags)
     lr, beta, eps = _f32(work.lr), _f32(work.beta), _f32(work.eps)
     coeffs = tuple(_f32(c) for c in work.coeffs)
     for t in range(steps):
@@ -113,6 +114,27 @@ def test_small_short_iteration_counts(steps_ns):
 def test_small_variants():
     _run(wl.ragged(SHAPES), "muonh", flags=mh.FLAG_NESTEROV | mh.FLAG_SCALE_SHAPE, nesterov=True, scale="shape")
     _run(wl.ragged(SHAPES), "muon", flags=mh.FLAG_SCALE_RMS, scale="rms")
+
+
+@pytest.mark.parametrize("g_scale,eps", [(1e12, 1e-7), (1e-12, 0.0)])
+def test_small_extreme_norms_fold_the_scale_into_x(g_scale, eps):
+    # The kernel keeps X in TMEM up to a scalar sigma (starting at
+    # 1/(||M|| + eps), times a per iteration).  Gradients of 1e12 (sigma below
+    # 2^-32) and of 1e-12 with eps = 0 (sigma above 2^32) make it fold sigma
+    # into X instead, at the first iteration; the result must not change.
+    work = wl.ragged(SHAPES[:6])
+    work.g_scale, work.eps = g_scale, eps
+    _run(work, "muonh")
+    _run(work, "muon")
+
+
+@pytest.mark.parametrize("coeffs", [(0.0, 1.5, -0.5), (1.5, -0.5, 0.0)])
+def test_small_coefficients_with_a_zero_term(coeffs):
+    # a = 0: no a*X term (the scale cannot be kept in sigma); c = 0: no A*A product
+    work = wl.ragged(SHAPES[:6])
+    work.coeffs = coeffs
+    _run(work, "muonh")
+    _run(work, "muon")
 
 
 def test_small_batched_more_than_one_launch():
