@@ -459,11 +459,27 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
             put_mnmajor(xc, i, j0, x);
         }
         }
-        const double nu2 = pair_sum(part, red, peer, peer_remote, (int)rank);
+        // ||M||^2 over the pair (the order of pair_sum: warps, then CTA 0 +
+        // CTA 1), exchanged in the cluster barrier that publishes X
+        {
+            const double v = warp_sum(part);
+            if (lane == 0) red[warp] = v;
+        }
+        tmem_st_wait();
+        fence_proxy_async();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double t = 0.0;
+            for (int k = 0; k < THREADS / 32; ++k) t += red[k];
+            peer[rank] = t;
+            st_cluster_f64(peer_remote + 8 * rank, t);
+        }
+        tc_fence_before();
+        cluster_sync();
+        const double nu2 = peer[0] + peer[1];
         const bool finite = isfinite(nu2);
         const float inv = finite ? (float)(1.0 / (sqrt(nu2) + (double)p.eps)) : 0.f;
         if (!finite && threadIdx.x == 0 && rank == 0) raise_status(p.status, MUONH_STATUS_NONFINITE_INPUT);
-        publish();
 
         // ---- Newton-Schulz iterations ----
         float sigma = inv;   // the iterate is sigma times the X held in TMEM
