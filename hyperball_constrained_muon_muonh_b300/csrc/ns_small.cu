@@ -129,6 +129,12 @@ __device__ __forceinline__ void put_mnmajor(const uint32_t (&xc)[2], int k, int 
     for (int u = 0; u < 4; ++u) st_cluster_v4(base + mnmajor_off(k, n0 + 8 * u), pack8(v + 8 * u));
 }
 
+// Cluster barrier without release semantics: prior memory accesses of this
+// thread are not ordered before it (its global stores need not be performed).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
+}
+
 // Sum of one double per thread over both CTAs of the pair, the same value
 // in every thread of both (fixed order: warps, then CTA 0 + CTA 1).
 __device__ __forceinline__ double pair_sum(double v, double* red, double* peer, uint32_t peer_remote, int rank) {
@@ -615,7 +621,7 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
                     store_w(D, tall, C, i, j0, row_ok, l, wv);
                 }
             }
-            cluster_sync();
+            cluster_sync_relaxed();   // the stores of W need not be performed first
         } else {
             double up = 0.0;
             if (coal) {
@@ -695,8 +701,11 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
                     }
                 }
             }
+            // the reduction slots, the accumulator and the U buffer are free
+            // again (every read of them has returned: its value was stored);
+            // the stores of W need not be performed first
             tc_fence_before();
-            cluster_sync();   // the reduction slots, the accumulator and the U buffer are free again
+            cluster_sync_relaxed();
             tc_fence_after();
         }
     }
