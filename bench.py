@@ -159,6 +159,19 @@ def _ns_traffic_from_profiles():
         return None
 
 
+L2_BYTES = 126 * 2 ** 20
+
+
+def _l2_note(work, optimizer):
+    """Whether a step's inputs exceed L2 (the timed steps do not flush it)."""
+    per_el = 28 if optimizer == "adamw" else 22   # bytes of state a step reads and writes per element
+    b = per_el * work.n_params
+    if b > 2 * L2_BYTES:
+        return f"inputs larger than L2 ({b / 1e9:.2f} GB of optimizer state touched per step)"
+    return (f"inputs fit in L2 ({b / 1e6:.2f} MB of optimizer state per step), not flushed between steps: "
+            "a latency figure")
+
+
 def _oracle_cores():
     try:
         from threadpoolctl import threadpool_info
@@ -591,7 +604,7 @@ def main():
         "config": {"workload": work.name, "matrices": len(work.shapes), "params": work.n_params,
                    "ns_steps": work.ns_steps, "ns_coeffs": list(work.coeffs), "beta": work.beta, "lr": work.lr,
                    "eps": work.eps, "state": "fp32 W/M/G + bf16 W copy; NS bf16 operands, iterate as bf16 hi + bf16 lo (fp32 in the first and last iterations)",
-                   "l2": "inputs larger than L2 (about 20 GB of optimizer state touched per step)",
+                   "l2": _l2_note(work, args.optimizer),
                    "parallelism": f"replica x{world}",
                    "ns_streams": "caller's stream only" if args.one_stream else
                                  "independent buckets on up to 4 streams (caller's + 3 side streams)",
