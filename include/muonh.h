@@ -205,8 +205,8 @@ int muonh_orthogonalize_workspace_size(int64_t rows, int64_t cols, uint32_t flag
  * in_dtype) is normalised by its Frobenius norm and iterated; the result O
  * is written to `out` (same shape, element type out_dtype; bf16 output is
  * the round-to-nearest-even of the fp32 result).  The model card's
- * "Training" section keeps state "in BF16 or FP32 as appropriate", hence
- * both types on either side.  `out` may equal `in` when the types match.
+ * "Training" section lets state be bf16 or fp32, whichever each needs,
+ * hence both types on either side.  `out` may equal `in` when the types match.
  * A bf16 input is widened exactly to fp32 before the iteration.  Same
  * meaning of ns_steps, ns_coeffs, eps, flags and workspace as muonh_step;
  * the workspace size does not depend on the types.  A dtype other than
