@@ -444,7 +444,7 @@ __device__ __forceinline__ void gram_slice(const GemmParams& p, int g, int i0, i
 // accumulator, releases it after the last TMEM read (`release`), and for
 // NS_OUT_U writes this warp's ||U||^2 partial to *upart_slot (0 when the
 // warp's rows or columns fall outside the matrix).  False if the wait gave up.
-// QUAD (the Gram only) selects the fragment-layout epilogue; otherwise slices
+// FRAG (the Gram only) selects the fragment-layout epilogue; otherwise slices
 // pass through the warp's 4 KB staging tile `st`.
 //
 // Split-K Gram (`kp0` set): this warp's partial for K range `split` goes to
@@ -452,22 +452,22 @@ __device__ __forceinline__ void gram_slice(const GemmParams& p, int g, int i0, i
 // (32k + i)*32 + l, so every store is one coalesced 128-byte row); after the
 // stores, one arrival on *kcnt.  The warp that brings the count to `splits`
 // resets it, sums the partials in range order and runs the epilogue.
-template <int MODE, int VAR, bool QUAD, class Release>
+template <int MODE, int VAR, bool FRAG, class Release>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0, int jb, uint32_t tfull_bar,
                                               uint32_t acc_phase, uint32_t trow, float* st, int lane,
                                               volatile int* abort_flag, double* upart_slot, Release release,
                                               float* kp0 = nullptr, size_t kstride = 0, int split = 0,
                                               int* kcnt = nullptr) {
-    static_assert(!QUAD || MODE == NS_GRAM, "the fragment-layout epilogue serves the Gram");
+    static_assert(!FRAG || MODE == NS_GRAM, "the fragment-layout epilogue serves the Gram");
     const int nsl = max(0, min(BN / 64, (p.N - jb + 31) / 32));
     float sc = 1.f;
     if (MODE != NS_POLY && p.scale) sc = p.scale[g];
     auto load_slice = [&](uint32_t taddr, float (&v)[32]) {
-        if constexpr (QUAD) tmem_ld_quad32(taddr, v);
+        if constexpr (FRAG) tmem_ld_quad32(taddr, v);
         else tmem_ld32(taddr, v);
     };
     auto gram_out = [&](int j0, float (&v)[32]) {
-        if constexpr (QUAD) {
+        if constexpr (FRAG) {
             gram_slice(p, g, i0, lane, j0, v, sc);
         } else {
             const float4 unused[8] = {};
@@ -519,7 +519,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
         }
         return true;
     }
-    if constexpr (QUAD) {
+    if constexpr (FRAG) {
         if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, wait_limit(p))) return false;
         tc_fence_after();
         if (nsl == 0) release();
