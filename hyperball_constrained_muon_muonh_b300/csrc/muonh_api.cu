@@ -753,6 +753,12 @@ int run_newton_schulz(const Plan& P, uint8_t* ws, const Scalars& sc, int ns_step
         a.mode = NS_APPLY; a.G = B.G; a.M = B.R; a.N = B.C; a.K = B.s;
         a.b_mn = !B.tall;
         a.m_outer = B.tall;
+        // Elongated matrices with a short side of at most 1024: a tile's
+        // mainloop (K = s) is short and its epilogue's reads of X are the
+        // slower side, so the epilogue prefetches them into L2.  Measured:
+        // the 16384 x 1024 set +3.4 %; enabled for every s <= 1024 it cost
+        // the 2B set 0.5 % (its 1024 x 2048 bucket), for every s 1.2 %.
+        a.epi_l2pf = B.s <= 1024 && B.l >= 4 * B.s;
         a.ld_x = B.ld_x; a.ld_s = B.ld_s;
         a.x_state = reinterpret_cast<float*>(ws + B.off_xs);
         a.x_op_out = (it + 1 < ns_steps) ? xn : nullptr;

@@ -45,6 +45,8 @@ struct GemmParams {
     int a_mn, b_mn;         // operand A / B stored MN-major
     int m_outer;            // apply: tiles ordered row panels outermost (consecutive tiles
                             // share their A panel) instead of column panels outermost
+    int epi_l2pf;           // apply: the epilogue prefetches a tile's later slices of X (and W)
+                            // into L2 when it starts the tile
     int G, M, N, K;
     int tiles_m, tiles_n, tiles_per_mat;   // filled by the launcher
     int ld_x, ld_s;

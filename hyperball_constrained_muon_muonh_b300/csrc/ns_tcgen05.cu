@@ -208,6 +208,34 @@ __device__ __forceinline__ void prefetch_hilo(const __nv_bfloat16* hi, const __n
     }
 }
 
+// L2 prefetch of what prefetch_rm / prefetch_hilo read for the slice at
+// column j0: one lane per row (lanes 4r) touches the row's segment of each
+// array; nothing is loaded into registers.
+__device__ __forceinline__ void l2_prefetch(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ void l2_prefetch_hilo(const __nv_bfloat16* hi, const __nv_bfloat16* lo, int ld, int M, int N,
+                                                 int i0, int lane, int j0) {
+    if ((lane & 3) != 0 || j0 >= N) return;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int row = i0 + st_row(lane, k);
+        if (row < M) {
+            const size_t off = (size_t)row * ld + j0;
+            l2_prefetch(hi + off);
+            l2_prefetch(lo + off);
+        }
+    }
+}
+__device__ __forceinline__ void l2_prefetch_rm(const float* base, int ld, int M, int N, int i0, int lane, int j0) {
+    if ((lane & 3) != 0 || j0 >= N) return;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int row = i0 + st_row(lane, k);
+        if (row < M) l2_prefetch(base + (size_t)row * ld + j0);
+    }
+}
+
 // The 8 values hi + lo of pass k of a prefetch_hilo slot pair
 __device__ __forceinline__ void hilo_values(float4 hs, float4 ls, float (&x)[8]) {
     const uint4 h = slot_bits(hs), l = slot_bits(ls);
@@ -552,6 +580,17 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
             else
                 prefetch_rm(p.x_state + xoff, p.ld_x, p.M, p.N, i0, lane, j0, dst);
         };
+        // L2 prefetch of the epilogue's X (and W) for later slices (when
+        // p.epi_l2pf): with one slice in registers per warp, a tile's later
+        // slices otherwise wait for DRAM one after another
+        auto l2_x = [&](int j0) {
+            if (VAR & NS_IN_SRC)
+                l2_prefetch_rm(io.src, p.N, p.M, p.N, i0, lane, j0);
+            else if (p.in_hilo)
+                l2_prefetch_hilo(p.x_hi + xoff, p.x_lo + xoff, p.ld_x, p.M, p.N, i0, lane, j0);
+            else
+                l2_prefetch_rm(p.x_state + xoff, p.ld_x, p.M, p.N, i0, lane, j0);
+        };
         // Operands the epilogue reads are loaded one slice ahead.  With
         // NS_OUT_U / NS_OUT_W both X and W are read for the current slice
         // only, at its start (the register budget holds two 32-value slices,
@@ -564,6 +603,13 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, int g, int i0
         if (nsl > 0) {
             if (MODE == NS_APPLY) pre_x(jb, xc);
             if (reads_w) prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, jb, wc, true);
+            if (MODE == NS_APPLY && p.epi_l2pf) {
+                // the tile's other slices, into L2
+                for (int k = 1; k < nsl; ++k) {
+                    l2_x(jb + 32 * k);
+                    if (reads_w) l2_prefetch_rm(io.w, p.N, p.M, p.N, i0, lane, jb + 32 * k);
+                }
+            }
             if (MODE == NS_POLY) prefetch_a_st(p, g, i0, lane, jb, ac);
         }
         if (!mbar_wait(tfull_bar, acc_phase, abort_flag, p.status, wait_limit(p))) return false;
