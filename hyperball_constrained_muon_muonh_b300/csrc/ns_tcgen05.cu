@@ -382,6 +382,10 @@ __device__ __forceinline__ void sym_slice_st(const GemmParams& p, int g, int i0,
     __nv_bfloat16* ob = p.sym_bf16 + mbase;
     stage_rows(st, lane, v);
     const int col = j0 + st_col(lane);
+    // a slice wholly above the diagonal and inside the matrix writes its
+    // mirror through the staged slice, 16 bytes per lane; others element by
+    // element
+    const bool whole = j0 > i0 + 31 && i0 + 32 <= M && j0 + 32 <= N;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int r = st_row(lane, k), row = i0 + r;
@@ -396,6 +400,13 @@ __device__ __forceinline__ void sym_slice_st(const GemmParams& p, int g, int i0,
                 y[2 * w] = fmaf(p.cb, bf_lo(w4[w]), y[2 * w]);
                 y[2 * w + 1] = fmaf(p.cb, bf_hi(w4[w]), y[2 * w + 1]);
             }
+            if (whole) {
+                // the final values back into the staged slice, for the mirror
+                *reinterpret_cast<float4*>(st + r * 32 + (((2 * (lane & 3)) ^ (r & 7)) << 2)) =
+                    make_float4(y[0], y[1], y[2], y[3]);
+                *reinterpret_cast<float4*>(st + r * 32 + (((2 * (lane & 3) + 1) ^ (r & 7)) << 2)) =
+                    make_float4(y[4], y[5], y[6], y[7]);
+            }
         }
         const size_t off = (size_t)row * p.ld_s + col;
         if (col >= row && col + 8 <= N) {
@@ -406,11 +417,32 @@ __device__ __forceinline__ void sym_slice_st(const GemmParams& p, int g, int i0,
             for (int e = 0; e < 8; ++e)
                 if (col + e >= row && col + e < N) ob[off + e] = __float2bfloat16_rn(y[e]);
         }
-        // mirrors (strictly above the diagonal): for each e, the warp's lanes
-        // write 8 consecutive elements of 4 transposed rows
+        if (!whole) {
+            // mirrors (strictly above the diagonal): for each e, the warp's
+            // lanes write 8 consecutive elements of 4 transposed rows
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (col + e > row && col + e < N) ob[(size_t)(col + e) * p.ld_s + row] = __float2bfloat16_rn(y[e]);
+            for (int e = 0; e < 8; ++e)
+                if (col + e > row && col + e < N) ob[(size_t)(col + e) * p.ld_s + row] = __float2bfloat16_rn(y[e]);
+        }
+    }
+    if (whole) {
+        // pass k: this lane's column c = 8k + lane/4 of the slice and rows
+        // 8(lane%4)..+7, which are 8 consecutive elements of row j0 + c of the
+        // mirror (i0 is a multiple of 32, ld_s of 8: 16-byte aligned)
+        __syncwarp();
+        const int r0 = 8 * (lane & 3);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int c = 8 * k + (lane >> 2);
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int r = r0 + e;
+                y[e] = st[r * 32 + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3)];
+            }
+            *reinterpret_cast<uint4*>(ob + (size_t)(j0 + c) * p.ld_s + i0 + r0) =
+                pack_bf16x8(make_float4(y[0], y[1], y[2], y[3]), make_float4(y[4], y[5], y[6], y[7]));
+        }
     }
 }
 
