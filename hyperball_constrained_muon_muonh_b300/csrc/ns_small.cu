@@ -495,9 +495,9 @@ small_step_kernel(const __grid_constant__ SmallBatch b, const __grid_constant__ 
                 // While the last two iterations run on chip, pull into L2 this
                 // matrix's weight (read by the write-out) and the gradient and
                 // momentum of this cluster's next matrix (read by its load
-                // phase), so those phases read L2 instead of HBM.  (Issued at
-                // the last iteration alone, the copies were not all in L2 by
-                // the end of it: 0.920 against 0.915 ms for the batched 256^2.)
+                // phase), so those phases read L2 instead of HBM (two
+                // iterations ahead measured faster than one: 0.915 against
+                // 0.920 ms for 1024 matrices of 256 x 256).
                 if (rank == 1) {
                     prefetch_l2(D.w, (size_t)R * C * 4);
                 } else if (mi + (int)cluster_count() < b.n) {
