@@ -126,10 +126,13 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int local, int&
 // which keeps the epilogue's memory instructions, not only its bytes, few.
 // The staging tile is XOR-swizzled in 16-byte chunks (chunk c of row r sits
 // at c ^ (r & 7)), which keeps the row-per-lane writes and the reads free of
-// bank conflicts.  The mirror of a symmetric product is written from the same
-// lane layout, element by element.  Operands the epilogue reads (X for APPLY, A for POLY) are loaded one slice
-// ahead, as raw bits that are turned into values only where they are used,
-// so that the loads stay in flight while the previous slice is processed.
+// bank conflicts.  The mirror of a symmetric product is read back from the
+// staged slice by columns (8 consecutive rows of one column per lane, one
+// 16-byte store) where the slice lies wholly above the diagonal, and is
+// written element by element elsewhere.  Operands the epilogue reads (X for
+// APPLY, A for POLY) are loaded one slice ahead, as raw bits that are turned
+// into values only where they are used, so that the loads stay in flight
+// while the previous slice is processed.
 
 __device__ __forceinline__ void stage_rows(float* st, int lane, const float (&v)[32]) {
     __syncwarp();
