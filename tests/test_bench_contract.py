@@ -55,3 +55,22 @@ def test_mismatched_world_size_exits_nonzero():
                          timeout=600, env=env)
     assert out.returncode != 0
     assert "WORLD_SIZE=3" in out.stderr
+
+
+def test_l2_note_follows_the_workload():
+    # the timed steps do not flush L2: a line says whether its inputs exceed it
+    sys.path.insert(0, ROOT)
+    import bench
+    import muonh_workloads as wl
+    assert bench._l2_note(wl.qwen3_2b(), "muonh").startswith("inputs larger than L2")
+    assert bench._l2_note(wl.batched_256(), "muonh").startswith("inputs larger than L2")
+    assert bench._l2_note(wl.single_256x128(), "muonh").startswith("inputs fit in L2")
+
+
+def test_traffic_figure_names_its_workload():
+    # the roofline's DRAM traffic is reported only for the workload it was captured on
+    with open(os.path.join(ROOT, "profiles", "ns_gemm_traffic.json")) as f:
+        d = json.load(f)
+    assert d["workload"] == "qwen3_2b_28layers"
+    assert 1e9 < d["bytes_per_launch"] < 1e10
+    assert os.path.exists(os.path.join(ROOT, "profiles", d["source"].split(":")[0]))
